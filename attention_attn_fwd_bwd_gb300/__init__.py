@@ -1,1 +1,296 @@
-"""attnfuse-gb300: fused RoPE + variant attention for GB300 (sm_103a)."""
+"""attnfuse-gb300: fused RoPE + variant attention for NVIDIA GB300 (sm_103a).
+
+Thin Python binding over the C ABI declared in ``include/attnfuse.h`` (ctypes; argument
+marshalling only — every step of the computation runs in the library's CUDA kernels).
+PyTorch supplies device memory and streams. There is no CPU fallback: every call raises
+if ``libattnfuse.so`` is missing or fails to load.
+
+Low-level functions carry the C names (``attnfuse_fwd`` ...) and take raw pointers; the
+torch-level helpers ``fwd``, ``bwd``, ``decode`` and ``rope_prerotate`` allocate outputs and
+workspace with torch and call them on the current CUDA stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+__all__ = [
+    "ROPE_NONE", "ROPE_FUSED", "ROPE_PREROTATE", "MASK_FULL", "MASK_CAUSAL", "MASK_WINDOW",
+    "MASK_BLOCK_SPARSE", "BIAS_NONE", "BIAS_ALIBI", "BIAS_ADDITIVE", "AttnfuseError", "Variant",
+    "load", "library_path", "fwd", "bwd", "decode", "rope_prerotate", "device_status",
+    "fwd_workspace_size", "bwd_workspace_size", "decode_workspace_size",
+]
+
+ROPE_NONE, ROPE_FUSED, ROPE_PREROTATE = 0, 1, 2
+MASK_FULL, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK_SPARSE = 0, 1, 2, 3
+BIAS_NONE, BIAS_ALIBI, BIAS_ADDITIVE = 0, 1, 2
+_STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
+           4: "CUDA_ERROR", 5: "TIMEOUT"}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_lib", "libattnfuse.so")
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnfuseError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"attnfuse error {code} ({_STATUS.get(code, '?')}): {msg}")
+        self.code = code
+
+
+class CVariant(ctypes.Structure):
+    """Mirror of the C struct attnfuse_variant."""
+    _fields_ = [
+        ("mask", ctypes.c_int32),
+        ("causal", ctypes.c_int32),
+        ("window", ctypes.c_int32),
+        ("bs_block", ctypes.c_int32),
+        ("bs_row_ptr", ctypes.c_void_p),
+        ("bs_col_idx", ctypes.c_void_p),
+        ("bias", ctypes.c_int32),
+        ("add_bias_is_bf16", ctypes.c_int32),
+        ("alibi_slopes", ctypes.c_void_p),
+        ("add_bias", ctypes.c_void_p),
+        ("add_bias_strides", ctypes.c_int64 * 4),
+        ("tile_visits", ctypes.c_void_p),
+    ]
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def load():
+    """Load libattnfuse.so (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise AttnfuseError(4, f"{_LIB_PATH} not built; run __graft_entry__.build() or "
+                                   f"python -m attention_attn_fwd_bwd_gb300._build")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I, F, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        ST = ctypes.POINTER(ctypes.c_int64)
+        VP = ctypes.POINTER(CVariant)
+        sig = {
+            "attnfuse_last_error": ([], ctypes.c_char_p),
+            "attnfuse_version": ([], I),
+            "attnfuse_device_status": ([P, I, ctypes.POINTER(I)], I),
+            "attnfuse_fwd_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(S)], I),
+            "attnfuse_fwd": ([P, ST, P, ST, P, ST, P, ST, P, I, I, I, I, I, F, F, I, VP, P, S, P], I),
+            "attnfuse_bwd_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(S)], I),
+            "attnfuse_bwd": ([P, ST, P, ST, P, ST, P, ST, P, P, ST, P, ST, P, ST, P, ST,
+                              I, I, I, I, I, F, F, I, VP, P, S, P], I),
+            "attnfuse_decode_workspace_size": ([I, I, I, I, I, I, ctypes.POINTER(S)], I),
+            "attnfuse_decode": ([P, ST, P, ST, P, ST, P, ST, P, I, I, I, I, I, I, F, F, I, I,
+                                 P, S, P], I),
+            "attnfuse_decode_auto_splits": ([I, I, I, ctypes.POINTER(I)], I),
+            "attnfuse_rope_prerotate": ([P, ST, P, I, I, I, I, F, P, S, P], I),
+            "attnfuse_debug_wait_timeout": ([ctypes.c_uint64, P], I),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc):
+    if rc != 0:
+        raise AttnfuseError(rc, load().attnfuse_last_error().decode())
+
+
+def _strides(t, n):
+    arr = (ctypes.c_int64 * n)(*t.stride())
+    return arr
+
+
+def _stream(stream=None):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+# ------------------------------------------------------------------------------------------
+# C names (raw pointers)
+# ------------------------------------------------------------------------------------------
+def __getattr__(name):
+    if name.startswith("attnfuse_"):
+        return getattr(load(), name)
+    raise AttributeError(name)
+
+
+# ------------------------------------------------------------------------------------------
+# torch-level helpers
+# ------------------------------------------------------------------------------------------
+class Variant:
+    """Combinator set (paper §3.1). Tensors must live on the device of the attention inputs.
+
+    mask: MASK_*; causal: also require n <= m; window: W for MASK_WINDOW; bs_row_ptr /
+    bs_col_idx: int32 CSR block layout (block edge bs_block, 64 or 128); bias: BIAS_*;
+    alibi_slopes: fp32 [Hq]; add_bias: fp32 or bf16 tensor broadcastable to [B, Hq, N, N];
+    tile_visits: uint8 [B, Hq, ceil(N/128), ceil(N/128)] (debug record of computed tiles).
+    """
+
+    def __init__(self, mask=MASK_CAUSAL, causal=False, window=0, bs_block=64, bs_row_ptr=None,
+                 bs_col_idx=None, bias=BIAS_NONE, alibi_slopes=None, add_bias=None,
+                 tile_visits=None):
+        self.mask, self.causal, self.window, self.bs_block = mask, causal, window, bs_block
+        self.bs_row_ptr, self.bs_col_idx = bs_row_ptr, bs_col_idx
+        self.bias, self.alibi_slopes, self.add_bias = bias, alibi_slopes, add_bias
+        self.tile_visits = tile_visits
+
+    def c_struct(self):
+        v = CVariant()
+        v.mask, v.causal, v.window, v.bs_block = self.mask, int(bool(self.causal)), self.window, self.bs_block
+        if self.bs_row_ptr is not None:
+            v.bs_row_ptr, v.bs_col_idx = self.bs_row_ptr.data_ptr(), self.bs_col_idx.data_ptr()
+        v.bias = self.bias
+        if self.alibi_slopes is not None:
+            v.alibi_slopes = self.alibi_slopes.data_ptr()
+        if self.add_bias is not None:
+            import torch
+
+            ab = self.add_bias
+            while ab.dim() < 4:
+                ab = ab.unsqueeze(0)
+            v.add_bias = ab.data_ptr()
+            v.add_bias_is_bf16 = int(ab.dtype == torch.bfloat16)
+            for i in range(4):
+                v.add_bias_strides[i] = ab.stride(i) if ab.size(i) > 1 else 0
+        if self.tile_visits is not None:
+            v.tile_visits = self.tile_visits.data_ptr()
+        return v
+
+
+def fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode):
+    n = ctypes.c_size_t()
+    _check(load().attnfuse_fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, ctypes.byref(n)))
+    return n.value
+
+
+def bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode):
+    n = ctypes.c_size_t()
+    _check(load().attnfuse_bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, ctypes.byref(n)))
+    return n.value
+
+
+def decode_workspace_size(B, Hq, Hkv, L, d, num_splits):
+    n = ctypes.c_size_t()
+    _check(load().attnfuse_decode_workspace_size(B, Hq, Hkv, L, d, num_splits, ctypes.byref(n)))
+    return n.value
+
+
+def _workspace(nbytes, device, workspace=None):
+    import torch
+
+    if nbytes == 0:
+        return None
+    if workspace is not None and workspace.numel() * workspace.element_size() >= nbytes:
+        return workspace
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=None,
+        out=None, lse=None, with_lse=True, workspace=None, stream=None):
+    """Forward: q [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 CUDA tensors -> (out, lse)."""
+    import torch
+
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    ws_n = fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode)
+    ws = _workspace(ws_n, q.device, workspace)
+    cv = (variant or Variant()).c_struct()
+    _check(load().attnfuse_fwd(
+        _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
+        _ptr(out), _strides(out, 4), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+        float(rope_theta), rope_mode, ctypes.byref(cv), _ptr(ws), ws_n, _stream(stream)))
+    return out, lse
+
+
+def bwd(q, k, v, out, lse, dout, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED,
+        variant=None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward (paper §4.4): returns (dq, dk, dv) w.r.t. the un-rotated q, k and v."""
+    import torch
+
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = d ** -0.5
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    ws_n = bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode)
+    ws = _workspace(ws_n, q.device, workspace)
+    cv = (variant or Variant()).c_struct()
+    _check(load().attnfuse_bwd(
+        _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
+        _ptr(out), _strides(out, 4), _ptr(lse), _ptr(dout), _strides(dout, 4),
+        _ptr(dq), _strides(dq, 4), _ptr(dk), _strides(dk, 4), _ptr(dv), _strides(dv, 4),
+        B, Hq, Hkv, N, d, float(scale), float(rope_theta), rope_mode, ctypes.byref(cv),
+        _ptr(ws), ws_n, _stream(stream)))
+    return dq, dk, dv
+
+
+def decode(q, k_cache, v_cache, q_pos, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED,
+           num_splits=0, out=None, lse=None, with_lse=True, workspace=None, stream=None):
+    """Split-KV decode (paper §4.2): q [B,Hq,d], caches [B,Hkv,L,d] -> (out [B,Hq,d], lse)."""
+    import torch
+
+    B, Hq, d = q.shape
+    Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if with_lse and lse is None:
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    ws_n = decode_workspace_size(B, Hq, Hkv, L, d, num_splits)
+    ws = _workspace(ws_n, q.device, workspace)
+    _check(load().attnfuse_decode(
+        _ptr(q), _strides(q, 3), _ptr(k_cache), _strides(k_cache, 4), _ptr(v_cache),
+        _strides(v_cache, 4), _ptr(out), _strides(out, 3), _ptr(lse), B, Hq, Hkv, L, d,
+        int(q_pos), float(scale), float(rope_theta), rope_mode, int(num_splits), _ptr(ws), ws_n,
+        _stream(stream)))
+    return out, lse
+
+
+def decode_auto_splits(B, Hkv, L):
+    n = ctypes.c_int()
+    _check(load().attnfuse_decode_auto_splits(B, Hkv, L, ctypes.byref(n)))
+    return n.value
+
+
+def rope_prerotate(x, rope_theta, out=None, workspace=None, stream=None):
+    """x [B,H,N,d] bf16 -> R_n x (contiguous)."""
+    import torch
+
+    B, H, N, d = x.shape
+    out = torch.empty((B, H, N, d), dtype=x.dtype, device=x.device) if out is None else out
+    ws_n = fwd_workspace_size(B, H, H, N, d, ROPE_FUSED)
+    ws = _workspace(ws_n, x.device, workspace)
+    _check(load().attnfuse_rope_prerotate(_ptr(x), _strides(x, 4), _ptr(out), B, H, N, d,
+                                          float(rope_theta), _ptr(ws), ws_n, _stream(stream)))
+    return out
+
+
+def device_status(clear=True, stream=None):
+    """Synchronise and return the device status word (0 OK, 5 TIMEOUT)."""
+    code = ctypes.c_int()
+    _check(load().attnfuse_device_status(_stream(stream), int(clear), ctypes.byref(code)))
+    return code.value

@@ -1,0 +1,342 @@
+// C-ABI layer: argument validation, workspace carving, TMA descriptor encoding and launches.
+// Declarations and the meaning of every argument are in include/attnfuse.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/attnfuse.h"
+#include "launch.h"
+
+namespace afx {
+
+// Device status word: kernels write a non-zero code here when a bounded wait gives up.
+__device__ int g_status_word;
+
+namespace {
+
+thread_local std::string t_err;
+
+attnfuse_status fail(attnfuse_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+attnfuse_status ok() {
+  t_err.clear();
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ATTNFUSE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// ---------------------------------------------------------------------------------------------
+// Per-device state: status word address and the TMA descriptor encoder.
+// ---------------------------------------------------------------------------------------------
+constexpr int kMaxDevices = 64;
+int* g_status_ptr[kMaxDevices] = {};
+std::mutex g_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+attnfuse_status device_state(int** status) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(ATTNFUSE_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_status_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status)");
+    g_status_ptr[dev] = static_cast<int*>(ptr);
+  }
+  if (!g_encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+      return fail(ATTNFUSE_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  *status = g_status_ptr[dev];
+  return ATTNFUSE_OK;
+}
+
+// bf16 [B, H, N, d] view with element strides; box (64, 128, 1, 1), 128-byte swizzle.
+attnfuse_status encode_bhnd(CUtensorMap* m, const void* ptr, const int64_t st[4], int B, int H,
+                            int N, int d, const char* name) {
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
+  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "%s: tensor map encode failed (CUresult %d)", name,
+                (int)r);
+  return ATTNFUSE_OK;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Validation
+// ---------------------------------------------------------------------------------------------
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attnfuse_status check_tensor(const void* p, const int64_t st[4], const char* name) {
+  if (!p) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  if (!st) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s strides are NULL", name);
+  if (st[3] != 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s: innermost stride must be 1", name);
+  for (int i = 0; i < 3; ++i)
+    if (st[i] <= 0 || (st[i] % 8) != 0)
+      return fail(ATTNFUSE_ERR_INVALID_ARG,
+                  "%s: stride[%d] = %lld must be a positive multiple of 8 elements", name, i,
+                  (long long)st[i]);
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status check_shape(int B, int Hq, int Hkv, int N, int d) {
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || N <= 0)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "sizes must be positive (B=%d Hq=%d Hkv=%d N=%d)", B,
+                Hq, Hkv, N);
+  if (Hq % Hkv) return fail(ATTNFUSE_ERR_UNSUPPORTED, "Hq=%d not a multiple of Hkv=%d", Hq, Hkv);
+  if (d != 64 && d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "head dim %d (need 64 or 128)", d);
+  return ATTNFUSE_OK;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t rope_table_bytes(int N, int d) { return align_up((size_t)N * (d / 2) * sizeof(float2), 256); }
+
+RopeFreqs make_freqs(int d, float theta) {
+  RopeFreqs f;
+  memset(&f, 0, sizeof(f));
+  const double two_pi = 6.283185307179586476925286766559;
+  for (int i = 0; i < d / 2; ++i) {
+    const double turns = std::pow((double)theta, -2.0 * i / d) / two_pi;
+    f.hi[i] = (float)turns;
+    f.lo[i] = (float)(turns - (double)f.hi[i]);
+  }
+  return f;
+}
+
+attnfuse_status to_dev_variant(const attnfuse_variant* v, int N, int Hq, VariantDev* out) {
+  memset(out, 0, sizeof(*out));
+  if (!v) {
+    out->mask = ATTNFUSE_MASK_CAUSAL;
+    out->causal = 1;
+    return ATTNFUSE_OK;
+  }
+  if (v->mask < 0 || v->mask > 3) return fail(ATTNFUSE_ERR_INVALID_ARG, "mask kind %d", v->mask);
+  out->mask = v->mask;
+  out->causal = (v->mask == ATTNFUSE_MASK_CAUSAL || v->causal) ? 1 : 0;
+  if (v->mask == ATTNFUSE_MASK_WINDOW) {
+    if (v->window < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "window %d < 1", v->window);
+    out->window = v->window;
+  }
+  if (v->mask == ATTNFUSE_MASK_BLOCK_SPARSE) {
+    if (v->bs_block != 64 && v->bs_block != 128)
+      return fail(ATTNFUSE_ERR_UNSUPPORTED, "block-sparse block %d (need 64 or 128)", v->bs_block);
+    if (N > kBsMaxN)
+      return fail(ATTNFUSE_ERR_UNSUPPORTED, "block-sparse needs N <= %d", kBsMaxN);
+    if (!v->bs_row_ptr || !v->bs_col_idx)
+      return fail(ATTNFUSE_ERR_INVALID_ARG, "block-sparse CSR pointers are NULL");
+    out->bs_block = v->bs_block;
+    out->bs_row_ptr = v->bs_row_ptr;
+    out->bs_col_idx = v->bs_col_idx;
+  }
+  if (v->bias < 0 || v->bias > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "bias kind %d", v->bias);
+  out->bias = v->bias;
+  if (v->bias == ATTNFUSE_BIAS_ALIBI) {
+    if (!v->alibi_slopes) return fail(ATTNFUSE_ERR_INVALID_ARG, "ALiBi slopes are NULL");
+    out->slopes = v->alibi_slopes;
+  }
+  if (v->bias == ATTNFUSE_BIAS_ADDITIVE) {
+    if (!v->add_bias) return fail(ATTNFUSE_ERR_INVALID_ARG, "additive bias is NULL");
+    out->add_bias = v->add_bias;
+    out->add_bias_bf16 = v->add_bias_is_bf16 ? 1 : 0;
+    for (int i = 0; i < 4; ++i) {
+      if (v->add_bias_strides[i] < 0)
+        return fail(ATTNFUSE_ERR_INVALID_ARG, "negative additive-bias stride");
+      out->ab_s[i] = v->add_bias_strides[i];
+    }
+  }
+  out->visits = v->tile_visits;
+  (void)Hq;
+  return ATTNFUSE_OK;
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
+
+}  // namespace afx
+
+using namespace afx;
+
+extern "C" {
+
+const char* attnfuse_last_error(void) { return t_err.c_str(); }
+
+int attnfuse_version(void) { return 100; }
+
+attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code) {
+  if (!code) return fail(ATTNFUSE_ERR_INVALID_ARG, "code is NULL");
+  int* st = nullptr;
+  attnfuse_status rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpy(&v, st, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (clear && v) {
+    const int zero = 0;
+    e = cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+  }
+  *code = v ? ATTNFUSE_ERR_TIMEOUT : ATTNFUSE_OK;
+  return ok();
+}
+
+attnfuse_status attnfuse_fwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                            attnfuse_rope_mode rope_mode, size_t* bytes) {
+  if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  size_t n = 0;
+  if (rope_mode == ATTNFUSE_ROPE_FUSED || rope_mode == ATTNFUSE_ROPE_PREROTATE)
+    n += rope_table_bytes(N, d);
+  if (rope_mode == ATTNFUSE_ROPE_PREROTATE) {
+    n += align_up((size_t)B * Hq * N * d * 2, 256);
+    n += align_up((size_t)B * Hkv * N * d * 2, 256);
+  }
+  if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
+  *bytes = n;
+  return ok();
+}
+
+attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4], void* out,
+                                        int B, int H, int N, int d, float rope_theta,
+                                        void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+  attnfuse_status rc = check_shape(B, H, H, N, d);
+  if (rc) return rc;
+  if ((rc = check_tensor(x, x_strides, "x"))) return rc;
+  if (!out || !aligned16(out)) return fail(ATTNFUSE_ERR_INVALID_ARG, "out NULL or misaligned");
+  if (!(rope_theta > 0.f) || !std::isfinite(rope_theta))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
+  const size_t need = rope_table_bytes(N, d);
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes", need);
+  int* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  float2* cs = static_cast<float2*>(workspace);
+  cudaError_t e = launch_rope_table(cs, N, d / 2, make_freqs(d, rope_theta), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
+  return ok();
+}
+
+attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const void* k,
+                             const int64_t k_strides[4], const void* v,
+                             const int64_t v_strides[4], void* out, const int64_t o_strides[4],
+                             float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                             float rope_theta, attnfuse_rope_mode rope_mode,
+                             const attnfuse_variant* variant, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  if ((rc = check_tensor(q, q_strides, "q"))) return rc;
+  if ((rc = check_tensor(k, k_strides, "k"))) return rc;
+  if ((rc = check_tensor(v, v_strides, "v"))) return rc;
+  if ((rc = check_tensor(out, o_strides, "out"))) return rc;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "lse is not 4-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
+  if (rope_mode != ATTNFUSE_ROPE_NONE && (!(rope_theta > 0.f) || !std::isfinite(rope_theta)))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if ((rc = to_dev_variant(variant, N, Hq, &p.var))) return rc;
+  size_t need = 0;
+  if ((rc = attnfuse_fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, &need))) return rc;
+  if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need,
+                workspace_bytes);
+  int* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+
+  const void* qa = q;
+  const void* ka = k;
+  const int64_t* qs = q_strides;
+  const int64_t* ks = k_strides;
+  int64_t qs_c[4], ks_c[4];
+  float2* cs = nullptr;
+  if (rope_mode != ATTNFUSE_ROPE_NONE) {
+    cs = static_cast<float2*>(workspace);
+    cudaError_t e = launch_rope_table(cs, N, d / 2, make_freqs(d, rope_theta), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+  }
+  if (rope_mode == ATTNFUSE_ROPE_PREROTATE) {
+    uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
+    void* qr = base;
+    void* kr = base + align_up((size_t)B * Hq * N * d * 2, 256);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, stream);
+    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
+    qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
+    ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
+    qa = qr; ka = kr; qs = qs_c; ks = ks_c;
+  }
+  if ((rc = encode_bhnd(&p.tmQ, qa, qs, B, Hq, N, d, "q"))) return rc;
+  if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k"))) return rc;
+  if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v"))) return rc;
+  p.rope_cs = cs;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.o_sb = o_strides[0]; p.o_sh = o_strides[1]; p.o_sn = o_strides[2];
+  p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv;
+  const int TQ = (N + 127) / 128;
+  p.pair_heads = (p.g % 2 == 0) ? 1 : 0;
+  p.num_t = p.pair_heads ? TQ : (TQ + 1) / 2;
+  p.pairs = p.pair_heads ? Hq / 2 : Hq;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = st;
+  const int64_t grid = (int64_t)p.num_t * B * p.pairs;
+  if (grid > 0x7fffffff) return fail(ATTNFUSE_ERR_UNSUPPORTED, "problem too large (grid %lld)", (long long)grid);
+  const int rk = rope_mode == ATTNFUSE_ROPE_FUSED ? kRopeFused
+                 : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
+  cudaError_t e = launch_fwd(p, d, rk, (int)grid, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ok();
+}
+
+attnfuse_status attnfuse_debug_wait_timeout(uint64_t limit_ns, cudaStream_t stream) {
+  int* st = nullptr;
+  attnfuse_status rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = launch_wait_timeout(limit_ns, st, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "wait-timeout launch");
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,38 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace afx {
+
+struct FwdParams {
+  CUtensorMap tmQ, tmK, tmV;  // bf16 [B, H, N, d] maps, 128B swizzle, box (64, 128, 1, 1)
+  const float2* rope_cs;      // (cos, sin) table [N][d/2] (fused RoPE only)
+  __nv_bfloat16* out;
+  int64_t o_sb, o_sh, o_sn;
+  float* lse;                 // [B, Hq, N] or null
+  int B, Hq, Hkv, N, g;
+  int pair_heads;             // 1: sub-tiles are heads (2p, 2p+1) at one q tile; 0: tiles (2t, 2t+1)
+  int num_t;                  // q tiles (pair_heads) or q-tile pairs
+  int pairs;                  // head pairs (Hq/2) or heads (Hq)
+  float scale_log2;           // scale * log2(e)
+  VariantDev var;
+  int* status;
+};
+
+size_t fwd_smem_size(int d);
+// rope_kind: how the score operands were produced.
+constexpr int kRopeNone = 0;        // bf16 inputs used as they are
+constexpr int kRopeFused = 1;       // rotated in shared memory by the kernel, rounded to fp16
+constexpr int kRopePrerotated = 2;  // rotated by the pre-rotation kernel into fp16 buffers
+cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream);
+cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
+                              cudaStream_t stream);
+cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
+                             int N, int d, const float2* cs, bool out_f16, cudaStream_t stream);
+cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
+
+}  // namespace afx

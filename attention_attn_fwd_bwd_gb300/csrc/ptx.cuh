@@ -1,0 +1,288 @@
+// Inline-PTX layer for sm_103a: mbarrier, TMA (cp.async.bulk.tensor), tcgen05 MMA and
+// tensor memory (TMEM), shared-memory matrix descriptors and small math helpers.
+//
+// Everything here is written from the public PTX ISA description of these instructions.
+// Every wait loop is bounded: when the bound is hit the helper records an error code in the
+// kernel's device status word and returns false, so callers can unwind instead of hanging.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+
+namespace afx {
+
+// ---------------------------------------------------------------------------------------------
+// Device status word (one per process, in the library module). Non-zero = a kernel gave up.
+// ---------------------------------------------------------------------------------------------
+enum : int {
+  kDevOk = 0,
+  kDevTimeout = 1,
+};
+
+// Wall-clock limit for any single wait, in nanoseconds (globaltimer). Generous: a legitimate
+// wait inside one CTA is microseconds.
+#ifndef ATTNFUSE_WAIT_LIMIT_NS
+#define ATTNFUSE_WAIT_LIMIT_NS 2000000000ull
+#endif
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ---------------------------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar_addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete. Returns false on timeout
+// (and records kDevTimeout in *status); also returns false immediately if *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort_flag) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait(a, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    if (mbar_try_wait(a, parity)) return true;
+    if ((++spins & 255u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
+        if (status) atomicExch(status, kDevTimeout);
+        if (abort_flag) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Proxy fences / named barriers
+// ---------------------------------------------------------------------------------------------
+// Make generic-proxy writes to shared memory visible to the async proxy (TMA, tcgen05.mma).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// TMA (tiled tensor copies, no multicast)
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_4d(void* dst, const void* tmap, uint64_t* bar, int c0,
+                                            int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2),
+      "r"(c3)
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------------------------
+// tcgen05: TMEM allocation, MMA, commit, loads/stores
+// ---------------------------------------------------------------------------------------------
+// Executed by one full warp. Writes the TMEM base address to *dst (shared memory).
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem desc]
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive once on *bar when all previously issued tcgen05.mma of this thread have completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bits, 16 consecutive columns: thread i of the warp gets lane (base+i).
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+// 32 lanes x 32 bits, 32 consecutive columns into r[OFF .. OFF+31] (compile-time offset so the
+// destination stays in registers).
+template <int OFF = 0, int TOT>
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[TOT]) {
+  static_assert(OFF + 32 <= TOT, "tmem_ld32 range");
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[OFF + 0]),"=r"(r[OFF + 1]),"=r"(r[OFF + 2]),"=r"(r[OFF + 3]),"=r"(r[OFF + 4]),"=r"(r[OFF + 5]),"=r"(r[OFF + 6]),"=r"(r[OFF + 7]),"=r"(r[OFF + 8]),"=r"(r[OFF + 9]),"=r"(r[OFF + 10]),"=r"(r[OFF + 11]),"=r"(r[OFF + 12]),"=r"(r[OFF + 13]),"=r"(r[OFF + 14]),"=r"(r[OFF + 15]),"=r"(r[OFF + 16]),"=r"(r[OFF + 17]),"=r"(r[OFF + 18]),"=r"(r[OFF + 19]),"=r"(r[OFF + 20]),"=r"(r[OFF + 21]),"=r"(r[OFF + 22]),"=r"(r[OFF + 23]),"=r"(r[OFF + 24]),"=r"(r[OFF + 25]),"=r"(r[OFF + 26]),"=r"(r[OFF + 27]),"=r"(r[OFF + 28]),"=r"(r[OFF + 29]),"=r"(r[OFF + 30]),"=r"(r[OFF + 31])
+      : "r"(taddr));
+}
+
+template <int OFF = 0, int TOT>
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[TOT]) {
+  static_assert(OFF + 32 <= TOT, "tmem_st32 range");
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+      :: "r"(taddr), "r"(r[OFF + 0]),"r"(r[OFF + 1]),"r"(r[OFF + 2]),"r"(r[OFF + 3]),"r"(r[OFF + 4]),"r"(r[OFF + 5]),"r"(r[OFF + 6]),"r"(r[OFF + 7]),"r"(r[OFF + 8]),"r"(r[OFF + 9]),"r"(r[OFF + 10]),"r"(r[OFF + 11]),"r"(r[OFF + 12]),"r"(r[OFF + 13]),"r"(r[OFF + 14]),"r"(r[OFF + 15]),"r"(r[OFF + 16]),"r"(r[OFF + 17]),"r"(r[OFF + 18]),"r"(r[OFF + 19]),"r"(r[OFF + 20]),"r"(r[OFF + 21]),"r"(r[OFF + 22]),"r"(r[OFF + 23]),"r"(r[OFF + 24]),"r"(r[OFF + 25]),"r"(r[OFF + 26]),"r"(r[OFF + 27]),"r"(r[OFF + 28]),"r"(r[OFF + 29]),"r"(r[OFF + 30]),"r"(r[OFF + 31])
+      : "memory");
+}
+
+// TMEM address of (lane, column) relative to an allocation base.
+__device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
+  return base + (lane << 16) + col;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Descriptors
+// ---------------------------------------------------------------------------------------------
+// Shared-memory matrix descriptor, 128-byte swizzle, for tiles whose rows are 128 bytes
+// (64 bf16) and whose 8-row swizzle atoms are 1024 bytes apart.
+//   K-major operand: rows = M/N index, 64 K-elements per row; lbo unused, sbo = 1024.
+//   MN-major operand: rows = K index, 64 MN-elements per row; lbo = byte distance between
+//                     64-element MN panels, sbo = 1024 (next 8 K-rows).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
+                                                    uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version for tcgen05
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with fp32 accumulation. A and B share one element type:
+// bf16 (f16 = 0) or fp16 (f16 = 1). a_mn / b_mn: 1 when that operand is MN-major
+// ("transposed"), 0 when K-major.
+__host__ __device__ constexpr uint32_t idesc_f32acc(uint32_t M, uint32_t N, uint32_t a_mn,
+                                                    uint32_t b_mn, uint32_t f16 = 0) {
+  return (1u << 4)                  // D = f32
+         | ((f16 ? 0u : 1u) << 7)   // A = f16 (0) or bf16 (1)
+         | ((f16 ? 0u : 1u) << 10)  // B = f16 (0) or bf16 (1)
+         | (a_mn << 15)             // A major
+         | (b_mn << 16)             // B major
+         | ((N >> 3) << 17)         // N / 8
+         | ((M >> 4) << 24);        // M / 16
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, uint32_t a_mn,
+                                                      uint32_t b_mn) {
+  return idesc_f32acc(M, N, a_mn, b_mn, 0);
+}
+
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled tile whose
+// base is 1024-byte aligned and whose rows are 128 bytes apart.
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
+  return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Math helpers
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Round two floats to fp16, saturating to the largest finite value instead of overflowing.
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(uint32_t w) {
+  return __uint_as_float(w & 0xFFFF0000u);
+}
+
+}  // namespace afx

@@ -1,0 +1,186 @@
+/*
+ * attnfuse — fused RoPE + variant attention for NVIDIA GB300 (sm_103a). C ABI.
+ *
+ * The operation is the one described in "AttnFuse: A Composable DSL for Compiling Attentions
+ * to Fused GPU Kernels" (arXiv 2609.13612): rotary position embedding applied to Q and K tiles
+ * on-chip (§4.1, NeoX half-split pairs (i, i+d/2)), score combinators applied to score tiles
+ * (§3.1: scaled_dot_product, causal, sliding_window, full, block_sparse, alibi, additive_bias,
+ * softmax), an online-softmax accumulation into O and the per-row log-sum-exp (§2, §4.4), the
+ * three-kernel backward (§4.4), and split-KV decoding (§4.2).
+ *
+ * Definitions used by every call (0-based positions; query row m sits at position m, key n at
+ * position n; decode query at q_pos):
+ *   theta_i   = rope_theta^(-2i/d), i < d/2;  R_p rotates pair (x_i, x_{i+d/2}) by p*theta_i
+ *   s_mn      = scale * <R_m q_m, R_n k_n>  [+ slope_h * (n - m)]  [+ bias(b, h, m, n)]
+ *   allowed   = FULL: all; CAUSAL: n <= m; WINDOW: |m - n| < W (and n <= m if causal);
+ *               BLOCK_SPARSE: (m / blk, n / blk) in the CSR layout (and n <= m if causal)
+ *   LSE_m     = ln sum_{allowed n} exp(s_mn)        (natural log; -inf if no n is allowed)
+ *   O_m       = sum_{allowed n} exp(s_mn - LSE_m) v_n              (0 if no n is allowed)
+ *   GQA: query head h reads key/value head h / (Hq / Hkv).
+ *
+ * Conventions:
+ *   - Every function returns an attnfuse_status and never throws or exits. On error,
+ *     attnfuse_last_error() returns a thread-local message.
+ *   - Every launch is asynchronous on the caller's stream. The library never allocates or
+ *     frees device memory: the caller owns every pointer, including the workspace, whose size
+ *     the *_workspace_size functions report.
+ *   - Q, K, V, O, dO, dQ, dK, dV are bf16 with element strides (b, h, n, c); the last stride
+ *     must be 1, the other strides multiples of 8 elements, pointers 16-byte aligned.
+ *   - LSE tensors are fp32 contiguous [B, Hq, N] (decode: [B, Hq]).
+ *   - Supported head dims: d in {64, 128}. Hq % Hkv == 0.
+ *   - Kernels give up on any internal wait after a bounded time instead of hanging; the
+ *     device status word then reads ATTNFUSE_ERR_TIMEOUT (see attnfuse_device_status).
+ */
+#ifndef ATTNFUSE_H_
+#define ATTNFUSE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int attnfuse_status;
+#define ATTNFUSE_OK 0
+#define ATTNFUSE_ERR_INVALID_ARG 1
+#define ATTNFUSE_ERR_UNSUPPORTED 2
+#define ATTNFUSE_ERR_WORKSPACE_TOO_SMALL 3
+#define ATTNFUSE_ERR_CUDA 4
+#define ATTNFUSE_ERR_TIMEOUT 5
+
+/* Where RoPE is applied (paper §4.1 "Fused RoPE" vs. the pre-rotation of Fig. 1a / §5.3).
+ * In both rotating modes the rotation runs in fp32 and the rotated Q', K' are rounded to fp16
+ * (not bf16) before the score MMA: fp16 keeps 3 more mantissa bits, which keeps the LSE within
+ * 1e-3 of the exact value. fp16 saturates at +-65504, so these modes need |q|, |k| < 46000
+ * (a rotation can grow one component by sqrt(2)). ROPE_NONE feeds bf16 inputs unchanged. */
+typedef enum {
+  ATTNFUSE_ROPE_NONE = 0,      /* no rotation: plain scaled_dot_product */
+  ATTNFUSE_ROPE_FUSED = 1,     /* rotate the Q tile once and each K tile in shared memory */
+  ATTNFUSE_ROPE_PREROTATE = 2  /* separate rotate kernel writes Q', K' to the workspace, then
+                                  attention runs without rotation (the paper's baseline) */
+} attnfuse_rope_mode;
+
+/* Mask combinators (paper §3.1 causal / sliding_window / full / block_sparse). */
+typedef enum {
+  ATTNFUSE_MASK_FULL = 0,
+  ATTNFUSE_MASK_CAUSAL = 1,
+  ATTNFUSE_MASK_WINDOW = 2,
+  ATTNFUSE_MASK_BLOCK_SPARSE = 3
+} attnfuse_mask_kind;
+
+/* Bias combinators (paper §3.1 alibi / additive_bias). */
+typedef enum {
+  ATTNFUSE_BIAS_NONE = 0,
+  ATTNFUSE_BIAS_ALIBI = 1,
+  ATTNFUSE_BIAS_ADDITIVE = 2
+} attnfuse_bias_kind;
+
+/* A variant: one mask combinator, an optional causal restriction and one bias combinator.
+ * All pointers are device pointers owned by the caller; unused fields are ignored. */
+typedef struct {
+  int32_t mask;                /* attnfuse_mask_kind */
+  int32_t causal;              /* non-zero: also require n <= m (WINDOW, BLOCK_SPARSE, FULL) */
+  int32_t window;              /* W >= 1 for ATTNFUSE_MASK_WINDOW */
+  int32_t bs_block;            /* block edge for BLOCK_SPARSE: 64 or 128 */
+  const int32_t* bs_row_ptr;   /* CSR block layout (paper §4.3 BlockMask): [ceil(N/blk) + 1] */
+  const int32_t* bs_col_idx;   /* active block columns per block row, any order, no repeats */
+  int32_t bias;                /* attnfuse_bias_kind */
+  int32_t add_bias_is_bf16;    /* additive bias element type: 1 = bf16, 0 = fp32 */
+  const float* alibi_slopes;   /* [Hq] fp32, required for ATTNFUSE_BIAS_ALIBI */
+  const void* add_bias;        /* additive bias, element (b, h, m, n) at add_bias_strides */
+  int64_t add_bias_strides[4]; /* element strides; 0 broadcasts that dimension */
+  uint8_t* tile_visits;        /* debug, nullable: [B, Hq, ceil(N/128), ceil(N/128)] bytes; the
+                                  forward writes 1 for every (q-tile, kv-tile) it computes.
+                                  The caller zeroes it first. */
+} attnfuse_variant;
+
+/* Last error message of this thread (empty string if none). */
+const char* attnfuse_last_error(void);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int attnfuse_version(void);
+
+/* Synchronise `stream`, then read (and if `clear`, reset) the device status word of the
+ * current device: ATTNFUSE_OK, or ATTNFUSE_ERR_TIMEOUT if a kernel gave up waiting. */
+attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code);
+
+/* ------------------------------------------------------------------------------------------
+ * Forward (paper §4.1 fused RoPE, §2 online softmax, §3.1 combinators, §4.3 block skipping).
+ * q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; out: [B, Hq, N, d]; lse: [B, Hq, N] or NULL.
+ * variant: NULL means causal with no bias. Fully masked (q-tile, kv-tile) pairs are skipped.
+ * ------------------------------------------------------------------------------------------ */
+attnfuse_status attnfuse_fwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                            attnfuse_rope_mode rope_mode, size_t* bytes);
+
+attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const void* k,
+                             const int64_t k_strides[4], const void* v,
+                             const int64_t v_strides[4], void* out, const int64_t o_strides[4],
+                             float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                             float rope_theta, attnfuse_rope_mode rope_mode,
+                             const attnfuse_variant* variant, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Backward (paper §4.4): preprocess D = rowsum(dO * O), a dK/dV kernel and a dQ kernel, no
+ * atomics. Gradients are with respect to the un-rotated q and k (the inverse rotation is
+ * applied in the epilogues) and dk, dv are summed over each GQA group.
+ * out and lse are the forward's outputs. Supported variants: FULL or CAUSAL mask, no bias.
+ * ------------------------------------------------------------------------------------------ */
+attnfuse_status attnfuse_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                            attnfuse_rope_mode rope_mode, size_t* bytes);
+
+attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const void* k,
+                             const int64_t k_strides[4], const void* v,
+                             const int64_t v_strides[4], const void* out,
+                             const int64_t o_strides[4], const float* lse, const void* dout,
+                             const int64_t do_strides[4], void* dq, const int64_t dq_strides[4],
+                             void* dk, const int64_t dk_strides[4], void* dv,
+                             const int64_t dv_strides[4], int B, int Hq, int Hkv, int N, int d,
+                             float scale, float rope_theta, attnfuse_rope_mode rope_mode,
+                             const attnfuse_variant* variant, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Split-KV decode (paper §4.2): one query row per (b, h) at position q_pos against a cache of
+ * L keys stored already rotated. Phase 1 computes partial (max, sum, acc) per KV chunk, phase
+ * 2 merges the chunks through their log-sum-exp. rope_mode applies to q only (NONE or FUSED).
+ * q: [B, Hq, d] (strides b, h, c); k_cache, v_cache: [B, Hkv, L, d]; out: [B, Hq, d];
+ * lse: [B, Hq] or NULL. num_splits: number of KV chunks per (b, kv-head), 0 = automatic.
+ * Requires Hq / Hkv <= 16.
+ * ------------------------------------------------------------------------------------------ */
+attnfuse_status attnfuse_decode_workspace_size(int B, int Hq, int Hkv, int L, int d,
+                                               int num_splits, size_t* bytes);
+
+attnfuse_status attnfuse_decode(const void* q, const int64_t q_strides[3], const void* k_cache,
+                                const int64_t k_strides[4], const void* v_cache,
+                                const int64_t v_strides[4], void* out,
+                                const int64_t o_strides[3], float* lse, int B, int Hq, int Hkv,
+                                int L, int d, int q_pos, float scale, float rope_theta,
+                                attnfuse_rope_mode rope_mode, int num_splits, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/* Number of KV chunks attnfuse_decode uses for num_splits = 0 on the current device. */
+attnfuse_status attnfuse_decode_auto_splits(int B, int Hkv, int L, int* num_splits);
+
+/* ------------------------------------------------------------------------------------------
+ * Pre-rotation alone (paper Fig. 1a / §5.3 T_pre): x_rot = R_n x for x of shape [B, H, N, d]
+ * (row n at position n), written contiguously to `out`. Used by ATTNFUSE_ROPE_PREROTATE and
+ * exposed for the fused-vs-pre-rotated crossover measurement. workspace holds the cos/sin
+ * table: attnfuse_fwd_workspace_size(.., ATTNFUSE_ROPE_FUSED, ..) bytes.
+ * ------------------------------------------------------------------------------------------ */
+attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4], void* out,
+                                        int B, int H, int N, int d, float rope_theta,
+                                        void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream);
+
+/* Debug: launch one kernel whose only wait can never complete, bounded by `limit_ns`
+ * nanoseconds. The kernel then records ATTNFUSE_ERR_TIMEOUT in the device status word and
+ * returns, leaving the context usable. Exercises the timeout path without faulting. */
+attnfuse_status attnfuse_debug_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* ATTNFUSE_H_ */

@@ -1,0 +1,52 @@
+"""Shared test helpers: tolerances and comparisons against the fp64 oracle.
+
+Tolerances (the target's stated bar): bf16 outputs within max-abs 2e-2 and mean-abs 2e-3 of
+the oracle; LSE within 1e-3 relative (|d| <= 1e-3 * max(1, |ref|)); gradients within
+5e-2 * max|ref grad| per tensor; tile-visit sets bit-exact.
+"""
+import numpy as np
+import torch
+
+O_MAX_ABS = 2e-2
+O_MEAN_ABS = 2e-3
+LSE_REL = 1e-3
+GRAD_REL_MAX = 5e-2
+
+
+def f64(t):
+    if isinstance(t, torch.Tensor):
+        return t.detach().to("cpu", torch.float64).numpy()
+    return np.asarray(t, np.float64)
+
+
+def check_out(got, ref, what="O"):
+    got, ref = f64(got), f64(ref)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    assert err.max() <= O_MAX_ABS, f"{what}: max-abs err {err.max():.3e} > {O_MAX_ABS}"
+    assert err.mean() <= O_MEAN_ABS, f"{what}: mean-abs err {err.mean():.3e} > {O_MEAN_ABS}"
+    return err.max(), err.mean()
+
+
+def check_lse(got, ref, what="LSE"):
+    got, ref = f64(got), f64(ref)
+    assert got.shape == ref.shape
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isfinite(got), fin), f"{what}: -inf pattern differs"
+    assert np.all(got[~fin] == ref[~fin]), f"{what}: masked rows must be -inf"
+    if fin.any():
+        err = np.abs(got[fin] - ref[fin]) / np.maximum(1.0, np.abs(ref[fin]))
+        assert err.max() <= LSE_REL, f"{what}: rel err {err.max():.3e} > {LSE_REL}"
+        return err.max()
+    return 0.0
+
+
+def check_grad(got, ref, what):
+    got, ref = f64(got), f64(ref)
+    assert got.shape == ref.shape
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    scale = max(np.abs(ref).max(), 1e-30)
+    err = np.abs(got - ref).max()
+    assert err <= GRAD_REL_MAX * scale, f"{what}: max err {err:.3e} > {GRAD_REL_MAX} * {scale:.3e}"
+    return err / scale
