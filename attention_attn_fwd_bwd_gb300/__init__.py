@@ -23,6 +23,7 @@ __all__ = [
 ]
 
 ROPE_NONE, ROPE_FUSED, ROPE_PREROTATE = 0, 1, 2
+ROPE_REUSE_TABLE = 0x100
 MASK_FULL, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK_SPARSE = 0, 1, 2, 3
 BIAS_NONE, BIAS_ALIBI, BIAS_ADDITIVE = 0, 1, 2
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
@@ -90,6 +91,7 @@ def load():
             "attnfuse_decode_auto_splits": ([I, I, I, ctypes.POINTER(I)], I),
             "attnfuse_rope_prerotate": ([P, ST, P, I, I, I, I, F, P, S, P], I),
             "attnfuse_debug_wait_timeout": ([ctypes.c_uint64, P], I),
+            "attnfuse_rope_table": ([P, S, I, I, F, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -213,7 +215,7 @@ def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=N
         out = torch.empty_like(q)
     if with_lse and lse is None:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
-    ws_n = fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode)
+    ws_n = fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode & 0xFF)
     ws = _workspace(ws_n, q.device, workspace)
     cv = (variant or Variant()).c_struct()
     _check(load().attnfuse_fwd(

@@ -121,7 +121,12 @@ attnfuse_status check_shape(int B, int Hq, int Hkv, int N, int d) {
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t rope_table_bytes(int N, int d) { return align_up((size_t)N * (d / 2) * sizeof(float2), 256); }
+// The table always covers at least 128 positions: the fused key rotation reads the entry of
+// position 128 / (d / 16) as its per-row step.
+int rope_table_rows(int N) { return N < 128 ? 128 : N; }
+size_t rope_table_bytes(int N, int d) {
+  return align_up((size_t)rope_table_rows(N) * (d / 2) * sizeof(float2), 256);
+}
 
 RopeFreqs make_freqs(int d, float theta) {
   RopeFreqs f;
@@ -247,9 +252,9 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
   int* st = nullptr;
   if ((rc = device_state(&st))) return rc;
   float2* cs = static_cast<float2*>(workspace);
-  cudaError_t e = launch_rope_table(cs, N, d / 2, make_freqs(d, rope_theta), stream);
+  cudaError_t e = launch_rope_table(cs, rope_table_rows(N), d / 2, make_freqs(d, rope_theta), stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
-  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, stream);
+  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, false, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
   return ok();
 }
@@ -261,6 +266,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
                              float rope_theta, attnfuse_rope_mode rope_mode,
                              const attnfuse_variant* variant, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
+  const bool reuse_table = (rope_mode & ATTNFUSE_ROPE_REUSE_TABLE) != 0;
+  rope_mode = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
   attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
   if (rc) return rc;
   if ((rc = check_tensor(q, q_strides, "q"))) return rc;
@@ -293,15 +300,18 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   float2* cs = nullptr;
   if (rope_mode != ATTNFUSE_ROPE_NONE) {
     cs = static_cast<float2*>(workspace);
-    cudaError_t e = launch_rope_table(cs, N, d / 2, make_freqs(d, rope_theta), stream);
-    if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+    if (!reuse_table) {
+      cudaError_t e =
+          launch_rope_table(cs, rope_table_rows(N), d / 2, make_freqs(d, rope_theta), stream);
+      if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+    }
   }
   if (rope_mode == ATTNFUSE_ROPE_PREROTATE) {
     uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
     void* qr = base;
     void* kr = base + align_up((size_t)B * Hq * N * d * 2, 256);
-    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, stream);
-    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, stream);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, false, stream);
+    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, true, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
     qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
@@ -327,6 +337,23 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
                  : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
   cudaError_t e = launch_fwd(p, d, rk, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ok();
+}
+
+attnfuse_status attnfuse_rope_table(void* table, size_t table_bytes, int N, int d,
+                                    float rope_theta, cudaStream_t stream) {
+  if (N <= 0 || (d != 64 && d != 128))
+    return fail(ATTNFUSE_ERR_UNSUPPORTED, "rope table for N=%d d=%d", N, d);
+  if (!(rope_theta > 0.f) || !std::isfinite(rope_theta))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (!table || !aligned16(table) || table_bytes < rope_table_bytes(N, d))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "table needs %zu bytes", rope_table_bytes(N, d));
+  int* st = nullptr;
+  attnfuse_status rc = device_state(&st);
+  if (rc) return rc;
+  cudaError_t e = launch_rope_table(static_cast<float2*>(table), rope_table_rows(N), d / 2,
+                                    make_freqs(d, rope_theta), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
   return ok();
 }
 

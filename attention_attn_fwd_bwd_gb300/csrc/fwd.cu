@@ -3,12 +3,14 @@
 //
 // One CTA computes two 128-row query sub-tiles that read the same key/value head: either two
 // query heads of one GQA group at the same positions (they then share every rotated K tile),
-// or two consecutive query tiles of one head. Warp roles (12 warps):
-//   warp 0      TMA producer: Q sub-tiles once, then K/V tiles through a ring of stages
+// or two consecutive query tiles of one head. Warp roles (16 warps, 4 warpgroups):
+//   warp 0      TMA producer: Q sub-tiles once, then K and V tiles through separate rings
 //   warp 1      MMA issuer: S_s = Q_s K^T and O_s += P_s V with tcgen05.mma, TMEM accumulators
-//   warps 2-3   K rotators (fused RoPE): rotate each K stage in shared memory in place
 //   warps 4-7   softmax for sub-tile 0 (one thread per query row)
 //   warps 8-11  softmax for sub-tile 1
+//   warps 12-15 K rotators (fused RoPE): rotate each K stage in shared memory in place, one
+//               warp per SM sub-partition; (cos, sin) advance down the rows by angle addition
+// Registers are re-balanced with setmaxnreg: 64 (producers), 80 (rotators), 184 (softmax).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D, 256+2D); P_s (bf16)
 // overwrites the first 64 columns of S_s. Every wait is bounded (see ptx.cuh).
 #include <cuda.h>
@@ -22,26 +24,47 @@
 
 namespace afx {
 
+// Optional pipeline tracing (compile with -DATTNFUSE_TRACE=<block index>; off by default):
+// one CTA records clock64() at each pipeline event of its first 64 kv tiles.
+#ifdef ATTNFUSE_TRACE
+__device__ unsigned long long g_fwd_trace[64 * 16];
+#define AF_TRACE(i, e)                                                   \
+  do {                                                                   \
+    if (blockIdx.x == (ATTNFUSE_TRACE) && (i) < 64) g_fwd_trace[(i) * 16 + (e)] = clock64(); \
+  } while (0)
+#else
+#define AF_TRACE(i, e) \
+  do {                 \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int BM = 128;
 constexpr int BN = 128;
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
+constexpr uint32_t kRegsProducer = 64;   // warpgroup 0: TMA and MMA issue
+constexpr uint32_t kRegsRotator = 80;    // warpgroup 3: K rotation
+constexpr uint32_t kRegsSoftmax = 184;   // warpgroups 1, 2
+static_assert(kRegsProducer + kRegsRotator + 2 * kRegsSoftmax <= 4 * (65536 / kThreads),
+              "register split exceeds the registers the CTA is launched with");
 
 template <int D>
 struct FwdCfg {
-  static constexpr int ST = (D == 128) ? 2 : 4;          // K/V pipeline stages
+  static constexpr int KST = (D == 128) ? 3 : 5;          // K stages (released after S)
+  static constexpr int VST = (D == 128) ? 2 : 4;          // V stages (released after PV)
   static constexpr int PANELS = D / 64;                   // 128-byte swizzle panels per row
   static constexpr uint32_t TILE = 128u * D * 2u;         // bytes of one 128-row tile
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = 2 * TILE;
-  static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
-  static constexpr uint32_t OFF_CTL = OFF_V + ST * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
+  static constexpr uint32_t OFF_CTL = OFF_V + VST * TILE;
 };
 
 struct FwdCtl {
   uint64_t q_full[2], q_ready[2];
-  uint64_t k_full[4], k_ready[4], v_full[4], kv_empty[4];
+  uint64_t k_full[5], k_ready[5], k_empty[5];
+  uint64_t v_full[4], v_empty[4];
   uint64_t s_full[2], p_full[2], pv_done[2];
   uint64_t mma_final;
   uint32_t tmem_base;
@@ -52,8 +75,9 @@ struct FwdCtl {
 };
 
 __host__ __device__ constexpr size_t fwd_smem_bytes(int D) {
-  return 1024 + (D == 128 ? (2 + 2 * 2) : (2 + 2 * 4)) * (size_t)(128 * D * 2) + sizeof(FwdCtl);
+  return 1024 + (D == 128 ? (2 + 3 + 2) : (2 + 5 + 4)) * (size_t)(128 * D * 2) + sizeof(FwdCtl);
 }
+static_assert(1024 + 7 * 32768 + sizeof(FwdCtl) <= 232448, "d=128 shared memory budget");
 
 __device__ __forceinline__ bool bit_get(const uint32_t* w, int i) {
   return (w[i >> 5] >> (i & 31)) & 1u;
@@ -95,7 +119,7 @@ __device__ __forceinline__ bool tile_needs_mask(const FwdCtl* c, const FwdParams
 template <int D, int RK>
 __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D>;
-  constexpr int ST = C::ST;
+  constexpr int KST = C::KST, VST = C::VST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -137,11 +161,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       mbar_init(&ctl->p_full[s], 128);
       mbar_init(&ctl->pv_done[s], 1);
     }
-    for (int s = 0; s < ST; ++s) {
+    for (int s = 0; s < KST; ++s) {
       mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->k_ready[s], 64);
+      mbar_init(&ctl->k_ready[s], 128);
+      mbar_init(&ctl->k_empty[s], 1);
+    }
+    for (int s = 0; s < VST; ++s) {
       mbar_init(&ctl->v_full[s], 1);
-      mbar_init(&ctl->kv_empty[s], 1);
+      mbar_init(&ctl->v_empty[s], 1);
     }
     mbar_init(&ctl->mma_final, 1);
     fence_mbar_init();
@@ -186,43 +213,76 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
   int* status = p.status;
   volatile int* abort_flag = &ctl->abort_flag;
 
-  if (warp == 0) {
-    // ======================= TMA producer =======================
-    if (lane == 0) {
+  if (warp < 4) {
+    setmaxnreg_dec<kRegsProducer>();
+    if (warp == 0 && lane == 0) {
+      // ======================= TMA producer =======================
+      // One SM's TMA engine completes copies in issue order at a bounded byte rate, so copies
+      // are issued in the order the MMAs need them: Q, K(0), then K(i+1) ahead of V(i).
       tma_prefetch_desc(&p.tmQ);
       tma_prefetch_desc(&p.tmK);
       tma_prefetch_desc(&p.tmV);
+      // Q is read once; K and V are re-read by every query tile of the group.
+      const uint64_t pol_stream = l2_policy_evict_first();
+      const uint64_t pol_keep = l2_policy_evict_last();
       for (int s = 0; s < 2; ++s) {
         if (!ctl->valid[s]) continue;
         mbar_arrive_expect_tx(&ctl->q_full[s], C::TILE);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_Q + s * C::TILE + pn * (BM * 128), &p.tmQ, &ctl->q_full[s],
-                      pn * 64, ctl->q0[s], ctl->head[s], b);
+          tma_load_4d_hint(smem + C::OFF_Q + s * C::TILE + pn * (BM * 128), &p.tmQ,
+                           &ctl->q_full[s], pn * 64, ctl->q0[s], ctl->head[s], b, pol_stream);
       }
+      int ik = 0, iv = 0;
+      int jk = next_tile(ctl, p, jb, je), jv = jk;
+      bool go = true;
+      while (go && (jk < je || jv < je)) {
+        if (jk < je) {
+          const int s = ik % KST;
+          if (ik >= KST && !mbar_wait(&ctl->k_empty[s], ((ik / KST) - 1) & 1, status, abort_flag)) {
+            go = false;
+            break;
+          }
+          AF_TRACE(ik, 0);
+          mbar_arrive_expect_tx(&ctl->k_full[s], C::TILE);
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_4d_hint(smem + C::OFF_K + s * C::TILE + pn * (BN * 128), &p.tmK,
+                             &ctl->k_full[s], pn * 64, jk * BN, kvh, b, pol_keep);
+          ++ik;
+          jk = next_tile(ctl, p, jk + 1, je);
+        }
+        if (jv < je && (ik >= 2 || jk >= je)) {
+          const int s = iv % VST;
+          if (iv >= VST && !mbar_wait(&ctl->v_empty[s], ((iv / VST) - 1) & 1, status, abort_flag)) {
+            go = false;
+            break;
+          }
+          AF_TRACE(iv, 12);
+          mbar_arrive_expect_tx(&ctl->v_full[s], C::TILE);
+          for (int pn = 0; pn < C::PANELS; ++pn)
+            tma_load_4d_hint(smem + C::OFF_V + s * C::TILE + pn * (BN * 128), &p.tmV,
+                             &ctl->v_full[s], pn * 64, jv * BN, kvh, b, pol_keep);
+          ++iv;
+          jv = next_tile(ctl, p, jv + 1, je);
+        }
+      }
+      // Drain: no copy may still be landing in shared memory when the CTA exits.
+      for (int k = max(0, ik - KST); k < ik; ++k)
+        mbar_wait(&ctl->k_full[k % KST], (k / KST) & 1, status, nullptr);
+      for (int k = max(0, iv - VST); k < iv; ++k)
+        mbar_wait(&ctl->v_full[k % VST], (k / VST) & 1, status, nullptr);
+#ifdef ATTNFUSE_TRACE
+    } else if (warp == 3 && lane == 0) {
+      // trace builds only: record when each K and V copy lands
       int i = 0;
       for (int j = next_tile(ctl, p, jb, je); j < je; j = next_tile(ctl, p, j + 1, je), ++i) {
-        const int s = i % ST;
-        if (i >= ST && !mbar_wait(&ctl->kv_empty[s], ((i / ST) - 1) & 1, status, abort_flag))
-          break;
-        mbar_arrive_expect_tx(&ctl->k_full[s], C::TILE);
-        for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_K + s * C::TILE + pn * (BN * 128), &p.tmK, &ctl->k_full[s],
-                      pn * 64, j * BN, kvh, b);
-        mbar_arrive_expect_tx(&ctl->v_full[s], C::TILE);
-        for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_V + s * C::TILE + pn * (BN * 128), &p.tmV, &ctl->v_full[s],
-                      pn * 64, j * BN, kvh, b);
+        if (!mbar_wait(&ctl->k_full[i % KST], (i / KST) & 1, status, abort_flag)) break;
+        AF_TRACE(i, 14);
+        if (!mbar_wait(&ctl->v_full[i % VST], (i / VST) & 1, status, abort_flag)) break;
+        AF_TRACE(i, 15);
       }
-      // Drain: make sure no copy is still landing in shared memory when the CTA exits.
-      const int issued = i;
-      for (int k = max(0, issued - ST); k < issued; ++k) {
-        mbar_wait(&ctl->k_full[k % ST], (k / ST) & 1, status, nullptr);
-        mbar_wait(&ctl->v_full[k % ST], (k / ST) & 1, status, nullptr);
-      }
-    }
-  } else if (warp == 1) {
-    // ======================= MMA issuer =======================
-    if (lane == 0) {
+#endif
+    } else if (warp == 1 && lane == 0) {
+      // ======================= MMA issuer =======================
       constexpr uint32_t idesc_s = idesc_f32acc(128, BN, 0, 0, RK != kRopeNone);
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, D, 0, 1);
       bool ok = true;
@@ -258,80 +318,120 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       if (ok && j < je) {
         ok = mbar_wait(ROPE ? &ctl->k_ready[0] : &ctl->k_full[0], 0, status, abort_flag);
         tc_fence_after();
-        if (ok)
+        if (ok) {
           for (int s = 0; s < 2; ++s)
-            if (tile_active(ctl, p, s, j)) issue_s(s, 0);
+            if (tile_active(ctl, p, s, j)) {
+              AF_TRACE(0, 3 + s);
+              issue_s(s, 0);
+            }
+          mma_commit(&ctl->k_empty[0]);
+        }
       }
       for (int i = 0; ok && j < je; ++i) {
-        const int st = i % ST;
+        const int vs = i % VST;
         const int jn = next_tile(ctl, p, j + 1, je);
-        const int stn = (i + 1) % ST;
+        const int kn = (i + 1) % KST;
         bool kready = false;
-        if (!mbar_wait(&ctl->v_full[st], (i / ST) & 1, status, abort_flag)) break;
+        if (!mbar_wait(&ctl->v_full[vs], (i / VST) & 1, status, abort_flag)) break;
+        AF_TRACE(i, 13);
         for (int s = 0; s < 2 && ok; ++s) {
           if (tile_active(ctl, p, s, j)) {
             if (!mbar_wait(&ctl->p_full[s], cnt_pv[s] & 1, status, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            issue_pv(s, st, cnt_pv[s] > 0);
+            AF_TRACE(i, 9 + s);
+            issue_pv(s, vs, cnt_pv[s] > 0);
             ++cnt_pv[s];
             pv_pend[s] = true;
           }
-          if (s == 1) mma_commit(&ctl->kv_empty[st]);
+          if (s == 1) mma_commit(&ctl->v_empty[vs]);
           if (jn < je && tile_active(ctl, p, s, jn)) {
             if (!kready) {
-              if (!mbar_wait(ROPE ? &ctl->k_ready[stn] : &ctl->k_full[stn], ((i + 1) / ST) & 1,
+              if (!mbar_wait(ROPE ? &ctl->k_ready[kn] : &ctl->k_full[kn], ((i + 1) / KST) & 1,
                              status, abort_flag)) { ok = false; break; }
               kready = true;
             }
             if (pv_pend[s]) {
               if (!mbar_wait(&ctl->pv_done[s], (cnt_pv[s] - 1) & 1, status, abort_flag)) { ok = false; break; }
+              if (s == 0) AF_TRACE(i, 11);
               pv_pend[s] = false;
             }
             tc_fence_after();
-            issue_s(s, stn);
+            AF_TRACE(i + 1, 3 + s);
+            issue_s(s, kn);
           }
         }
+        if (ok && jn < je) mma_commit(&ctl->k_empty[kn]);
         j = jn;
       }
       // All issued MMAs must finish before TMEM is released.
       mma_commit(&ctl->mma_final);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
     }
-  } else if (warp < 4) {
+  } else if (warp >= 12) {
     // ======================= K rotators (fused RoPE) =======================
+    setmaxnreg_dec<kRegsRotator>();
     if (ROPE) {
-      const int rt = tid - 64;
-      constexpr int CP = D / 16;  // chunk pairs per row
+      constexpr int CP = D / 16;    // chunk pairs per row
+      constexpr int RG = 128 / CP;  // row groups; a thread owns rows rg, rg + RG, ...
+      const int rt = tid - 384;
+      const int c = rt % CP, rg = rt / CP;
+      uint64_t wc2[4], ws2[4], nws2[4];
+      {
+        float wc[8], ws[8];
+        load_cs8(p.rope_cs + (size_t)RG * (D / 2) + c * 8, wc, ws);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          wc2[w] = f2_pack(wc[2 * w], wc[2 * w + 1]);
+          ws2[w] = f2_pack(ws[2 * w], ws[2 * w + 1]);
+          nws2[w] = f2_pack(-ws[2 * w], -ws[2 * w + 1]);
+        }
+      }
       int i = 0;
       for (int j = next_tile(ctl, p, jb, je); j < je; j = next_tile(ctl, p, j + 1, je), ++i) {
-        const int st = i % ST;
-        if (!mbar_wait(&ctl->k_full[st], (i / ST) & 1, status, abort_flag)) break;
-        uint8_t* tile = smem + C::OFF_K + st * C::TILE;
-#pragma unroll 4
-        for (int it = rt; it < BN * CP; it += 64) {
-          const int row = it / CP, c = it % CP;
-          const int pos = j * BN + row;
-          if (pos >= p.N) continue;
-          uint32_t offl, offh;
-          if (D == 128) {
-            offl = sw128_offset(row, c);
-            offh = offl + BN * 128;
-          } else {
-            offl = sw128_offset(row, c);
-            offh = sw128_offset(row, c + 4);
+        const int st = i % KST;
+        uint64_t c2[4] = {0, 0, 0, 0}, s2[4] = {0, 0, 0, 0}, ns2[4] = {0, 0, 0, 0};
+        const int pos0 = j * BN + rg;
+        if (pos0 < p.N) {
+          float cc[8], ss[8];
+          load_cs8(p.rope_cs + (size_t)pos0 * (D / 2) + c * 8, cc, ss);
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            c2[w] = f2_pack(cc[2 * w], cc[2 * w + 1]);
+            s2[w] = f2_pack(ss[2 * w], ss[2 * w + 1]);
+            ns2[w] = f2_pack(-ss[2 * w], -ss[2 * w + 1]);
           }
-          uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
-          uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
-          rot_chunk<true>(lo, hi, p.rope_cs + (size_t)pos * (D / 2) + c * 8);
-          *reinterpret_cast<uint4*>(tile + offl) = lo;
-          *reinterpret_cast<uint4*>(tile + offh) = hi;
+        }
+        if (!mbar_wait(&ctl->k_full[st], (i / KST) & 1, status, abort_flag)) break;
+        if (rt == 0) AF_TRACE(i, 1);
+        uint8_t* tile = smem + C::OFF_K + st * C::TILE;
+#pragma unroll
+        for (int k = 0; k < CP; ++k) {
+          const int row = rg + RG * k;
+          if (j * BN + row < p.N) {
+            uint32_t offl, offh;
+            if (D == 128) {
+              offl = sw128_offset(row, c);
+              offh = offl + BN * 128;
+            } else {
+              offl = sw128_offset(row, c);
+              offh = sw128_offset(row, c + 4);
+            }
+            uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
+            uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
+            rot_chunk_cs2<true>(lo, hi, c2, s2, ns2);
+            *reinterpret_cast<uint4*>(tile + offl) = lo;
+            *reinterpret_cast<uint4*>(tile + offh) = hi;
+          }
+          if (k + 1 < CP) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
         }
         fence_proxy_async_smem();
+        if (rt == 0) AF_TRACE(i, 2);
         mbar_arrive(&ctl->k_ready[st]);
       }
     }
   } else {
     // ======================= softmax (one thread per query row) =======================
+    setmaxnreg_inc<kRegsSoftmax>();
     const int s = (warp - 4) >> 2;
     const int wq = warp & 3;                 // TMEM lane quarter
     const int r = wq * 32 + lane;            // row within the sub-tile
@@ -373,7 +473,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     const float scale_log2 = p.scale_log2;
     const float alibi = (var.bias == 1) ? var.slopes[head] * kLog2e : 0.f;
     const int blk_row = (var.mask == 3 && var.bs_block == 64) ? (r >> 6) : 0;
-    int jlast = -1;
     for (int j = next_tile(ctl, p, jb, je); valid && ok && j < je; j = next_tile(ctl, p, j + 1, je)) {
       if (!tile_active(ctl, p, s, j)) continue;
       const int k0 = j * BN;
@@ -382,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         ok = false;
         break;
       }
+      if (r == 0) AF_TRACE(n_done, 5 + 2 * s);
       tc_fence_after();
       uint32_t xr[BN];
       tmem_ld32<0>(tS, xr);
@@ -436,9 +536,15 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           x[c] = keep ? x[c] : kNegInf;
         }
       }
-      float mx = x[0];
+      // row max: 8 independent 3-input chains, then a small tree
+      float mp[8];
 #pragma unroll
-      for (int c = 1; c < BN; ++c) mx = fmaxf(mx, x[c]);
+      for (int k = 0; k < 8; ++k) mp[k] = fmaxf(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+      for (int i2 = 1; i2 < BN / 16; ++i2)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mp[k] = max3f(mp[k], x[16 * i2 + 2 * k], x[16 * i2 + 2 * k + 1]);
+      float mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
       mx *= mul;
       // ---- online softmax with lazy rescaling (exact after the final division) ----
       const float m_new = fmaxf(m_run, mx);
@@ -451,15 +557,18 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         rescale = true;
       }
       const float nb = (m_use == kNegInf) ? 0.f : -m_use;
-      float sum = 0.f;
+      const uint64_t mul2v = f2_pack(mul, mul), nb2 = f2_pack(nb, nb);
+      uint64_t acc2[4] = {0, 0, 0, 0};
       uint32_t pk[BN / 2];
 #pragma unroll
       for (int c = 0; c < BN / 2; ++c) {
-        const float p0 = ex2_approx(__fmaf_rn(x[2 * c], mul, nb));
-        const float p1 = ex2_approx(__fmaf_rn(x[2 * c + 1], mul, nb));
-        sum += p0 + p1;
+        const uint64_t a = fma2(f2_pack(x[2 * c], x[2 * c + 1]), mul2v, nb2);
+        const float p0 = ex2_approx(f2_lo(a)), p1 = ex2_approx(f2_hi(a));
+        acc2[c & 3] = add2(acc2[c & 3], f2_pack(p0, p1));
         pk[c] = pack_bf16x2(p0, p1);
       }
+      const uint64_t acc = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
+      const float sum = f2_lo(acc) + f2_hi(acc);
       tmem_st32<0>(tS, pk);
       tmem_st32<32>(tS + 32, pk);
       tmem_wait_st();
@@ -490,15 +599,14 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       l_run += sum;
       m_run = m_use;
       tc_fence_before();
+      if (r == 0) AF_TRACE(n_done, 6 + 2 * s);
       mbar_arrive(&ctl->p_full[s]);
       if (var.visits && r == 0) {
         const int TQ = (p.N + BM - 1) / BM;
         var.visits[((static_cast<int64_t>(b) * p.Hq + head) * TQ + q0 / BM) * TK + j] = 1;
       }
       ++n_done;
-      jlast = j;
     }
-    (void)jlast;
     // ---- epilogue: O = acc / l, LSE = ln(sum) ----
     if (valid) {
       if (ok && n_done > 0) {
@@ -527,7 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             w.y = pack_bf16x2(__uint_as_float(o[v4 * 8 + 2]) * inv, __uint_as_float(o[v4 * 8 + 3]) * inv);
             w.z = pack_bf16x2(__uint_as_float(o[v4 * 8 + 4]) * inv, __uint_as_float(o[v4 * 8 + 5]) * inv);
             w.w = pack_bf16x2(__uint_as_float(o[v4 * 8 + 6]) * inv, __uint_as_float(o[v4 * 8 + 7]) * inv);
-            dst[v4] = w;
+            __stcs(dst + v4, w);  // streaming store: O is not re-read
           }
         }
       }
@@ -561,10 +669,12 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int N, int half, Rope
 // Pre-rotation (paper Fig. 1a): out[b,h,n,:] = R_n x[b,h,n,:], out contiguous. One thread per
 // (row, chunk pair); HBM-bound elementwise pass.
 // ---------------------------------------------------------------------------------------------
-template <bool OUT_F16>
+template <bool OUT_F16, int KEY_D>
 __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb, int64_t sh,
                                  int64_t sn, __nv_bfloat16* __restrict__ out, int H, int N, int d,
                                  const float2* __restrict__ cs, int64_t rows) {
+  // KEY_D != 0: keys, whose (cos, sin) follow the fused kernel's in-tile recurrence (key_cs8)
+  // so that fused and pre-rotated attention see bit-identical K'. KEY_D == 0: table entries.
   const int cp = d / 16;
   const int64_t total = rows * cp;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -578,7 +688,10 @@ __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb
     const __nv_bfloat16* src = x + bb * sb + h * sh + n * sn;
     uint4 lo = *reinterpret_cast<const uint4*>(src + c * 8);
     uint4 hi = *reinterpret_cast<const uint4*>(src + d / 2 + c * 8);
-    rot_chunk<OUT_F16>(lo, hi, cs + (size_t)n * (d / 2) + c * 8);
+    float cc[8], ss[8];
+    if (KEY_D != 0) key_cs8<KEY_D == 0 ? 64 : KEY_D>(cs, n, c, cc, ss);
+    else load_cs8(cs + (size_t)n * (d / 2) + c * 8, cc, ss);
+    rot_chunk_cs<OUT_F16>(lo, hi, cc, ss);
     __nv_bfloat16* dst = out + row * d;
     *reinterpret_cast<uint4*>(dst + c * 8) = lo;
     *reinterpret_cast<uint4*>(dst + d / 2 + c * 8) = hi;
@@ -617,12 +730,15 @@ cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
 }
 
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
-                             int N, int d, const float2* cs, bool out_f16, cudaStream_t stream) {
+                             int N, int d, const float2* cs, bool out_f16, bool keys,
+                             cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(B) * H * N;
   const int64_t total = rows * (d / 16);
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<int64_t>((total + threads - 1) / threads, 152 * 16));
-  auto fn = out_f16 ? prerotate_kernel<true> : prerotate_kernel<false>;
+  auto fn = !out_f16 ? prerotate_kernel<false, 0>
+            : !keys ? prerotate_kernel<true, 0>
+            : d == 128 ? prerotate_kernel<true, 128> : prerotate_kernel<true, 64>;
   fn<<<blocks, threads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(x), strides[0], strides[1], strides[2],
       static_cast<__nv_bfloat16*>(out), H, N, d, cs, rows);
@@ -630,3 +746,10 @@ cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, i
 }
 
 }  // namespace afx
+
+#ifdef ATTNFUSE_TRACE
+// Copy the forward pipeline trace (64 tiles x 16 events of clock64) to host memory.
+extern "C" int attnfuse_trace_read(unsigned long long* dst) {
+  return (int)cudaMemcpyFromSymbol(dst, afx::g_fwd_trace, sizeof(unsigned long long) * 64 * 16);
+}
+#endif

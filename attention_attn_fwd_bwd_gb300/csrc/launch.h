@@ -32,7 +32,8 @@ cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaS
 cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
                               cudaStream_t stream);
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
-                             int N, int d, const float2* cs, bool out_f16, cudaStream_t stream);
+                             int N, int d, const float2* cs, bool out_f16, bool keys,
+                             cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
 
 }  // namespace afx

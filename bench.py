@@ -1,0 +1,455 @@
+#!/usr/bin/env python3
+"""Benchmark: fused RoPE + causal attention forward on GB300 (TFLOP/s, % of bf16 peak).
+
+Default workload (one step = one pass of the forward hot path: the RoPE (cos, sin) table and
+the fused forward kernel, through the C ABI): Llama-3-8B-shaped RoPE+causal forward,
+B=4, Hq=32, Hkv=8, N=4096, d=128, rope_theta=5e5, fused RoPE, O and LSE, synthetic N(0,1)
+bf16 inputs. Algorithmic work counts only the allowed (m, n) pairs: 4 d B Hq N(N+1)/2 FLOP.
+
+Prints ONE JSON line (rank 0). Multi-GPU: one rank per GPU (torchrun), each rank runs the same
+workload on its own GPU (weak scaling, no data-path collective); the time is the max over
+ranks. ``--impl reference`` times the fp64 CPU oracle on a bounded sample instead.
+Other measurements (``--workload``, ``--sweep``) print extra lines for the design notes.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused RoPE+causal attn fwd TFLOP/s (bf16) and % of GB300 dense BF16 peak"
+WORKLOADS = {
+    # name: (B, Hq, Hkv, N, d, theta, rope_mode_name, mask)
+    "llama8b_fused": (4, 32, 8, 4096, 128, 5e5, "fused", "causal"),
+    "llama8b_prerotate": (4, 32, 8, 4096, 128, 5e5, "prerotate", "causal"),
+    "llama8b_none": (4, 32, 8, 4096, 128, 5e5, "none", "causal"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama8b_fused", choices=sorted(WORKLOADS))
+    ap.add_argument("--sweep", action="store_true", help="fused vs pre-rotated N sweep")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="one warm-up call and one call of the workload, then exit (for ncu)")
+    return ap.parse_args()
+
+
+def causal_flops(B, Hq, N, d):
+    return 4.0 * d * B * Hq * N * (N + 1) / 2.0
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+# ------------------------------------------------------------------------------------------
+# clocks during the timed region
+# ------------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.proc, self.lines = index, None, []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------------------
+# ncu traffic figure committed under profiles/ (null when the kernel source changed since)
+# ------------------------------------------------------------------------------------------
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "attention_attn_fwd_bwd_gb300", "csrc")
+    for name in ("fwd.cu", "ptx.cuh", "common.cuh", "launch.h"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload):
+    path = os.path.join(ROOT, "profiles", f"fwd_kernel_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", text)
+    if not m or not s or s.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+# ------------------------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ------------------------------------------------------------------------------------------
+class OracleSampler:
+    """The fp64 oracle as it stands, timed on sampled full query rows of the workload."""
+
+    def __init__(self, B, Hq, Hkv, N, d, theta, rope_on, seed):
+        import oracle
+        from attention_attn_fwd_bwd_gb300 import inputs
+
+        oracle.build()
+        self.oracle, self.inputs = oracle, inputs
+        x = inputs.prefill(B, Hq, Hkv, N, d, seed)
+        self.q, self.k, self.v = (x[n].double().numpy() for n in ("q", "k", "v"))
+        self.shape = (B, Hq, N, d)
+        self.theta, self.rope_on = theta, rope_on
+        self.var = oracle.Variant(mask=1)
+
+    def run(self, nrows, seed):
+        """One batch of nrows sampled rows: (flops, seconds)."""
+        B, Hq, N, d = self.shape
+        rows = self.inputs.sample_rows(B, Hq, N, nrows, seed=seed)
+        t0 = time.perf_counter()
+        self.oracle.forward_rows(self.q, self.k, self.v, d ** -0.5, self.theta, self.rope_on,
+                                 self.var, rows)
+        secs = time.perf_counter() - t0
+        return sum(4.0 * d * (int(m) + 1) for _, _, m in rows), secs
+
+    def timed(self, budget_s, batch):
+        flops, secs, rows, it = 0.0, 0.0, 0, 0
+        while secs < budget_s or rows == 0:
+            f, s = self.run(batch, seed=7000 + it)
+            flops, secs, rows, it = flops + f, secs + s, rows + batch, it + 1
+        return flops / secs / 1e12, rows, secs
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
+    smp = OracleSampler(B, Hq, Hkv, N, d, theta, mode != "none", seed=2000)
+    batch = os.cpu_count() or 8
+    per_step = []
+    for i in range(args.warmup + args.steps):
+        f, secs = smp.run(batch, seed=5000 + i)
+        if i >= args.warmup:
+            per_step.append((f, secs))
+    tflops = sum(f for f, _ in per_step) / sum(t for _, t in per_step) / 1e12
+    ms = 1e3 * sum(t for _, t in per_step) / len(per_step)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": workload_config(args.workload),
+        "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                         "kind": "oracle",
+                         "sample": f"{batch} full query rows of the workload per step (fp64 "
+                                   f"oracle, rows drawn uniformly over (b, h, m))"},
+        "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(name):
+    B, Hq, Hkv, N, d, theta, mode, mask = WORKLOADS[name]
+    return {"workload": f"Llama-3-8B-shaped RoPE+{mask} forward, {mode} RoPE "
+                        f"(B={B}, Hq={Hq}, Hkv={Hkv}, N={N}, d={d})",
+            "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d, "rope_theta": theta, "rope_mode": mode,
+            "mask": mask, "outputs": "O bf16, LSE fp32",
+            "l2": "inputs rotated over 3 resident sets (3 x 322 MiB > 126 MiB L2)"}
+
+
+# ------------------------------------------------------------------------------------------
+# GPU arm
+# ------------------------------------------------------------------------------------------
+def run_ours(args, rank, world):
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
+    rope_mode = {"fused": af.ROPE_FUSED, "prerotate": af.ROPE_PREROTATE, "none": af.ROPE_NONE}[mode]
+    scale = d ** -0.5
+    flops = causal_flops(B, Hq, N, d)
+    nsets = 3
+    sets = []
+    for i in range(nsets):
+        x = inputs.prefill(B, Hq, Hkv, N, d, seed=2000 + i)
+        sets.append({n: x[n].to(dev) for n in ("q", "k", "v")})
+        sets[-1]["out"] = torch.empty_like(sets[-1]["q"])
+        sets[-1]["lse"] = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    ws_n = af.fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=dev)
+    var = af.Variant(mask=af.MASK_CAUSAL)
+    stream = torch.cuda.current_stream()
+
+    def step(i, flags=0):
+        s = sets[i % nsets]
+        af.fwd(s["q"], s["k"], s["v"], scale=scale, rope_theta=theta, rope_mode=rope_mode | flags,
+               variant=var, out=s["out"], lse=s["lse"], workspace=ws)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    barrier()
+    assert af.device_status() == 0
+
+    # ---- timed region: K full steps (table + forward kernel) ----
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    elapsed_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * flops / (ms_per_step * 1e-3) / 1e12
+    assert af.device_status() == 0
+
+    # ---- the forward kernel alone (table reused): per-launch duration for the roofline ----
+    launches_per_step = 1 + (1 if rope_mode != af.ROPE_NONE else 0) + (2 if rope_mode == af.ROPE_PREROTATE else 0)
+    kern_steps = min(args.steps, 200)
+    barrier()
+    ev0.record(stream)
+    for i in range(kern_steps):
+        step(i, af.ROPE_REUSE_TABLE if rope_mode == af.ROPE_FUSED else 0)
+    ev1.record(stream)
+    barrier()
+    kern_ms = ev0.elapsed_time(ev1) / kern_steps
+    if rope_mode == af.ROPE_PREROTATE:
+        kern_ms = None  # pre-rotation launches three kernels per call; see the sweep lines
+
+    # ---- end to end: host buffers, H2D + call + D2H inside the timed region ----
+    e2e = None
+    if rank == 0 or world > 1:
+        pin = {n: sets[0][n].cpu().pin_memory() for n in ("q", "k", "v")}
+        out_h = torch.empty(sets[0]["out"].shape, dtype=torch.bfloat16).pin_memory()
+        lse_h = torch.empty(sets[0]["lse"].shape, dtype=torch.float32).pin_memory()
+        dq = {n: torch.empty_like(sets[0][n]) for n in ("q", "k", "v")}
+        e2e_steps = max(3, min(args.steps, 20))
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = out_h.numel() * 2 + lse_h.numel() * 4
+        barrier()
+        ev0.record(stream)
+        for i in range(e2e_steps):
+            for n in ("q", "k", "v"):
+                dq[n].copy_(pin[n], non_blocking=True)
+            af.fwd(dq["q"], dq["k"], dq["v"], scale=scale, rope_theta=theta, rope_mode=rope_mode,
+                   variant=var, out=sets[0]["out"], lse=sets[0]["lse"], workspace=ws)
+            out_h.copy_(sets[0]["out"], non_blocking=True)
+            lse_h.copy_(sets[0]["lse"], non_blocking=True)
+        ev1.record(stream)
+        barrier()
+        e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    if rank != 0:
+        return
+    peaks, src = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    roof = None
+    if kern_ms is not None:
+        ach = flops / (kern_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
+                "frac": ach / peak, "traffic": committed_traffic(args.workload),
+                "kernel": "fwd_kernel<128, fused>", "kernel_ms": kern_ms,
+                "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
+                "frac_of_sustained": ach / float(peaks.get("bf16_tflops_sustained", peak))}
+    cpu = None
+    if not args.no_cpu_baseline:
+        smp = OracleSampler(B, Hq, Hkv, N, d, theta, mode != "none", seed=2000)
+        tf, rows, secs = smp.timed(budget_s=12.0, batch=os.cpu_count() or 8)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": f"{rows} full query rows of the workload (fp64 oracle, {secs:.1f} s), "
+                         f"rows drawn uniformly over (b, h, m); value = their causal FLOPs / time"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(args.workload),
+        "pct_of_peak": 100.0 * value / world / peak,
+        "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_sweep(args):
+    """Fused vs pre-rotated vs no RoPE over N at B*N = 16384 tokens (the Rotation Calculus)."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    dev = torch.device("cuda")
+    Hq, Hkv, d, theta = 32, 8, 128, 5e5
+    res = []
+    for N in (1024, 2048, 4096, 8192, 16384):
+        B = 16384 // N
+        x = inputs.prefill(B, Hq, Hkv, N, d, seed=N)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        out = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        times = {}
+        for name, mode in (("fused", af.ROPE_FUSED), ("prerotate", af.ROPE_PREROTATE),
+                           ("none", af.ROPE_NONE)):
+            ws = torch.empty(max(16, af.fwd_workspace_size(B, Hq, Hkv, N, d, mode)),
+                             dtype=torch.uint8, device=dev)
+            for _ in range(5):
+                af.fwd(q, k, v, rope_theta=theta, rope_mode=mode, out=out, lse=lse, workspace=ws)
+            torch.cuda.synchronize()
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+            reps = 30
+            samples = []
+            for _ in range(reps):
+                evs[0].record()
+                af.fwd(q, k, v, rope_theta=theta, rope_mode=mode, out=out, lse=lse, workspace=ws)
+                evs[1].record()
+                torch.cuda.synchronize()
+                samples.append(evs[0].elapsed_time(evs[1]))
+            times[name] = statistics.median(samples)
+        fl = causal_flops(B, Hq, N, d)
+        res.append({"N": N, "B": B, **{f"{k}_ms": v for k, v in times.items()},
+                    "fused_over_prerotate": times["prerotate"] / times["fused"],
+                    "fused_tflops": fl / times["fused"] / 1e9,
+                    "none_tflops": fl / times["none"] / 1e9})
+        print(json.dumps({"sweep": "rotation_calculus", **res[-1]}), flush=True)
+    # crossover: where prerotate/fused crosses 1 (log-linear interpolation in N)
+    nstar = None
+    for a, b in zip(res, res[1:]):
+        ra, rb = a["fused_over_prerotate"] - 1, b["fused_over_prerotate"] - 1
+        if ra >= 0 > rb or ra <= 0 < rb:
+            t = ra / (ra - rb)
+            nstar = math.exp(math.log(a["N"]) + t * (math.log(b["N"]) - math.log(a["N"])))
+    print(json.dumps({"sweep": "rotation_calculus_crossover", "N_star": nstar,
+                      "note": "speedup = t_prerotate / t_fused; >1 means fusion wins"}), flush=True)
+
+
+def run_profile(args):
+    """Warm-up call plus one call of the workload: a small, self-contained ncu target."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
+    rope_mode = {"fused": af.ROPE_FUSED, "prerotate": af.ROPE_PREROTATE, "none": af.ROPE_NONE}[mode]
+    x = inputs.prefill(B, Hq, Hkv, N, d, seed=2000)
+    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+    for _ in range(2):
+        out, lse = af.fwd(q, k, v, rope_theta=theta, rope_mode=rope_mode)
+    torch.cuda.synchronize()
+    if af.device_status() != 0:
+        raise SystemExit("device status reports a timeout")
+    print(json.dumps({"profile": args.workload, "ok": True}))
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+
+        torch.distributed.init_process_group("nccl")
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
+        return
+    if args.profile:
+        run_profile(args)
+        return
+    run_ours(args, rank, world)
+    if world > 1:
+        import torch
+
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -62,6 +62,12 @@ typedef enum {
                                   attention runs without rotation (the paper's baseline) */
 } attnfuse_rope_mode;
 
+/* Flag OR-ed into rope_mode: the workspace already holds the (cos, sin) table, built by an
+ * earlier call on the same workspace (or by attnfuse_rope_table) for the same d and rope_theta
+ * and for at least N positions, so the call skips rebuilding it. The table depends on
+ * positions only, so a caller reusing one workspace across layers or steps can build it once. */
+#define ATTNFUSE_ROPE_REUSE_TABLE 0x100
+
 /* Mask combinators (paper §3.1 causal / sliding_window / full / block_sparse). */
 typedef enum {
   ATTNFUSE_MASK_FULL = 0,
@@ -174,6 +180,13 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
                                         int B, int H, int N, int d, float rope_theta,
                                         void* workspace, size_t workspace_bytes,
                                         cudaStream_t stream);
+
+/* Build the (cos, sin) table that the rotating modes keep at the start of their workspace:
+ * entry (p, i) = (cos, sin)(p * theta_i) for p < N, i < d/2, fp32 pairs, computed in-kernel
+ * with the angle reduced in turns (exact product split) so large positions keep full accuracy.
+ * table: at least attnfuse_fwd_workspace_size(.., ATTNFUSE_ROPE_FUSED, ..) bytes. */
+attnfuse_status attnfuse_rope_table(void* table, size_t table_bytes, int N, int d,
+                                    float rope_theta, cudaStream_t stream);
 
 /* Debug: launch one kernel whose only wait can never complete, bounded by `limit_ns`
  * nanoseconds. The kernel then records ATTNFUSE_ERR_TIMEOUT in the device status word and
