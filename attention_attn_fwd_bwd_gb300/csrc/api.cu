@@ -7,6 +7,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -354,6 +355,122 @@ attnfuse_status attnfuse_rope_table(void* table, size_t table_bytes, int N, int 
   cudaError_t e = launch_rope_table(static_cast<float2*>(table), rope_table_rows(N), d / 2,
                                     make_freqs(d, rope_theta), stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode (paper §4.2)
+// ---------------------------------------------------------------------------------------------
+static attnfuse_status decode_plan(int B, int Hkv, int L, int num_splits, int* splits, int* chunk) {
+  if (num_splits < 0) return fail(ATTNFUSE_ERR_INVALID_ARG, "num_splits %d < 0", num_splits);
+  const int tiles = (L + 127) / 128;
+  int s = num_splits;
+  if (s == 0) {
+    // One resident CTA per SM: pick the split count with the smallest makespan
+    // (waves x tiles per chunk, plus about one tile of fixed cost per wave).
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess)
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long pairs = (long long)B * Hkv;
+    long long best = -1;
+    for (int c = 1; c <= tiles; ++c) {
+      const long long waves = (pairs * c + sms - 1) / sms;
+      const long long cost = waves * ((tiles + c - 1) / c + 1);
+      if (best < 0 || cost < best) {
+        best = cost;
+        s = c;
+      }
+    }
+  }
+  s = std::max(1, std::min(s, tiles));
+  const int ch = ((tiles + s - 1) / s) * 128;
+  *chunk = ch;
+  *splits = s;
+  return ATTNFUSE_OK;
+}
+
+attnfuse_status attnfuse_decode_auto_splits(int B, int Hkv, int L, int* num_splits) {
+  if (!num_splits || B <= 0 || Hkv <= 0 || L <= 0)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "bad arguments");
+  int chunk = 0;
+  attnfuse_status rc = decode_plan(B, Hkv, L, 0, num_splits, &chunk);
+  if (rc) return rc;
+  return ok();
+}
+
+attnfuse_status attnfuse_decode_workspace_size(int B, int Hq, int Hkv, int L, int d,
+                                               int num_splits, size_t* bytes) {
+  if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
+  attnfuse_status rc = check_shape(B, Hq, Hkv, L, d);
+  if (rc) return rc;
+  int splits = 0, chunk = 0;
+  if ((rc = decode_plan(B, Hkv, L, num_splits, &splits, &chunk))) return rc;
+  const size_t rows = (size_t)B * Hq * splits;
+  *bytes = align_up(rows * d * 4, 256) + 2 * align_up(rows * 4, 256);
+  return ok();
+}
+
+attnfuse_status attnfuse_decode(const void* q, const int64_t q_strides[3], const void* k_cache,
+                                const int64_t k_strides[4], const void* v_cache,
+                                const int64_t v_strides[4], void* out,
+                                const int64_t o_strides[3], float* lse, int B, int Hq, int Hkv,
+                                int L, int d, int q_pos, float scale, float rope_theta,
+                                attnfuse_rope_mode rope_mode, int num_splits, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  attnfuse_status rc = check_shape(B, Hq, Hkv, L, d);
+  if (rc) return rc;
+  const int g = Hq / Hkv;
+  if (g > 32) return fail(ATTNFUSE_ERR_UNSUPPORTED, "decode needs Hq / Hkv <= 32 (got %d)", g);
+  if (!q || !aligned16(q) || !q_strides || q_strides[2] != 1 || q_strides[0] % 8 ||
+      q_strides[1] % 8 || q_strides[0] <= 0 || q_strides[1] <= 0)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "q: NULL, misaligned or bad strides");
+  if (!out || !o_strides || o_strides[2] != 1 || o_strides[0] <= 0 || o_strides[1] <= 0)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "out: NULL or bad strides");
+  if ((rc = check_tensor(k_cache, k_strides, "k_cache"))) return rc;
+  if ((rc = check_tensor(v_cache, v_strides, "v_cache"))) return rc;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "lse is not 4-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (rope_mode != ATTNFUSE_ROPE_NONE && rope_mode != ATTNFUSE_ROPE_FUSED)
+    return fail(ATTNFUSE_ERR_UNSUPPORTED, "decode rotates q only: rope_mode NONE or FUSED");
+  if (rope_mode == ATTNFUSE_ROPE_FUSED && (!(rope_theta > 0.f) || !std::isfinite(rope_theta)))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
+  if (q_pos < 0) return fail(ATTNFUSE_ERR_INVALID_ARG, "q_pos %d < 0", q_pos);
+  size_t need = 0;
+  if ((rc = attnfuse_decode_workspace_size(B, Hq, Hkv, L, d, num_splits, &need))) return rc;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need,
+                workspace_bytes);
+  int* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  DecParams p;
+  memset(&p, 0, sizeof(p));
+  int splits = 0, chunk = 0;
+  if ((rc = decode_plan(B, Hkv, L, num_splits, &splits, &chunk))) return rc;
+  if ((rc = encode_bhnd(&p.tmK, k_cache, k_strides, B, Hkv, L, d, "k_cache"))) return rc;
+  if ((rc = encode_bhnd(&p.tmV, v_cache, v_strides, B, Hkv, L, d, "v_cache"))) return rc;
+  const size_t rows = (size_t)B * Hq * splits;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.part_acc = reinterpret_cast<float*>(ws);
+  p.part_m = reinterpret_cast<float*>(ws + align_up(rows * d * 4, 256));
+  p.part_l = reinterpret_cast<float*>(ws + align_up(rows * d * 4, 256) + align_up(rows * 4, 256));
+  p.q = static_cast<const __nv_bfloat16*>(q);
+  p.q_sb = q_strides[0];
+  p.q_sh = q_strides[1];
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.o_sb = o_strides[0];
+  p.o_sh = o_strides[1];
+  p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.g = g; p.L = L; p.q_pos = q_pos;
+  p.chunk = chunk;
+  p.splits = splits;
+  p.splits_used = (L + chunk - 1) / chunk;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  if (rope_mode == ATTNFUSE_ROPE_FUSED) p.freqs = make_freqs(d, rope_theta);
+  p.status = st;
+  cudaError_t e = launch_decode(p, d, rope_mode == ATTNFUSE_ROPE_FUSED, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return ok();
 }
 

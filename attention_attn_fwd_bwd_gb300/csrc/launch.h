@@ -23,6 +23,28 @@ struct FwdParams {
   int* status;
 };
 
+struct DecParams {
+  CUtensorMap tmK, tmV;       // caches [B, Hkv, L, d], box (64, 128, 1, 1)
+  const __nv_bfloat16* q;     // [B, Hq, d]
+  int64_t q_sb, q_sh;
+  __nv_bfloat16* out;         // [B, Hq, d]
+  int64_t o_sb, o_sh;
+  float* lse;                 // [B, Hq] or null
+  float* part_acc;            // [B, Hq, splits, d]
+  float* part_m;              // [B, Hq, splits] (log2 units)
+  float* part_l;              // [B, Hq, splits]
+  int B, Hq, Hkv, g, L, q_pos;
+  int chunk;                  // keys per split (multiple of 128)
+  int splits;                 // partial-buffer stride
+  int splits_used;            // ceil(L / chunk)
+  float scale_log2;
+  RopeFreqs freqs;
+  int* status;
+};
+
+size_t decode_smem_size(int d);
+cudaError_t launch_decode(const DecParams& p, int d, bool rope_q, cudaStream_t stream);
+
 size_t fwd_smem_size(int d);
 // rope_kind: how the score operands were produced.
 constexpr int kRopeNone = 0;        // bf16 inputs used as they are

@@ -15,18 +15,4 @@ attnfuse_status attnfuse_bwd(const void*, const int64_t*, const void*, const int
                              void*, size_t, cudaStream_t) {
   return ATTNFUSE_ERR_UNSUPPORTED;
 }
-attnfuse_status attnfuse_decode_workspace_size(int, int, int, int, int, int, size_t* bytes) {
-  if (bytes) *bytes = 0;
-  return ATTNFUSE_ERR_UNSUPPORTED;
-}
-attnfuse_status attnfuse_decode(const void*, const int64_t*, const void*, const int64_t*,
-                                const void*, const int64_t*, void*, const int64_t*, float*, int,
-                                int, int, int, int, int, float, float, attnfuse_rope_mode, int,
-                                void*, size_t, cudaStream_t) {
-  return ATTNFUSE_ERR_UNSUPPORTED;
-}
-attnfuse_status attnfuse_decode_auto_splits(int, int, int, int* n) {
-  if (n) *n = 1;
-  return ATTNFUSE_ERR_UNSUPPORTED;
-}
 }

@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_fused", choices=sorted(WORKLOADS))
     ap.add_argument("--sweep", action="store_true", help="fused vs pre-rotated N sweep")
+    ap.add_argument("--decode", action="store_true",
+                    help="split-KV decode at the Llama-3-70B head shape (B=1, 8; splits sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
@@ -424,6 +426,57 @@ def run_profile(args):
     print(json.dumps({"profile": args.workload, "ok": True}))
 
 
+def run_decode_bench(args):
+    """Split-KV decode: Hq=64, Hkv=8, d=128, L=32768, q at 32767; K+V bytes / time (cold L2)."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    dev = torch.device("cuda")
+    peaks, src = measured_peaks()
+    Hq, Hkv, d, L = 64, 8, 128, 32768
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x the L2
+    for B in (1, 8):
+        x = inputs.decode(B, Hq, Hkv, L, d, seed=5000 + B)
+        q, kc, vc = (x[n].to(dev) for n in ("q", "k_cache", "v_cache"))
+        out = torch.empty_like(q)
+        lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+        nbytes = 2 * B * Hkv * L * d * 2
+        for splits in (0, 1, 8, 32, 128):
+            ws = torch.empty(af.decode_workspace_size(B, Hq, Hkv, L, d, splits), dtype=torch.uint8,
+                             device=dev)
+            for _ in range(3):
+                af.decode(q, kc, vc, L - 1, rope_theta=5e5, num_splits=splits, out=out, lse=lse,
+                          workspace=ws)
+            res = {}
+            for cold in (True, False):
+                samples = []
+                for _ in range(30):
+                    if cold:
+                        flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    af.decode(q, kc, vc, L - 1, rope_theta=5e5, num_splits=splits, out=out,
+                              lse=lse, workspace=ws)
+                    e1.record()
+                    torch.cuda.synchronize()
+                    samples.append(e0.elapsed_time(e1) * 1e3)
+                samples.sort()
+                res["cold" if cold else "warm"] = samples
+            med = res["cold"][len(res["cold"]) // 2]
+            gbs = nbytes / (med * 1e-6) / 1e9
+            used = splits if splits else af.decode_auto_splits(B, Hkv, L)
+            print(json.dumps({"decode": "llama70b_head_shape", "B": B, "splits": splits,
+                              "splits_used": used, "us_median_cold_l2": med,
+                              "us_min_cold_l2": res["cold"][0],
+                              "us_p90_cold_l2": res["cold"][int(0.9 * len(res["cold"]))],
+                              "us_median_warm_l2": res["warm"][len(res["warm"]) // 2],
+                              "kv_bytes": nbytes, "gbs_cold": gbs,
+                              "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
+                              "launches": 2}), flush=True)
+
+
 def main():
     args = parse()
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -443,6 +496,10 @@ def main():
         return
     if args.profile:
         run_profile(args)
+        return
+    if args.decode:
+        if rank == 0:
+            run_decode_bench(args)
         return
     run_ours(args, rank, world)
     if world > 1:

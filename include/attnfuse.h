@@ -153,8 +153,10 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
  * L keys stored already rotated. Phase 1 computes partial (max, sum, acc) per KV chunk, phase
  * 2 merges the chunks through their log-sum-exp. rope_mode applies to q only (NONE or FUSED).
  * q: [B, Hq, d] (strides b, h, c); k_cache, v_cache: [B, Hkv, L, d]; out: [B, Hq, d];
- * lse: [B, Hq] or NULL. num_splits: number of KV chunks per (b, kv-head), 0 = automatic.
- * Requires Hq / Hkv <= 16.
+ * lse: [B, Hq] or NULL. num_splits: number of KV chunks per (b, kv-head), 0 = automatic
+ * (about two resident CTAs per SM); chunks are whole 128-key tiles, so fewer chunks than
+ * requested are used when L / 128 < num_splits. Requires Hq / Hkv <= 32. The q rotation
+ * (FUSED) is rounded to bf16, the element type of the cache.
  * ------------------------------------------------------------------------------------------ */
 attnfuse_status attnfuse_decode_workspace_size(int B, int Hq, int Hkv, int L, int d,
                                                int num_splits, size_t* bytes);
