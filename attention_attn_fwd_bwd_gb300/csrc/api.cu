@@ -359,6 +359,106 @@ attnfuse_status attnfuse_rope_table(void* table, size_t table_bytes, int N, int 
 }
 
 // ---------------------------------------------------------------------------------------------
+// Backward (paper §4.4)
+// ---------------------------------------------------------------------------------------------
+attnfuse_status attnfuse_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                            attnfuse_rope_mode rope_mode, size_t* bytes) {
+  if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
+  rope_mode = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
+  size_t n = 0;
+  if (rope_mode != ATTNFUSE_ROPE_NONE) n += rope_table_bytes(N, d);
+  n += align_up((size_t)B * Hq * N * 4, 256);  // D = rowsum(dO * O)
+  *bytes = n;
+  return ok();
+}
+
+static attnfuse_status check3(const void* p, const int64_t st[4], const char* name) {
+  return check_tensor(p, st, name);
+}
+
+attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const void* k,
+                             const int64_t k_strides[4], const void* v,
+                             const int64_t v_strides[4], const void* out,
+                             const int64_t o_strides[4], const float* lse, const void* dout,
+                             const int64_t do_strides[4], void* dq, const int64_t dq_strides[4],
+                             void* dk, const int64_t dk_strides[4], void* dv,
+                             const int64_t dv_strides[4], int B, int Hq, int Hkv, int N, int d,
+                             float scale, float rope_theta, attnfuse_rope_mode rope_mode,
+                             const attnfuse_variant* variant, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+  const bool reuse_table = (rope_mode & ATTNFUSE_ROPE_REUSE_TABLE) != 0;
+  rope_mode = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  if ((rc = check3(q, q_strides, "q")) || (rc = check3(k, k_strides, "k")) ||
+      (rc = check3(v, v_strides, "v")) || (rc = check3(out, o_strides, "out")) ||
+      (rc = check3(dout, do_strides, "dout")) || (rc = check3(dq, dq_strides, "dq")) ||
+      (rc = check3(dk, dk_strides, "dk")) || (rc = check3(dv, dv_strides, "dv")))
+    return rc;
+  if (!lse || (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "lse NULL or misaligned");
+  if (!(scale > 0.f) || !std::isfinite(scale))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
+  if (rope_mode != ATTNFUSE_ROPE_NONE && (!(rope_theta > 0.f) || !std::isfinite(rope_theta)))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
+  int causal = 1;
+  if (variant) {
+    if (variant->bias != ATTNFUSE_BIAS_NONE ||
+        (variant->mask != ATTNFUSE_MASK_FULL && variant->mask != ATTNFUSE_MASK_CAUSAL))
+      return fail(ATTNFUSE_ERR_UNSUPPORTED, "backward supports FULL or CAUSAL masks without bias");
+    causal = (variant->mask == ATTNFUSE_MASK_CAUSAL || variant->causal) ? 1 : 0;
+  }
+  size_t need = 0;
+  if ((rc = attnfuse_bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, &need))) return rc;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need,
+                workspace_bytes);
+  int* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  BwdParams p;
+  memset(&p, 0, sizeof(p));
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  if (rope_mode != ATTNFUSE_ROPE_NONE) {
+    p.rope_cs = reinterpret_cast<const float2*>(ws);
+    if (!reuse_table) {
+      cudaError_t e = launch_rope_table(reinterpret_cast<float2*>(ws), rope_table_rows(N), d / 2,
+                                        make_freqs(d, rope_theta), stream);
+      if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
+    }
+    ws += rope_table_bytes(N, d);
+  }
+  p.Dvec = reinterpret_cast<float*>(ws);
+  if ((rc = encode_bhnd(&p.tmQ, q, q_strides, B, Hq, N, d, "q"))) return rc;
+  if ((rc = encode_bhnd(&p.tmK, k, k_strides, B, Hkv, N, d, "k"))) return rc;
+  if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v"))) return rc;
+  if ((rc = encode_bhnd(&p.tmDO, dout, do_strides, B, Hq, N, d, "dout"))) return rc;
+  p.o = static_cast<const __nv_bfloat16*>(out);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  for (int i = 0; i < 3; ++i) {
+    p.o_s[i] = o_strides[i];
+    p.do_s[i] = do_strides[i];
+    p.dq_s[i] = dq_strides[i];
+    p.dk_s[i] = dk_strides[i];
+    p.dv_s[i] = dv_strides[i];
+  }
+  p.lse = lse;
+  p.dq = static_cast<__nv_bfloat16*>(dq);
+  p.dk = static_cast<__nv_bfloat16*>(dk);
+  p.dv = static_cast<__nv_bfloat16*>(dv);
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.g = Hq / Hkv; p.causal = causal;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.status = st;
+  cudaError_t e = launch_bwd(p, rope_mode != ATTNFUSE_ROPE_NONE, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------------------------
 // Decode (paper §4.2)
 // ---------------------------------------------------------------------------------------------
 static attnfuse_status decode_plan(int B, int Hkv, int L, int num_splits, int* splits, int* chunk) {

@@ -1,0 +1,654 @@
+// Backward attention for sm_103a (AttnFuse paper §4.4): three kernels and no atomics.
+//   bwd_pre_kernel   D_m = sum_c dO_mc O_mc                       (HBM-bound row reduction)
+//   dkdv_kernel      one CTA per (key tile, kv head, batch): K' and V stay in shared memory;
+//                    for every query head of the GQA group and every query tile that can see
+//                    the key tile: S^T = K' Q'^T and dP^T = V dO^T (tcgen05, TMEM), then
+//                    P^T = exp(S^T - L), dS^T = P^T (dP^T - D), dV += P^T dO, dK' += dS^T Q'.
+//                    Epilogue: dK = scale R_n^T dK', dV (GQA sums stay inside the CTA).
+//   dq_kernel        one CTA per (query tile, head, batch): Q' and dO stay in shared memory;
+//                    for every visible key tile: S = Q' K'^T, dP = dO V^T, dS = P (dP - D),
+//                    dQ' += dS K'. Epilogue: dQ = scale R_m^T dQ'.
+// Rotations use the (cos, sin) table; the rotated operands are rounded to bf16 (the other
+// operands of these contractions are bf16). Every wait is bounded (see ptx.cuh).
+//
+// Warp roles (12 warps): 0 TMA, 1 MMA, 4-7 element-wise (one thread per TMEM lane/row),
+// 8-11 rotate Q/K tiles in shared memory.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace afx {
+
+namespace {
+
+constexpr int kBwdThreads = 384;
+constexpr int kT = 128;  // tile edge (keys and queries)
+
+// Rotate a [128 x D] bf16 tile (128B-swizzled panels) in place: row r at position pos0 + r.
+// Executed by 128 threads (t = 0..127); rows at or beyond N are left untouched.
+template <int D>
+__device__ __forceinline__ void rotate_tile_bf16(uint8_t* tile, int pos0, int N,
+                                                 const float2* __restrict__ cs, int t) {
+  constexpr int CP = D / 16;
+  for (int it = t; it < kT * CP; it += 128) {
+    const int row = it / CP, c = it % CP;
+    const int pos = pos0 + row;
+    if (pos >= N) continue;
+    uint32_t offl, offh;
+    if (D == 128) {
+      offl = sw128_offset(row, c);
+      offh = offl + kT * 128;
+    } else {
+      offl = sw128_offset(row, c);
+      offh = sw128_offset(row, c + 4);
+    }
+    uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
+    uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
+    rot_chunk<false>(lo, hi, cs + (size_t)pos * (D / 2) + c * 8);
+    *reinterpret_cast<uint4*>(tile + offl) = lo;
+    *reinterpret_cast<uint4*>(tile + offh) = hi;
+  }
+}
+
+// Apply scale * R_pos^T to a row of D fp32 values held in registers and store it as bf16.
+template <int D, bool ROPE>
+__device__ __forceinline__ void store_grad_row(float (&g)[D], float scale, int pos,
+                                               const float2* __restrict__ cs,
+                                               __nv_bfloat16* __restrict__ dst) {
+  if (ROPE) {
+#pragma unroll
+    for (int i = 0; i < D / 2; ++i) {
+      const float2 t = __ldg(cs + (size_t)pos * (D / 2) + i);
+      float yl, yh;
+      rot_pair(g[i], g[i + D / 2], t.x, -t.y, yl, yh);  // inverse rotation
+      g[i] = yl;
+      g[i + D / 2] = yh;
+    }
+  }
+  uint4* out = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int v = 0; v < D / 8; ++v) {
+    uint4 w;
+    w.x = pack_bf16x2(g[8 * v + 0] * scale, g[8 * v + 1] * scale);
+    w.y = pack_bf16x2(g[8 * v + 2] * scale, g[8 * v + 3] * scale);
+    w.z = pack_bf16x2(g[8 * v + 4] * scale, g[8 * v + 5] * scale);
+    w.w = pack_bf16x2(g[8 * v + 6] * scale, g[8 * v + 7] * scale);
+    out[v] = w;
+  }
+}
+
+// Load a TMEM row segment of D fp32 columns (one 32x32b load per 32 columns).
+template <int D>
+__device__ __forceinline__ void tmem_row(uint32_t taddr, float (&g)[D]) {
+#pragma unroll
+  for (int ch = 0; ch < D / 32; ++ch) {
+    uint32_t o[32];
+    tmem_ld32(taddr + ch * 32, o);
+    tmem_wait_ld();
+#pragma unroll
+    for (int e = 0; e < 32; ++e) g[ch * 32 + e] = __uint_as_float(o[e]);
+  }
+}
+
+template <int D>
+struct KvCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t TILE = kT * D * 2;
+  static constexpr int QST = 2;  // query / dO stages
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = TILE;
+  static constexpr uint32_t OFF_Q = 2 * TILE;
+  static constexpr uint32_t OFF_DO = OFF_Q + QST * TILE;
+  static constexpr uint32_t OFF_VEC = OFF_DO + QST * TILE;  // per stage: L (128 f32), D (128 f32)
+  static constexpr uint32_t OFF_CTL = OFF_VEC + QST * 1024;
+};
+
+struct KvCtl {
+  uint64_t k_full, v_full, k_ready;
+  uint64_t q_full[2], do_full[2], q_ready[2], vec_ready[2], stage_free[2];
+  uint64_t st_full, p_full, mma_done, mma_final;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+template <int D>
+struct DqCfg {
+  static constexpr int PANELS = D / 64;
+  static constexpr uint32_t TILE = kT * D * 2;
+  static constexpr int ST = 2;  // K/V stages
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_DO = TILE;
+  static constexpr uint32_t OFF_K = 2 * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
+  static constexpr uint32_t OFF_CTL = OFF_V + ST * TILE;
+};
+
+struct DqCtl {
+  uint64_t q_full, do_full, q_ready;
+  uint64_t k_full[2], v_full[2], k_ready[2], kv_free[2];
+  uint64_t s_full, p_full, mma_done, mma_final;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+__host__ __device__ constexpr size_t kv_smem_bytes(int D) {
+  return 1024 + (2 + 2 * 2) * (size_t)(kT * D * 2) + 2 * 1024 + sizeof(KvCtl);
+}
+__host__ __device__ constexpr size_t dq_smem_bytes(int D) {
+  return 1024 + (2 + 2 * 2) * (size_t)(kT * D * 2) + sizeof(DqCtl);
+}
+
+// Query tiles that can see key tile j (FULL: all; causal: i >= j).
+__device__ __forceinline__ int first_q_tile(const BwdParams& p, int j) { return p.causal ? j : 0; }
+// Key tiles visible from query tile i.
+__device__ __forceinline__ int last_k_tile(const BwdParams& p, int i, int TK) {
+  return p.causal ? min(i + 1, TK) : TK;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------------------------
+// D = rowsum(dO * O)
+// ---------------------------------------------------------------------------------------------
+__global__ void bwd_pre_kernel(const __grid_constant__ BwdParams p) {
+  const int tpr = p.d / 8;  // threads per row
+  const int64_t rows = (int64_t)p.B * p.Hq * p.N;
+  const int64_t row = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) / tpr;
+  const int c = threadIdx.x % tpr;
+  float acc = 0.f;
+  if (row < rows) {
+    const int n = static_cast<int>(row % p.N);
+    const int64_t bh = row / p.N;
+    const int h = static_cast<int>(bh % p.Hq);
+    const int64_t b = bh / p.Hq;
+    const uint4 o = *reinterpret_cast<const uint4*>(p.o + b * p.o_s[0] + h * p.o_s[1] + n * p.o_s[2] + c * 8);
+    const uint4 g = *reinterpret_cast<const uint4*>(p.dout + b * p.do_s[0] + h * p.do_s[1] + n * p.do_s[2] + c * 8);
+    const uint32_t* ow = reinterpret_cast<const uint32_t*>(&o);
+    const uint32_t* gw = reinterpret_cast<const uint32_t*>(&g);
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+      acc += bf16lo_to_f32(ow[w]) * bf16lo_to_f32(gw[w]) + bf16hi_to_f32(ow[w]) * bf16hi_to_f32(gw[w]);
+  }
+  for (int off = tpr / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (row < rows && c == 0) p.Dvec[row] = acc;
+}
+
+// ---------------------------------------------------------------------------------------------
+// dK, dV
+// ---------------------------------------------------------------------------------------------
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
+  using C = KvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  KvCtl* ctl = reinterpret_cast<KvCtl*>(smem + C::OFF_CTL);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int TK = (p.N + kT - 1) / kT;
+  const int TQ = TK;
+  // longest first: key tile 0 sees the most query tiles under causal masking
+  const int per_j = p.B * p.Hkv;
+  const int j = static_cast<int>(blockIdx.x) / per_j;
+  const int rem = static_cast<int>(blockIdx.x) % per_j;
+  const int b = rem / p.Hkv, kvh = rem % p.Hkv;
+  const int i0 = first_q_tile(p, j);
+  const int nq = TQ - i0;             // query tiles per head
+  const int total = p.g * nq;         // (head, query tile) items
+  int* status = p.status;
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  if (tid == 0) {
+    mbar_init(&ctl->k_full, 1);
+    mbar_init(&ctl->v_full, 1);
+    mbar_init(&ctl->k_ready, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl->q_full[s], 1);
+      mbar_init(&ctl->do_full[s], 1);
+      mbar_init(&ctl->q_ready[s], 128);
+      mbar_init(&ctl->vec_ready[s], 128);
+      mbar_init(&ctl->stage_free[s], 1);
+    }
+    mbar_init(&ctl->st_full, 1);
+    mbar_init(&ctl->p_full, 128);
+    mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->mma_final, 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  // TMEM: dV [0, D), dK' [D, 2D), S^T [2D, 2D+128), dP^T [2D+128, 2D+256)
+  const uint32_t T_DV = 0, T_DK = D, T_S = 2 * D, T_DP = 2 * D + 128;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- TMA: K, V once; then Q and dO for every (head, query tile) ----
+      tma_prefetch_desc(&p.tmQ);
+      tma_prefetch_desc(&p.tmK);
+      tma_prefetch_desc(&p.tmV);
+      tma_prefetch_desc(&p.tmDO);
+      mbar_arrive_expect_tx(&ctl->k_full, C::TILE);
+      for (int pn = 0; pn < C::PANELS; ++pn)
+        tma_load_4d(smem + C::OFF_K + pn * (kT * 128), &p.tmK, &ctl->k_full, pn * 64, j * kT, kvh, b);
+      mbar_arrive_expect_tx(&ctl->v_full, C::TILE);
+      for (int pn = 0; pn < C::PANELS; ++pn)
+        tma_load_4d(smem + C::OFF_V + pn * (kT * 128), &p.tmV, &ctl->v_full, pn * 64, j * kT, kvh, b);
+      int it = 0;
+      for (; it < total; ++it) {
+        const int s = it & 1;
+        const int h = kvh * p.g + it / nq, qi = i0 + it % nq;
+        if (it >= 2 && !mbar_wait(&ctl->stage_free[s], ((it >> 1) - 1) & 1, status, abort_flag)) break;
+        mbar_arrive_expect_tx(&ctl->q_full[s], C::TILE);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::OFF_Q + s * C::TILE + pn * (kT * 128), &p.tmQ, &ctl->q_full[s],
+                      pn * 64, qi * kT, h, b);
+        mbar_arrive_expect_tx(&ctl->do_full[s], C::TILE);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::OFF_DO + s * C::TILE + pn * (kT * 128), &p.tmDO, &ctl->do_full[s],
+                      pn * 64, qi * kT, h, b);
+      }
+      mbar_wait(&ctl->k_full, 0, status, nullptr);
+      mbar_wait(&ctl->v_full, 0, status, nullptr);
+      for (int k = max(0, it - 2); k < it; ++k) {
+        mbar_wait(&ctl->q_full[k & 1], (k >> 1) & 1, status, nullptr);
+        mbar_wait(&ctl->do_full[k & 1], (k >> 1) & 1, status, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMA ----
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, kT, 0, 0);  // S^T, dP^T: both K-major
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // dV, dK': B MN-major
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      bool ok = mbar_wait(&ctl->k_ready, 0, status, abort_flag) &&
+                mbar_wait(&ctl->v_full, 0, status, abort_flag);
+      for (int it = 0; ok && it < total; ++it) {
+        const int s = it & 1;
+        const uint32_t ph = (it >> 1) & 1;
+        if (!mbar_wait(&ctl->q_ready[s], ph, status, abort_flag)) break;
+        if (!mbar_wait(&ctl->do_full[s], ph, status, abort_flag)) break;
+        if (it > 0 && !mbar_wait(&ctl->mma_done, (it - 1) & 1, status, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+          mma_ss(tmem + T_S, smem_desc_sw128(sK + koff, 16, 1024),
+                 smem_desc_sw128(sQ + s * C::TILE + koff, 16, 1024), idesc_st, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+          mma_ss(tmem + T_DP, smem_desc_sw128(sV + koff, 16, 1024),
+                 smem_desc_sw128(sDO + s * C::TILE + koff, 16, 1024), idesc_st, kk > 0);
+        }
+        mma_commit(&ctl->st_full);
+        if (!mbar_wait(&ctl->p_full, it & 1, status, abort_flag)) break;
+        tc_fence_after();
+        // dV += P^T dO ; dK' += dS^T Q'   (A from TMEM, B = dO / Q' MN-major)
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk) {
+          mma_ts(tmem + T_DV, tmem + T_S + kk * 8,
+                 smem_desc_sw128(sDO + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + T_DK, tmem + T_DP + kk * 8,
+                 smem_desc_sw128(sQ + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ctl->mma_done);
+        mma_commit(&ctl->stage_free[s]);
+      }
+      mma_commit(&ctl->mma_final);
+      mbar_wait(&ctl->mma_final, 0, status, nullptr);
+    }
+  } else if (warp >= 8) {
+    // ---- rotators: K once, then each Q tile ----
+    const int t = tid - 256;
+    if (ROPE) {
+      if (mbar_wait(&ctl->k_full, 0, status, abort_flag))
+        rotate_tile_bf16<D>(smem + C::OFF_K, j * kT, p.N, p.rope_cs, t);
+      fence_proxy_async_smem();
+    } else {
+      mbar_wait(&ctl->k_full, 0, status, abort_flag);
+    }
+    mbar_arrive(&ctl->k_ready);
+    for (int it = 0; it < total; ++it) {
+      const int s = it & 1;
+      const int qi = i0 + it % nq;
+      if (!mbar_wait(&ctl->q_full[s], (it >> 1) & 1, status, abort_flag)) break;
+      if (ROPE) {
+        rotate_tile_bf16<D>(smem + C::OFF_Q + s * C::TILE, qi * kT, p.N, p.rope_cs, t);
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(&ctl->q_ready[s]);
+    }
+  } else if (warp >= 4) {
+    // ---- element-wise: thread = key row n of the tile ----
+    const int r = (warp - 4) * 32 + lane;
+    const int n = j * kT + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);
+    bool ok = true;
+    const float c2 = p.scale_log2;
+    for (int it = 0; it < total; ++it) {
+      const int s = it & 1;
+      const int h = kvh * p.g + it / nq, qi = i0 + it % nq;
+      const int m0 = qi * kT;
+      // stage L (log2 units) and D of this query tile; masked rows get L = +inf (P = 0)
+      {
+        const int m = m0 + r;
+        float l2 = __int_as_float(0x7f800000), dd = 0.f;
+        if (m < p.N) {
+          const float l = p.lse[((int64_t)b * p.Hq + h) * p.N + m];
+          l2 = (l == kNegInf) ? __int_as_float(0x7f800000) : l * kLog2e;
+          dd = p.Dvec[((int64_t)b * p.Hq + h) * p.N + m];
+        }
+        vec[s * 256 + r] = l2;
+        vec[s * 256 + 128 + r] = dd;
+      }
+      named_bar_sync(1, 128);
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->st_full, it & 1, status, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool diag = p.causal && (qi == j);
+      // 32 columns at a time; P / dS chunk c lands in columns already read (c/2 < c+1 chunks)
+#pragma unroll
+      for (int ch = 0; ch < kT / 32; ++ch) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_off + T_S + ch * 32, sr);
+        tmem_ld32(tmem + lane_off + T_DP + ch * 32, dr);
+        tmem_wait_ld();
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = ch * 32 + 2 * c + e;
+            float pr = ex2_approx(__fmaf_rn(__uint_as_float(sr[2 * c + e]), c2, -vec[s * 256 + col]));
+            if (diag && m0 + col < n) pr = 0.f;
+            pv[e] = pr;
+            dv[e] = pr * (__uint_as_float(dr[2 * c + e]) - vec[s * 256 + 128 + col]);
+          }
+          pk[c] = pack_bf16x2(pv[0], pv[1]);
+          dk[c] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_st16(tmem + lane_off + T_S + ch * 16, pk);
+        tmem_st16(tmem + lane_off + T_DP + ch * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ctl->p_full);
+    }
+    // ---- epilogue ----
+    if (ok && total > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, (total - 1) & 1, status, abort_flag));
+      tc_fence_after();
+    }
+    float g[D];
+    if (ok && total > 0) tmem_row<D>(tmem + lane_off + T_DV, g);
+    else
+#pragma unroll
+      for (int c = 0; c < D; ++c) g[c] = 0.f;
+    if (n < p.N)
+      store_grad_row<D, false>(g, 1.f, n, p.rope_cs,
+                               p.dv + b * p.dv_s[0] + kvh * p.dv_s[1] + (int64_t)n * p.dv_s[2]);
+    if (ok && total > 0) tmem_row<D>(tmem + lane_off + T_DK, g);
+    else
+#pragma unroll
+      for (int c = 0; c < D; ++c) g[c] = 0.f;
+    if (n < p.N)
+      store_grad_row<D, ROPE>(g, p.scale, n, p.rope_cs,
+                              p.dk + b * p.dk_s[0] + kvh * p.dk_s[1] + (int64_t)n * p.dk_s[2]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------------------------
+// dQ
+// ---------------------------------------------------------------------------------------------
+template <int D, bool ROPE>
+__global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  DqCtl* ctl = reinterpret_cast<DqCtl*>(smem + C::OFF_CTL);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int TQ = (p.N + kT - 1) / kT;
+  const int per_i = p.B * p.Hq;
+  const int i = TQ - 1 - static_cast<int>(blockIdx.x) / per_i;  // longest first
+  const int rem = static_cast<int>(blockIdx.x) % per_i;
+  const int b = rem / p.Hq, h = rem % p.Hq;
+  const int kvh = h / p.g;
+  const int nk = last_k_tile(p, i, TQ);
+  int* status = p.status;
+  volatile int* abort_flag = &ctl->abort_flag;
+
+  if (tid == 0) {
+    mbar_init(&ctl->q_full, 1);
+    mbar_init(&ctl->do_full, 1);
+    mbar_init(&ctl->q_ready, 128);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl->k_full[s], 1);
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->k_ready[s], 128);
+      mbar_init(&ctl->kv_free[s], 1);
+    }
+    mbar_init(&ctl->s_full, 1);
+    mbar_init(&ctl->p_full, 128);
+    mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->mma_final, 1);
+    ctl->abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(&ctl->tmem_base, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+  // TMEM: dQ' [0, D), S [128, 256), dP [256, 384)
+  const uint32_t T_DQ = 0, T_S = 128, T_DP = 256;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_desc(&p.tmQ);
+      tma_prefetch_desc(&p.tmK);
+      tma_prefetch_desc(&p.tmV);
+      tma_prefetch_desc(&p.tmDO);
+      mbar_arrive_expect_tx(&ctl->q_full, C::TILE);
+      for (int pn = 0; pn < C::PANELS; ++pn)
+        tma_load_4d(smem + C::OFF_Q + pn * (kT * 128), &p.tmQ, &ctl->q_full, pn * 64, i * kT, h, b);
+      mbar_arrive_expect_tx(&ctl->do_full, C::TILE);
+      for (int pn = 0; pn < C::PANELS; ++pn)
+        tma_load_4d(smem + C::OFF_DO + pn * (kT * 128), &p.tmDO, &ctl->do_full, pn * 64, i * kT, h, b);
+      int jt = 0;
+      for (; jt < nk; ++jt) {
+        const int s = jt & 1;
+        if (jt >= 2 && !mbar_wait(&ctl->kv_free[s], ((jt >> 1) - 1) & 1, status, abort_flag)) break;
+        mbar_arrive_expect_tx(&ctl->k_full[s], C::TILE);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::OFF_K + s * C::TILE + pn * (kT * 128), &p.tmK, &ctl->k_full[s],
+                      pn * 64, jt * kT, kvh, b);
+        mbar_arrive_expect_tx(&ctl->v_full[s], C::TILE);
+        for (int pn = 0; pn < C::PANELS; ++pn)
+          tma_load_4d(smem + C::OFF_V + s * C::TILE + pn * (kT * 128), &p.tmV, &ctl->v_full[s],
+                      pn * 64, jt * kT, kvh, b);
+      }
+      mbar_wait(&ctl->q_full, 0, status, nullptr);
+      mbar_wait(&ctl->do_full, 0, status, nullptr);
+      for (int k = max(0, jt - 2); k < jt; ++k) {
+        mbar_wait(&ctl->k_full[k & 1], (k >> 1) & 1, status, nullptr);
+        mbar_wait(&ctl->v_full[k & 1], (k >> 1) & 1, status, nullptr);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, kT, 0, 0);  // S, dP: both K-major
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);   // dQ': B = K' MN-major
+      const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      bool ok = mbar_wait(&ctl->q_ready, 0, status, abort_flag) &&
+                mbar_wait(&ctl->do_full, 0, status, abort_flag);
+      for (int jt = 0; ok && jt < nk; ++jt) {
+        const int s = jt & 1;
+        const uint32_t ph = (jt >> 1) & 1;
+        if (!mbar_wait(&ctl->k_ready[s], ph, status, abort_flag)) break;
+        if (!mbar_wait(&ctl->v_full[s], ph, status, abort_flag)) break;
+        if (jt > 0 && !mbar_wait(&ctl->mma_done, (jt - 1) & 1, status, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+          mma_ss(tmem + T_S, smem_desc_sw128(sQ + koff, 16, 1024),
+                 smem_desc_sw128(sK + s * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+          mma_ss(tmem + T_DP, smem_desc_sw128(sDO + koff, 16, 1024),
+                 smem_desc_sw128(sV + s * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
+        }
+        mma_commit(&ctl->s_full);
+        if (!mbar_wait(&ctl->p_full, jt & 1, status, abort_flag)) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + T_DQ, tmem + T_S + kk * 8,
+                 smem_desc_sw128(sK + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
+                 (jt > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl->mma_done);
+        mma_commit(&ctl->kv_free[s]);
+      }
+      mma_commit(&ctl->mma_final);
+      mbar_wait(&ctl->mma_final, 0, status, nullptr);
+    }
+  } else if (warp >= 8) {
+    const int t = tid - 256;
+    if (mbar_wait(&ctl->q_full, 0, status, abort_flag) && ROPE) {
+      rotate_tile_bf16<D>(smem + C::OFF_Q, i * kT, p.N, p.rope_cs, t);
+      fence_proxy_async_smem();
+    }
+    mbar_arrive(&ctl->q_ready);
+    for (int jt = 0; jt < nk; ++jt) {
+      const int s = jt & 1;
+      if (!mbar_wait(&ctl->k_full[s], (jt >> 1) & 1, status, abort_flag)) break;
+      if (ROPE) {
+        rotate_tile_bf16<D>(smem + C::OFF_K + s * C::TILE, jt * kT, p.N, p.rope_cs, t);
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(&ctl->k_ready[s]);
+    }
+  } else if (warp >= 4) {
+    // ---- element-wise: thread = query row m ----
+    const int r = (warp - 4) * 32 + lane;
+    const int m = i * kT + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    float l2 = __int_as_float(0x7f800000), dd = 0.f;
+    if (m < p.N) {
+      const float l = p.lse[((int64_t)b * p.Hq + h) * p.N + m];
+      l2 = (l == kNegInf) ? __int_as_float(0x7f800000) : l * kLog2e;
+      dd = p.Dvec[((int64_t)b * p.Hq + h) * p.N + m];
+    }
+    bool ok = true;
+    const float c2 = p.scale_log2;
+    for (int jt = 0; jt < nk; ++jt) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->s_full, jt & 1, status, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int k0 = jt * kT;
+      const bool edge = (p.causal && jt == i) || (k0 + kT > p.N);
+#pragma unroll
+      for (int ch = 0; ch < kT / 32; ++ch) {
+        uint32_t sr[32], dr[32];
+        tmem_ld32(tmem + lane_off + T_S + ch * 32, sr);
+        tmem_ld32(tmem + lane_off + T_DP + ch * 32, dr);
+        tmem_wait_ld();
+        uint32_t dk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          float dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int col = ch * 32 + 2 * c + e;
+            float pr = ex2_approx(__fmaf_rn(__uint_as_float(sr[2 * c + e]), c2, -l2));
+            if (edge && ((p.causal && k0 + col > m) || k0 + col >= p.N)) pr = 0.f;
+            dv[e] = pr * (__uint_as_float(dr[2 * c + e]) - dd);
+          }
+          dk[c] = pack_bf16x2(dv[0], dv[1]);
+        }
+        tmem_st16(tmem + lane_off + T_S + ch * 16, dk);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&ctl->p_full);
+    }
+    if (ok && nk > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, (nk - 1) & 1, status, abort_flag));
+      tc_fence_after();
+    }
+    float g[D];
+    if (ok && nk > 0) tmem_row<D>(tmem + lane_off + T_DQ, g);
+    else
+#pragma unroll
+      for (int c = 0; c < D; ++c) g[c] = 0.f;
+    if (m < p.N)
+      store_grad_row<D, ROPE>(g, p.scale, m, p.rope_cs,
+                              p.dq + b * p.dq_s[0] + h * p.dq_s[1] + (int64_t)m * p.dq_s[2]);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------------------------
+cudaError_t launch_bwd(const BwdParams& p, bool rope, cudaStream_t stream) {
+  const int d = p.d;
+  {
+    const int64_t threads = (int64_t)p.B * p.Hq * p.N * (d / 8);
+    const int block = 256;
+    bwd_pre_kernel<<<static_cast<int>((threads + block - 1) / block), block, 0, stream>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  const int T = (p.N + kT - 1) / kT;
+  void (*kv)(BwdParams) = nullptr;
+  void (*dq)(BwdParams) = nullptr;
+  if (d == 128) {
+    kv = rope ? dkdv_kernel<128, true> : dkdv_kernel<128, false>;
+    dq = rope ? dq_kernel<128, true> : dq_kernel<128, false>;
+  } else {
+    kv = rope ? dkdv_kernel<64, true> : dkdv_kernel<64, false>;
+    dq = rope ? dq_kernel<64, true> : dq_kernel<64, false>;
+  }
+  const size_t s1 = kv_smem_bytes(d), s2 = dq_smem_bytes(d);
+  cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(dq, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s2);
+  if (e != cudaSuccess) return e;
+  kv<<<T * p.B * p.Hkv, kBwdThreads, s1, stream>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dq<<<T * p.B * p.Hq, kBwdThreads, s2, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace afx

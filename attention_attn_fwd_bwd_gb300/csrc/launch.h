@@ -42,6 +42,22 @@ struct DecParams {
   int* status;
 };
 
+struct BwdParams {
+  CUtensorMap tmQ, tmK, tmV, tmDO;  // bf16 [B, H, N, d], box (64, 128, 1, 1)
+  const __nv_bfloat16* o;           // forward output (for D = rowsum(dO * O))
+  const __nv_bfloat16* dout;
+  int64_t o_s[3], do_s[3];
+  const float* lse;                 // [B, Hq, N] natural log
+  float* Dvec;                      // [B, Hq, N] workspace
+  __nv_bfloat16 *dq, *dk, *dv;
+  int64_t dq_s[3], dk_s[3], dv_s[3];
+  const float2* rope_cs;
+  int B, Hq, Hkv, N, d, g, causal;
+  float scale, scale_log2;
+  int* status;
+};
+cudaError_t launch_bwd(const BwdParams& p, bool rope, cudaStream_t stream);
+
 size_t decode_smem_size(int d);
 cudaError_t launch_decode(const DecParams& p, int d, bool rope_q, cudaStream_t stream);
 

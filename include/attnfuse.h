@@ -133,6 +133,9 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
  * atomics. Gradients are with respect to the un-rotated q and k (the inverse rotation is
  * applied in the epilogues) and dk, dv are summed over each GQA group.
  * out and lse are the forward's outputs. Supported variants: FULL or CAUSAL mask, no bias.
+ * ROPE_PREROTATE is computed like ROPE_FUSED (the gradients are the same function). The
+ * recomputed scores use bf16-rounded rotated operands; workspace holds the (cos, sin) table
+ * (rotating modes) and D.
  * ------------------------------------------------------------------------------------------ */
 attnfuse_status attnfuse_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
                                             attnfuse_rope_mode rope_mode, size_t* bytes);

@@ -2,7 +2,9 @@
 
 Tolerances (the target's stated bar): bf16 outputs within max-abs 2e-2 and mean-abs 2e-3 of
 the oracle; LSE within 1e-3 relative (|d| <= 1e-3 * max(1, |ref|)); gradients within
-5e-2 * max|ref grad| per tensor; tile-visit sets bit-exact.
+5e-2 * max|ref grad| per tensor; tile-visit sets bit-exact. A gradient that is exactly zero
+in exact arithmetic (one visible key: dS = P (dP - D) = 0) is held to an absolute floor of
+5e-2 * 1e-4, far below any non-degenerate gradient of unit-variance inputs.
 """
 import numpy as np
 import torch
@@ -11,6 +13,7 @@ O_MAX_ABS = 2e-2
 O_MEAN_ABS = 2e-3
 LSE_REL = 1e-3
 GRAD_REL_MAX = 5e-2
+GRAD_ABS_FLOOR = 1e-4
 
 
 def f64(t):
@@ -46,7 +49,7 @@ def check_grad(got, ref, what):
     got, ref = f64(got), f64(ref)
     assert got.shape == ref.shape
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    scale = max(np.abs(ref).max(), 1e-30)
+    scale = max(np.abs(ref).max(), GRAD_ABS_FLOOR)
     err = np.abs(got - ref).max()
     assert err <= GRAD_REL_MAX * scale, f"{what}: max err {err:.3e} > {GRAD_REL_MAX} * {scale:.3e}"
     return err / scale
