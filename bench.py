@@ -45,6 +45,10 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="llama8b_fused", choices=sorted(WORKLOADS))
     ap.add_argument("--sweep", action="store_true", help="fused vs pre-rotated N sweep")
+    ap.add_argument("--train", action="store_true",
+                    help="forward + backward at B=8 Hq=32 Hkv=8 d=128, N=2048 and 4096")
+    ap.add_argument("--variants", action="store_true",
+                    help="mask-variant forwards at B=2 H=16 N=4096 d=64 (window, ALiBi, BigBird)")
     ap.add_argument("--decode", action="store_true",
                     help="split-KV decode at the Llama-3-70B head shape (B=1, 8; splits sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -426,6 +430,99 @@ def run_profile(args):
     print(json.dumps({"profile": args.workload, "ok": True}))
 
 
+def _time_ms(fn, reps=20, warm=3):
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    samples = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        samples.append(e0.elapsed_time(e1))
+    samples.sort()
+    return samples[len(samples) // 2], samples[0], samples[int(0.9 * len(samples))]
+
+
+def run_train_bench(args):
+    """Training-step attention: fused-RoPE causal forward (O, LSE) and the 3-kernel backward."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    dev = torch.device("cuda")
+    peaks, _ = measured_peaks()
+    peak = float(peaks["bf16_tflops"])
+    B, Hq, Hkv, d, theta = 8, 32, 8, 128, 5e5
+    for N in (2048, 4096):
+        x = inputs.prefill(B, Hq, Hkv, N, d, seed=4000 + N, with_dout=True)
+        q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+        out = torch.empty_like(q)
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        wsf = torch.empty(af.fwd_workspace_size(B, Hq, Hkv, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(af.bwd_workspace_size(B, Hq, Hkv, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
+        fwd = lambda: af.fwd(q, k, v, rope_theta=theta, out=out, lse=lse, workspace=wsf)
+        bwd = lambda: af.bwd(q, k, v, out, lse, do, rope_theta=theta, dq=dq, dk=dk, dv=dv, workspace=wsb)
+        tf, tf_min, tf_p90 = _time_ms(fwd)
+        tb, tb_min, tb_p90 = _time_ms(bwd)
+        fl = causal_flops(B, Hq, N, d)
+        print(json.dumps({"train": "fused_rope_causal", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+                          "fwd_ms": tf, "bwd_ms": tb, "fwd_tflops": fl / tf / 1e9,
+                          "bwd_tflops": 2.5 * fl / tb / 1e9,
+                          "total_tflops": 3.5 * fl / (tf + tb) / 1e9,
+                          "bwd_frac_of_peak": 2.5 * fl / tb / 1e9 / peak,
+                          "total_frac_of_peak": 3.5 * fl / (tf + tb) / 1e9 / peak,
+                          "fwd_min_p90_ms": [tf_min, tf_p90], "bwd_min_p90_ms": [tb_min, tb_p90],
+                          "launches": {"fwd": 2, "bwd": 4}}), flush=True)
+
+
+def run_variants_bench(args):
+    """Mask-variant forwards at B=2, H=16, N=4096, d=64, theta=1e4, fused RoPE."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    import oracle
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    dev = torch.device("cuda")
+    peaks, _ = measured_peaks()
+    B, H, N, d = 2, 16, 4096, 64
+    x = inputs.prefill(B, H, H, N, d, seed=3000)
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    rp, ci = inputs.bigbird_csr(N // 64, seed=3003)
+    cases = {
+        "window1024_causal": (af.Variant(mask=af.MASK_WINDOW, window=1024, causal=True),
+                              oracle.Variant(mask=2, window=1024, causal=True)),
+        "alibi_causal": (af.Variant(mask=af.MASK_CAUSAL, bias=af.BIAS_ALIBI,
+                                    alibi_slopes=torch.tensor(inputs.alibi_slopes(H), dtype=torch.float32, device=dev)),
+                         oracle.Variant(mask=1)),
+        "bigbird_blocksparse": (af.Variant(mask=af.MASK_BLOCK_SPARSE, bs_block=64,
+                                           bs_row_ptr=torch.tensor(rp, device=dev),
+                                           bs_col_idx=torch.tensor(ci, device=dev)),
+                                oracle.Variant(mask=3, bs_block=64, bs_row_ptr=rp, bs_col_idx=ci)),
+        "causal": (af.Variant(mask=af.MASK_CAUSAL), oracle.Variant(mask=1)),
+    }
+    for name, (gvar, ovar) in cases.items():
+        ws = torch.empty(af.fwd_workspace_size(B, H, H, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
+        out = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        t, tmin, tp90 = _time_ms(lambda: af.fwd(q, k, v, rope_theta=1e4, variant=gvar, out=out, lse=lse, workspace=ws))
+        pairs = oracle.allowed_pairs(N, ovar)
+        fl = 4.0 * d * B * H * pairs
+        print(json.dumps({"variant": name, "B": B, "H": H, "N": N, "d": d, "ms": t, "min_ms": tmin,
+                          "p90_ms": tp90, "allowed_pairs_per_head": pairs,
+                          "algorithmic_tflops": fl / t / 1e9,
+                          "frac_of_peak": fl / t / 1e9 / float(peaks["bf16_tflops"]),
+                          **({"active_blocks": int(len(ci)), "active_fraction": len(ci) / (N // 64) ** 2}
+                             if name.startswith("bigbird") else {})}), flush=True)
+
+
 def run_decode_bench(args):
     """Split-KV decode: Hq=64, Hkv=8, d=128, L=32768, q at 32767; K+V bytes / time (cold L2)."""
     import torch
@@ -500,6 +597,14 @@ def main():
     if args.decode:
         if rank == 0:
             run_decode_bench(args)
+        return
+    if args.train:
+        if rank == 0:
+            run_train_bench(args)
+        return
+    if args.variants:
+        if rank == 0:
+            run_variants_bench(args)
         return
     run_ours(args, rank, world)
     if world > 1:
