@@ -89,6 +89,8 @@ def load():
             "attnfuse_decode": ([P, ST, P, ST, P, ST, P, ST, P, I, I, I, I, I, I, F, F, I, I,
                                  P, S, P], I),
             "attnfuse_decode_auto_splits": ([I, I, I, ctypes.POINTER(I)], I),
+            "attnfuse_decode_noalloc": ([P, ST, P, ST, P, ST, P, ST, P, I, I, I, I, I, I, F, F, I,
+                                         I, P], I),
             "attnfuse_rope_prerotate": ([P, ST, P, I, I, I, I, F, P, S, P], I),
             "attnfuse_debug_wait_timeout": ([ctypes.c_uint64, P], I),
             "attnfuse_rope_table": ([P, S, I, I, F, P], I),

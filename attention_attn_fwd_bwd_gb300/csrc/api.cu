@@ -191,6 +191,10 @@ attnfuse_status to_dev_variant(const attnfuse_variant* v, int N, int Hq, Variant
 
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
 
+int set_last_error(int code, const char* msg) {
+  return fail(code, "%s", msg);
+}
+
 }  // namespace afx
 
 using namespace afx;

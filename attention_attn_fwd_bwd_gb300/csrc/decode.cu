@@ -17,7 +17,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstdio>
+#include <mutex>
 
+#include "../../include/attnfuse.h"
 #include "common.cuh"
 #include "launch.h"
 
@@ -393,3 +396,66 @@ cudaError_t launch_decode(const DecParams& p, int d, bool rope_q, cudaStream_t s
 }
 
 }  // namespace afx
+
+// ---------------------------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory.
+//
+// Some callers have no way to obtain a device workspace: a serving runtime whose memory is
+// entirely pre-reserved by its own allocator, a host program that links this library but has
+// no allocator API of its own to hand out scratch buffers, or a latency-critical path where a
+// cudaMalloc (which may synchronise the device) is not allowed. For them the split-KV partial
+// results live in one fixed array compiled into this library instead of in a caller buffer.
+// ---------------------------------------------------------------------------------------------
+namespace afx {
+
+// Scratch for attnfuse_decode_noalloc: the partial (acc, max, sum) rows of every split. Every
+// GPU that loads the library holds this array until the process exits.
+constexpr size_t kNoAllocScratchBytes = size_t(4) << 20;  // 4 MiB
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64] = {};
+
+// Device address of g_decode_scratch on the current device (looked up once per device).
+int scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_last_error(ATTNFUSE_ERR_CUDA, cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return set_last_error(ATTNFUSE_ERR_UNSUPPORTED, "device index out of range");
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* ptr = nullptr;
+    e = cudaGetSymbolAddress(&ptr, g_decode_scratch);
+    if (e != cudaSuccess) return set_last_error(ATTNFUSE_ERR_CUDA, cudaGetErrorString(e));
+    g_scratch_ptr[dev] = ptr;
+  }
+  *out = g_scratch_ptr[dev];
+  return ATTNFUSE_OK;
+}
+}  // namespace
+
+}  // namespace afx
+
+extern "C" attnfuse_status attnfuse_decode_noalloc(
+    const void* q, const int64_t q_strides[3], const void* k_cache, const int64_t k_strides[4],
+    const void* v_cache, const int64_t v_strides[4], void* out, const int64_t o_strides[3],
+    float* lse, int B, int Hq, int Hkv, int L, int d, int q_pos, float scale, float rope_theta,
+    attnfuse_rope_mode rope_mode, int num_splits, cudaStream_t stream) {
+  size_t need = 0;
+  attnfuse_status rc = attnfuse_decode_workspace_size(B, Hq, Hkv, L, d, num_splits, &need);
+  if (rc) return rc;
+  if (need > afx::kNoAllocScratchBytes) {
+    char msg[200];
+    snprintf(msg, sizeof(msg),
+             "attnfuse_decode_noalloc: this problem needs %zu bytes of scratch but the built-in "
+             "array holds %zu; use attnfuse_decode with a workspace or fewer splits",
+             need, afx::kNoAllocScratchBytes);
+    return afx::set_last_error(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, msg);
+  }
+  void* scratch = nullptr;
+  if ((rc = afx::scratch_address(&scratch))) return rc;
+  return attnfuse_decode(q, q_strides, k_cache, k_strides, v_cache, v_strides, out, o_strides, lse,
+                         B, Hq, Hkv, L, d, q_pos, scale, rope_theta, rope_mode, num_splits,
+                         scratch, afx::kNoAllocScratchBytes, stream);
+}

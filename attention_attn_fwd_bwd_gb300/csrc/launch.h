@@ -73,5 +73,7 @@ cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, i
                              int N, int d, const float2* cs, bool out_f16, bool keys,
                              cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
+// Record a message for attnfuse_last_error() and return code.
+int set_last_error(int code, const char* msg);
 
 }  // namespace afx

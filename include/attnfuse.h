@@ -172,6 +172,31 @@ attnfuse_status attnfuse_decode(const void* q, const int64_t q_strides[3], const
                                 attnfuse_rope_mode rope_mode, int num_splits, void* workspace,
                                 size_t workspace_bytes, cudaStream_t stream);
 
+/* attnfuse_decode for callers that cannot allocate device memory. (The paper has no
+ * counterpart; this is an interface choice of this library.)
+ * Some callers have no way to provide a device workspace: a serving runtime whose device memory
+ * is entirely pre-reserved by its own allocator, a host program without an allocator of its
+ * own to hand out scratch buffers, or a latency-critical path where a cudaMalloc (which may
+ * synchronise the device) is not allowed. This entry point takes the same arguments as
+ * attnfuse_decode minus the workspace and keeps the split-KV partial results in one fixed
+ * 4 MiB array compiled into the library (each GPU that loads the library holds it until the
+ * process exits). It allocates and frees nothing; the caller still passes q, the caches, out
+ * and lse.
+ *   - Problems whose partials need more than 4 MiB (attnfuse_decode_workspace_size) are
+ *     rejected with ATTNFUSE_ERR_WORKSPACE_TOO_SMALL and a message naming both sizes.
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
+ *     with that device current; make that first call before any stream capture.
+ *   - All calls share the array, which keeps the last call's contents (every value a call
+ *     reads is written by that same call first). Calls that overlap on the GPU, on one or
+ *     several streams, race on the array and must be serialised by the caller. */
+attnfuse_status attnfuse_decode_noalloc(const void* q, const int64_t q_strides[3],
+                                        const void* k_cache, const int64_t k_strides[4],
+                                        const void* v_cache, const int64_t v_strides[4], void* out,
+                                        const int64_t o_strides[3], float* lse, int B, int Hq,
+                                        int Hkv, int L, int d, int q_pos, float scale,
+                                        float rope_theta, attnfuse_rope_mode rope_mode,
+                                        int num_splits, cudaStream_t stream);
+
 /* Number of KV chunks attnfuse_decode uses for num_splits = 0 on the current device. */
 attnfuse_status attnfuse_decode_auto_splits(int B, int Hkv, int L, int* num_splits);
 
