@@ -61,6 +61,17 @@ def causal_flops(B, Hq, N, d):
     return 4.0 * d * B * Hq * N * (N + 1) / 2.0
 
 
+def max_over_ranks(value, device=None):
+    """Max of a per-rank float over all ranks (identity without a process group)."""
+    import torch
+
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -278,11 +289,7 @@ def run_ours(args, rank, world):
     ev1.record(stream)
     barrier()
     clk = clocks.stop()
-    elapsed_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(ev0.elapsed_time(ev1), dev)
     ms_per_step = elapsed_ms / args.steps
     value = world * flops / (ms_per_step * 1e-3) / 1e12
     assert af.device_status() == 0
@@ -321,11 +328,7 @@ def run_ours(args, rank, world):
             lse_h.copy_(sets[0]["lse"], non_blocking=True)
         ev1.record(stream)
         barrier()
-        e2e_ms = ev0.elapsed_time(ev1) / e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
+        e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, dev)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 

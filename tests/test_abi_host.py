@@ -1,0 +1,117 @@
+"""C-ABI boundary checks that need no GPU: every symbol declared in include/attnfuse.h is
+exported by libattnfuse.so, and argument validation returns the documented status codes
+before any CUDA call is made. No compute is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import attention_attn_fwd_bwd_gb300 as af
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, UNSUPPORTED, WS_SMALL = 0, 1, 2, 3
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_attn_fwd_bwd_gb300 import _build
+
+    _build.build()
+    return af.load()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "attnfuse.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(attnfuse_\w+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def _st(*v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+FAKE = ctypes.c_void_p(0x100000)  # 16-byte aligned, never dereferenced on these paths
+STR = _st(4 * 1024 * 128, 1024 * 128, 128, 1)
+
+
+def _fwd(lib, q=FAKE, qs=STR, B=1, Hq=4, Hkv=4, N=1024, d=128, scale=0.1, mode=1, var=None,
+         ws=FAKE, ws_bytes=1 << 30):
+    return lib.attnfuse_fwd(q, qs, FAKE, STR, FAKE, STR, FAKE, STR, None, B, Hq, Hkv, N, d, scale,
+                            1e4, mode, var, ws, ws_bytes, None)
+
+
+def test_fwd_validation(lib):
+    assert _fwd(lib, d=96) == UNSUPPORTED
+    assert _fwd(lib, Hq=6, Hkv=4) == UNSUPPORTED
+    assert _fwd(lib, q=None) == INVALID
+    assert b"q is NULL" in lib.attnfuse_last_error()
+    assert _fwd(lib, q=ctypes.c_void_p(0x100001)) == INVALID
+    assert _fwd(lib, qs=_st(4 * 1024 * 128, 1024 * 128, 128, 2)) == INVALID
+    assert _fwd(lib, qs=_st(4 * 1024 * 128, 1024 * 128, 130, 1)) == INVALID
+    assert _fwd(lib, scale=0.0) == INVALID
+    assert _fwd(lib, mode=7) == INVALID
+    assert _fwd(lib, ws=None, ws_bytes=0) == WS_SMALL
+    assert _fwd(lib, ws_bytes=1024) == WS_SMALL
+    v = af.CVariant()
+    v.mask = 3
+    v.bs_block = 64
+    assert _fwd(lib, var=ctypes.byref(v)) == INVALID  # CSR pointers missing
+    v.bs_block = 32
+    assert _fwd(lib, var=ctypes.byref(v)) == UNSUPPORTED
+    v = af.CVariant()
+    v.mask = 2
+    v.window = 0
+    assert _fwd(lib, var=ctypes.byref(v)) == INVALID
+    v = af.CVariant()
+    v.mask = 1
+    v.bias = 1
+    assert _fwd(lib, var=ctypes.byref(v)) == INVALID  # ALiBi slopes missing
+
+
+def test_workspace_sizes(lib):
+    n = ctypes.c_size_t()
+    assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 0, ctypes.byref(n)) == OK
+    assert n.value == 0
+    assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 1, ctypes.byref(n)) == OK
+    assert n.value == 4096 * 64 * 8  # (cos, sin) fp32 table
+    assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 2, ctypes.byref(n)) == OK
+    assert n.value == 4096 * 64 * 8 + 4 * 32 * 4096 * 128 * 2 + 4 * 8 * 4096 * 128 * 2
+    assert lib.attnfuse_fwd_workspace_size(1, 2, 2, 10, 64, 1, ctypes.byref(n)) == OK
+    assert n.value == 128 * 32 * 8  # the table always covers 128 positions
+    assert lib.attnfuse_bwd_workspace_size(8, 32, 8, 2048, 128, 1, ctypes.byref(n)) == OK
+    assert n.value == 2048 * 64 * 8 + 8 * 32 * 2048 * 4
+    assert lib.attnfuse_decode_workspace_size(1, 64, 8, 32768, 128, 8, ctypes.byref(n)) == OK
+    assert n.value == 64 * 8 * 128 * 4 + 2 * 2048  # acc + (max, sum), 256-byte aligned
+
+
+def test_decode_and_bwd_validation(lib):
+    q_st, c_st, o_st = _st(64 * 128, 128, 1), _st(8 * 32768 * 128, 32768 * 128, 128, 1), _st(64 * 128, 128, 1)
+    args = lambda Hq, Hkv, mode, ws_bytes: lib.attnfuse_decode(
+        FAKE, q_st, FAKE, c_st, FAKE, c_st, FAKE, o_st, None, 1, Hq, Hkv, 32768, 128, 32767,
+        0.088, 5e5, mode, 8, FAKE, ws_bytes, None)
+    assert args(64, 1, 1, 1 << 30) == UNSUPPORTED  # g = 64 > 32
+    assert args(64, 8, 2, 1 << 30) == UNSUPPORTED  # decode rotates q only
+    assert args(64, 8, 1, 100) == WS_SMALL
+    rc = lib.attnfuse_decode_noalloc(FAKE, q_st, FAKE, c_st, FAKE, c_st, FAKE, o_st, None, 8, 64, 8,
+                                     32768, 128, 32767, 0.088, 5e5, 1, 128, None)
+    assert rc == WS_SMALL and b"4194304" in lib.attnfuse_last_error()
+    v = af.CVariant()
+    v.mask = 2
+    v.window = 16
+    s = STR
+    rc = lib.attnfuse_bwd(FAKE, s, FAKE, s, FAKE, s, FAKE, s, FAKE, FAKE, s, FAKE, s, FAKE, s,
+                          FAKE, s, 1, 4, 4, 1024, 128, 0.1, 1e4, 1, ctypes.byref(v), FAKE, 1 << 30,
+                          None)
+    assert rc == UNSUPPORTED
+
+
+def test_version(lib):
+    assert lib.attnfuse_version() >= 100
