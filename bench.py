@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
+    ap.add_argument("--profile-target", default="fwd", choices=["fwd", "decode", "train"],
+                    help="--profile: forward workload, Llama-3-70B decode (B=8) or fwd+bwd (N=2048)")
     return ap.parse_args()
 
 
@@ -415,40 +417,34 @@ def run_sweep(args):
 
 
 def run_profile(args):
-    """Warm-up call plus one call of the workload: a small, self-contained ncu target."""
+    """Warm-up call plus one call of a workload: a small, self-contained ncu target."""
     import torch
 
     import attention_attn_fwd_bwd_gb300 as af
     from attention_attn_fwd_bwd_gb300 import inputs
 
-    B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
-    rope_mode = {"fused": af.ROPE_FUSED, "prerotate": af.ROPE_PREROTATE, "none": af.ROPE_NONE}[mode]
-    x = inputs.prefill(B, Hq, Hkv, N, d, seed=2000)
-    q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
-    for _ in range(2):
-        out, lse = af.fwd(q, k, v, rope_theta=theta, rope_mode=rope_mode)
+    if args.profile_target == "decode":
+        x = inputs.decode(8, 64, 8, 32768, 128, seed=5008)
+        q, kc, vc = (x[n].cuda() for n in ("q", "k_cache", "v_cache"))
+        for _ in range(2):
+            af.decode(q, kc, vc, 32767, rope_theta=5e5)
+    elif args.profile_target == "train":
+        x = inputs.prefill(8, 32, 8, 2048, 128, seed=6048, with_dout=True)
+        q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+        for _ in range(2):
+            out, lse = af.fwd(q, k, v, rope_theta=5e5)
+            af.bwd(q, k, v, out, lse, do, rope_theta=5e5)
+    else:
+        B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
+        rope_mode = {"fused": af.ROPE_FUSED, "prerotate": af.ROPE_PREROTATE, "none": af.ROPE_NONE}[mode]
+        x = inputs.prefill(B, Hq, Hkv, N, d, seed=2000)
+        q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+        for _ in range(2):
+            af.fwd(q, k, v, rope_theta=theta, rope_mode=rope_mode)
     torch.cuda.synchronize()
     if af.device_status() != 0:
         raise SystemExit("device status reports a timeout")
-    print(json.dumps({"profile": args.workload, "ok": True}))
-
-
-def _time_ms(fn, reps=20, warm=3):
-    import torch
-
-    for _ in range(warm):
-        fn()
-    torch.cuda.synchronize()
-    samples = []
-    for _ in range(reps):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record()
-        fn()
-        e1.record()
-        torch.cuda.synchronize()
-        samples.append(e0.elapsed_time(e1))
-    samples.sort()
-    return samples[len(samples) // 2], samples[0], samples[int(0.9 * len(samples))]
+    print(json.dumps({"profile": args.profile_target, "ok": True}))
 
 
 def run_train_bench(args):
