@@ -191,11 +191,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int TK = (p.N + kT - 1) / kT;
   const int TQ = TK;
-  // longest first: key tile 0 sees the most query tiles under causal masking
-  const int per_j = p.B * p.Hkv;
-  const int j = static_cast<int>(blockIdx.x) / per_j;
-  const int rem = static_cast<int>(blockIdx.x) % per_j;
-  const int b = rem / p.Hkv, kvh = rem % p.Hkv;
+  // Group-major order: the CTAs running together share one (b, kv head) group, so that
+  // group's Q and dO (re-read by every key tile) stay in L2. Within a group, key tile 0 (the
+  // most query tiles under causal masking) goes first.
+  const int grp = static_cast<int>(blockIdx.x) / TK;
+  const int j = static_cast<int>(blockIdx.x) % TK;
+  const int b = grp / p.Hkv, kvh = grp % p.Hkv;
   const int i0 = first_q_tile(p, j);
   const int nq = TQ - i0;             // query tiles per head
   const int total = p.g * nq;         // (head, query tile) items

@@ -447,6 +447,25 @@ def run_profile(args):
     print(json.dumps({"profile": args.profile_target, "ok": True}))
 
 
+def _time_ms(fn, reps=20, warm=3):
+    """Median, min and p90 of fn() in ms (CUDA events on the current stream)."""
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    samples = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        torch.cuda.synchronize()
+        samples.append(e0.elapsed_time(e1))
+    samples.sort()
+    return samples[len(samples) // 2], samples[0], samples[int(0.9 * len(samples))]
+
+
 def run_train_bench(args):
     """Training-step attention: fused-RoPE causal forward (O, LSE) and the 3-kernel backward."""
     import torch
