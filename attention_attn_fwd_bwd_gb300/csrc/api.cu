@@ -76,12 +76,12 @@ attnfuse_status device_state(int** status) {
   return ATTNFUSE_OK;
 }
 
-// bf16 [B, H, N, d] view with element strides; box (64, 128, 1, 1), 128-byte swizzle.
+// bf16 [B, H, N, d] view with element strides; box (64, box_rows, 1, 1), 128-byte swizzle.
 attnfuse_status encode_bhnd(CUtensorMap* m, const void* ptr, const int64_t st[4], int B, int H,
-                            int N, int d, const char* name) {
+                            int N, int d, const char* name, int box_rows = 128) {
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
-  cuuint32_t box[4] = {64, 128, 1, 1};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -323,7 +323,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     qa = qr; ka = kr; qs = qs_c; ks = ks_c;
   }
   if ((rc = encode_bhnd(&p.tmQ, qa, qs, B, Hq, N, d, "q"))) return rc;
-  if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k"))) return rc;
+  // head dim 128 runs on CTA pairs, each loading 64-key halves of K
+  if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k", d == 128 ? 64 : 128))) return rc;
   if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v"))) return rc;
   p.rope_cs = cs;
   p.out = static_cast<__nv_bfloat16*>(out);
@@ -340,7 +341,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   if (grid > 0x7fffffff) return fail(ATTNFUSE_ERR_UNSUPPORTED, "problem too large (grid %lld)", (long long)grid);
   const int rk = rope_mode == ATTNFUSE_ROPE_FUSED ? kRopeFused
                  : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
-  cudaError_t e = launch_fwd(p, d, rk, (int)grid, stream);
+  cudaError_t e = d == 128 ? launch_fwd_pair(p, rk, (int)grid, stream)
+                           : launch_fwd(p, d, rk, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ok();
 }

@@ -1,5 +1,6 @@
-// Forward attention kernel for sm_103a (AttnFuse paper §4.1 fused RoPE, §2 online softmax,
-// §3.1 combinators, §4.3 block skipping), plus the RoPE table and pre-rotation kernels.
+// Forward attention kernel for head dim 64 on sm_103a (AttnFuse paper §4.1 fused RoPE, §2
+// online softmax, §3.1 combinators, §4.3 block skipping), plus the RoPE table and pre-rotation
+// kernels. Head dim 128 runs on CTA pairs (fwd_pair.cu).
 //
 // One CTA computes two 128-row query sub-tiles that read the same key/value head: either two
 // query heads of one GQA group at the same positions (they then share every rotated K tile),
@@ -704,16 +705,11 @@ __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb
 size_t fwd_smem_size(int d) { return fwd_smem_bytes(d); }
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream) {
+  if (d != 64) return cudaErrorInvalidValue;  // head dim 128 runs on CTA pairs (fwd_pair.cu)
   const size_t smem = fwd_smem_bytes(d);
-  void (*fn)(FwdParams) = nullptr;
-  if (d == 128)
-    fn = rope_kind == kRopeFused ? fwd_kernel<128, kRopeFused>
-         : rope_kind == kRopePrerotated ? fwd_kernel<128, kRopePrerotated>
-                                        : fwd_kernel<128, kRopeNone>;
-  else
-    fn = rope_kind == kRopeFused ? fwd_kernel<64, kRopeFused>
-         : rope_kind == kRopePrerotated ? fwd_kernel<64, kRopePrerotated>
-                                        : fwd_kernel<64, kRopeNone>;
+  void (*fn)(FwdParams) = rope_kind == kRopeFused        ? fwd_kernel<64, kRopeFused>
+                          : rope_kind == kRopePrerotated ? fwd_kernel<64, kRopePrerotated>
+                                                         : fwd_kernel<64, kRopeNone>;
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   fn<<<grid, kThreads, smem, stream>>>(p);

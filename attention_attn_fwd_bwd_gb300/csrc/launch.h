@@ -10,6 +10,7 @@ namespace afx {
 
 struct FwdParams {
   CUtensorMap tmQ, tmK, tmV;  // bf16 [B, H, N, d] maps, 128B swizzle, box (64, 128, 1, 1)
+                              // (tmK: box (64, 64, 1, 1) for head dim 128)
   const float2* rope_cs;      // (cos, sin) table [N][d/2] (fused RoPE only)
   __nv_bfloat16* out;
   int64_t o_sb, o_sh, o_sn;
@@ -66,7 +67,11 @@ size_t fwd_smem_size(int d);
 constexpr int kRopeNone = 0;        // bf16 inputs used as they are
 constexpr int kRopeFused = 1;       // rotated in shared memory by the kernel, rounded to fp16
 constexpr int kRopePrerotated = 2;  // rotated by the pre-rotation kernel into fp16 buffers
+// One CTA per 256 query rows (two 128-row sub-tiles); head dim 64.
 cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream);
+// Head dim 128: clusters of two CTAs, one per 256 query rows (tmK box of 64 rows).
+size_t fwd_pair_smem_size();
+cudaError_t launch_fwd_pair(const FwdParams& p, int rope_kind, int clusters, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
                               cudaStream_t stream);
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,

@@ -143,7 +143,7 @@ class ClockSampler:
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_attn_fwd_bwd_gb300", "csrc")
-    for name in ("fwd.cu", "ptx.cuh", "common.cuh", "launch.h"):
+    for name in ("fwd_pair.cu", "ptx.cuh", "common.cuh", "launch.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -343,7 +343,7 @@ def run_ours(args, rank, world):
         ach = flops / (kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "traffic": committed_traffic(args.workload),
-                "kernel": "fwd_kernel<128, fused>", "kernel_ms": kern_ms,
+                "kernel": "fwd_pair_kernel<fused RoPE, no bias> (2-CTA cluster)", "kernel_ms": kern_ms,
                 "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
                 "frac_of_sustained": ach / float(peaks.get("bf16_tflops_sustained", peak))}
     cpu = None
