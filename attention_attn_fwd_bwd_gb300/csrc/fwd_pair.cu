@@ -9,18 +9,18 @@
 // compared with one CTA doing both halves.
 //
 // TMEM (512 columns, same addresses in both CTAs):
-//   S[0] [0,128), S[1] [128,256)  scores, double-buffered so S(i+1) is computed while the
-//                                 softmax of tile i runs
+//   S[0] [0,128), S[1] [128,256)  scores of even / odd tiles, so S(i+1) is computed while
+//                                 the softmax of tile i runs
 //   O    [256,384)                output accumulator
 //   Q'   [384,448)                rotated queries, A operand of the score MMA
 //   P    [448,512)                probabilities (bf16), A operand of the PV MMA
 // Warp roles (16 warps):
 //   warp 0      TMA producer: Q once, then this CTA's halves of K and V tiles
-//   warp 1      MMA issuer (even CTA only): S(i+1) = Q' K^T, then O += P(i) V
-//   warp 2      K relay (no fused RoPE): forwards "K half landed" to the even CTA
-//   warp 3      V relay: forwards "V half landed" to the even CTA
-//   warps 4-11  softmax, one query row per thread; warps 4-7 take key columns 0-63 of each
-//               tile, warps 8-11 columns 64-127 (the row maxima are exchanged per tile)
+//   warp 1      score MMA issuer (even CTA only): S(i) = Q' K(i)^T
+//   warp 2      PV MMA issuer (even CTA only): O += P(i) V(i)
+//   warp 3      relay: forwards "K / V half landed" to the even CTA (K only without fused RoPE)
+//   warps 4-11  softmax, one query row per thread: warps 4-7 take the even kv tiles, warps
+//               8-11 the odd ones (full 128-column rows), sharing the O accumulator
 //   warps 12-15 K rotators (fused RoPE): rotate this CTA's 64 keys in shared memory
 // Every wait is bounded (see ptx.cuh).
 #include <cuda.h>
@@ -75,8 +75,8 @@ constexpr uint32_t kOffV = kOffK + kPKSt * kKHalf;
 constexpr uint32_t kOffCtl = kOffV + kPVSt * kVHalf;
 constexpr uint32_t kTmS = 0, kTmO = 256, kTmQ = 384, kTmP = 448;
 
-constexpr uint32_t kRegsLow = 56;     // warpgroup 0: TMA, MMA, relays
-constexpr uint32_t kRegsRot = 88;     // warpgroup 3: K rotation
+constexpr uint32_t kRegsLow = 48;     // warpgroup 0: TMA, MMA, relays
+constexpr uint32_t kRegsRot = 96;     // warpgroup 3: K rotation
 constexpr uint32_t kRegsSm = 184;     // warpgroups 1, 2: softmax
 static_assert(kRegsLow + kRegsRot + 2 * kRegsSm <= 4 * (65536 / kPThreads),
               "register split exceeds the registers the CTA is launched with");
@@ -84,12 +84,14 @@ static_assert(kRegsLow + kRegsRot + 2 * kRegsSm <= 4 * (65536 / kPThreads),
 struct PairCtl {
   // local TMA completion
   uint64_t q_full, k_full[kPKSt], v_full[kPVSt];
-  // pair-MMA commits (multicast to both CTAs)
-  uint64_t k_empty[kPKSt], v_empty[kPVSt], s_full[2], pv_done, mma_final;
+  // pair-MMA commits (multicast to both CTAs); pv_done[t] completes once per PV of a tile
+  // of parity t, so each softmax warpgroup waits on consecutive phases of one barrier
+  uint64_t k_empty[kPKSt], v_empty[kPVSt], s_full[2], pv_done[2], mma_final;
   // gathered from both CTAs, waited on by the MMA issuer of the even CTA
   uint64_t q_ready, k_ready[kPKSt], v_ready[kPVSt], s_free[2], p_full;
-  // exchange between the two softmax column halves
-  uint64_t xchg[2];
+  // softmax warpgroups: O's row scale published by the owner of tile i (msync[i & 1]), and
+  // the final exchange of the two partial sums (xchg)
+  uint64_t msync[2], xchg;
   uint32_t tmem_base;
   int abort_flag;
   int lo[2], hi[2], valid[2], q0[2], head[2];
@@ -97,7 +99,8 @@ struct PairCtl {
   int16_t nxt[kBsMaxN / kPBN + 1];         // block-sparse: next needed tile after j
   uint32_t tile_bits[2][kTileWords];
   uint32_t row_bits[2][2][kBsWords];
-  float red_m[2][2][128];  // [tile parity][column half][row]
+  float m_sh[128];         // O's row scale (log2 units)
+  float red_m[2][128];     // [warpgroup][row] final scale and partial sum
   float red_l[2][128];
 };
 
@@ -192,13 +195,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&ctl->s_full[s], 1);
-      mbar_init(&ctl->s_free[s], 16);
-      mbar_init(&ctl->xchg[s], 8);
+      mbar_init(&ctl->s_free[s], 8);   // the 4 warps of the owning warpgroup, both CTAs
+      mbar_init(&ctl->pv_done[s], 1);
+      mbar_init(&ctl->msync[s], 4);
     }
-    mbar_init(&ctl->pv_done, 1);
-    mbar_init(&ctl->mma_final, 1);
-    mbar_init(&ctl->q_ready, 16);
-    mbar_init(&ctl->p_full, 16);
+    mbar_init(&ctl->xchg, 8);
+    mbar_init(&ctl->mma_final, 2);     // one commit per issuer
+    mbar_init(&ctl->q_ready, 16);      // all 8 softmax warps, both CTAs
+    mbar_init(&ctl->p_full, 8);
     fence_mbar_init();
   }
   if (var.mask == 3) {
@@ -277,33 +281,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           tma_load_4d_hint(smem + kOffQ + pn * (kPBM * 128), &p.tmQ, &ctl->q_full, pn * 64,
                            ctl->q0[rank], ctl->head[rank], b, pol_stream);
       }
+      // K and V stages are recycled by different MMAs (S and PV), so neither copy stream
+      // waits for the other: the free-stage barriers are polled and whichever copy can go is
+      // issued, K first (K(i+1) is needed before V(i)). The poll is bounded like every wait.
       int ik = 0, iv = 0;
       int jk = jb, jv = jk;
+      uint64_t t0 = 0;
+      uint32_t idle = 0;
       while (jk < je || jv < je) {
+        bool moved = false;
         if (jk < je) {
           const int s = ik % kPKSt;
-          if (ik >= kPKSt &&
-              !mbar_wait(&ctl->k_empty[s], ((ik / kPKSt) - 1) & 1, status, abort_flag))
-            break;
-          AF_PTRACE(ik, 0);
-          mbar_arrive_expect_tx(&ctl->k_full[s], kKHalf);
-          for (int pn = 0; pn < 2; ++pn)
-            tma_load_4d_hint(smem + kOffK + s * kKHalf + pn * (64 * 128), &p.tmK,
-                             &ctl->k_full[s], pn * 64, jk * kPBN + rank * 64, kvh, b, pol_keep);
-          ++ik;
-          jk = tile_next(T, jk);
+          if (ik < kPKSt || mbar_test(&ctl->k_empty[s], ((ik / kPKSt) - 1) & 1)) {
+            AF_PTRACE(ik, 0);
+            mbar_arrive_expect_tx(&ctl->k_full[s], kKHalf);
+            for (int pn = 0; pn < 2; ++pn)
+              tma_load_4d_hint(smem + kOffK + s * kKHalf + pn * (64 * 128), &p.tmK,
+                               &ctl->k_full[s], pn * 64, jk * kPBN + rank * 64, kvh, b, pol_keep);
+            ++ik;
+            jk = tile_next(T, jk);
+            moved = true;
+          }
         }
-        if (jv < je && (ik >= 2 || jk >= je)) {
+        if (jv < je && iv < ik) {
           const int s = iv % kPVSt;
-          if (iv >= kPVSt &&
-              !mbar_wait(&ctl->v_empty[s], ((iv / kPVSt) - 1) & 1, status, abort_flag))
+          if (iv < kPVSt || mbar_test(&ctl->v_empty[s], ((iv / kPVSt) - 1) & 1)) {
+            AF_PTRACE(iv, 1);
+            mbar_arrive_expect_tx(&ctl->v_full[s], kVHalf);
+            tma_load_4d_hint(smem + kOffV + s * kVHalf, &p.tmV, &ctl->v_full[s], rank * 64,
+                             jv * kPBN, kvh, b, pol_keep);
+            ++iv;
+            jv = tile_next(T, jv);
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+        } else if ((++idle & 255u) == 1u) {
+          const uint64_t now = globaltimer_ns();
+          if (idle == 1u) t0 = now;
+          if (*abort_flag) break;
+          if (now - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
+            atomicExch(status, kDevTimeout);
+            *abort_flag = 1;
             break;
-          AF_PTRACE(iv, 1);
-          mbar_arrive_expect_tx(&ctl->v_full[s], kVHalf);
-          tma_load_4d_hint(smem + kOffV + s * kVHalf, &p.tmV, &ctl->v_full[s], rank * 64,
-                           jv * kPBN, kvh, b, pol_keep);
-          ++iv;
-          jv = tile_next(T, jv);
+          }
         }
       }
       // Drain: no copy may still be landing in shared memory when the CTA exits.
@@ -311,77 +333,80 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         mbar_wait(&ctl->k_full[k % kPKSt], (k / kPKSt) & 1, status, nullptr);
       for (int k = max(0, iv - kPVSt); k < iv; ++k)
         mbar_wait(&ctl->v_full[k % kPVSt], (k / kPVSt) & 1, status, nullptr);
-    } else if (warp == 1 && lane == 0 && rank == 0) {
-      // ======================= pair-MMA issuer =======================
-      constexpr uint32_t idesc_s = idesc_f32acc(256, kPBN, 0, 0, RK != kRopeNone);
-      constexpr uint32_t idesc_o = idesc_bf16_f32(256, kPD, 0, 1);
-      const uint32_t sK = smem_u32(smem + kOffK);
-      const uint32_t sV = smem_u32(smem + kOffV);
+    } else if ((warp == 1 || warp == 2) && lane == 0 && rank == 0) {
+      // ======================= pair-MMA issuers =======================
+      // Warp 1 issues every score MMA S(i) = Q' K(i)^T, warp 2 every O += P(i) V(i). The two
+      // streams are independent (separate accumulators and operands; the softmax orders S
+      // buffers, P and O through the barriers), and a thread's commits track only its own
+      // MMAs. With one issuer, each wait or commit between MMA groups stalls it until its
+      // queued MMAs drain and the tensor pipe idles; two issuers overlap those gaps.
       int n = 0;
       for (int j = jb; j < je; j = tile_next(T, j)) ++n;
-      auto issue_s = [&](int i) -> bool {
-        const int st = i % kPKSt, bf = i & 1;
-        if (!mbar_wait_cluster(&ctl->k_ready[st], (i / kPKSt) & 1, status, abort_flag))
-          return false;
-        AF_PTRACE(i, 4);
-        if (i >= 2 && !mbar_wait_cluster(&ctl->s_free[bf], ((i - 2) >> 1) & 1, status, abort_flag))
-          return false;
-        AF_PTRACE(i, 5);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kPD / 16; ++kk) {
-          const uint64_t bd =
-              smem_desc_sw128(sK + st * kKHalf + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024);
-          mma_ts_pair(tmem + kTmS + bf * 128, tmem + kTmQ + kk * 8, bd, idesc_s, kk > 0);
-        }
-        mma_commit_pair(&ctl->s_full[bf], 3);
-        mma_commit_pair(&ctl->k_empty[st], 3);
-        AF_PTRACE(i, 19);
-        return true;
-      };
-      auto issue_pv = [&](int i) -> bool {
-        const int vs = i % kPVSt;
-        if (!mbar_wait_cluster(&ctl->v_ready[vs], (i / kPVSt) & 1, status, abort_flag))
-          return false;
-        AF_PTRACE(i, 6);
-        if (!mbar_wait_cluster(&ctl->p_full, i & 1, status, abort_flag)) return false;
-        AF_PTRACE(i, 7);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kPBN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(sV + vs * kVHalf + kk * 2048, kVHalf, 1024);
-          mma_ts_pair(tmem + kTmO, tmem + kTmP + kk * 8, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit_pair(&ctl->pv_done, 3);
-        mma_commit_pair(&ctl->v_empty[vs], 3);
-        AF_PTRACE(i, 20);
-        return true;
-      };
       bool ok = mbar_wait_cluster(&ctl->q_ready, 0, status, abort_flag);
-      if (ok && n > 0) ok = issue_s(0);
-      for (int i = 0; ok && i < n; ++i) {
-        if (i + 1 < n) ok = issue_s(i + 1);
-        if (ok) ok = issue_pv(i);
+      if (warp == 1) {
+        constexpr uint32_t idesc_s = idesc_f32acc(256, kPBN, 0, 0, RK != kRopeNone);
+        const uint32_t sK = smem_u32(smem + kOffK);
+        for (int i = 0; ok && i < n; ++i) {
+          const int st = i % kPKSt, bf = i & 1;
+          ok = mbar_wait_cluster(&ctl->k_ready[st], (i / kPKSt) & 1, status, abort_flag);
+          AF_PTRACE(i, 4);
+          if (ok && i >= 2)
+            ok = mbar_wait_cluster(&ctl->s_free[bf], ((i - 2) >> 1) & 1, status, abort_flag);
+          if (!ok) break;
+          AF_PTRACE(i, 5);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kPD / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(
+                sK + st * kKHalf + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024);
+            mma_ts_pair(tmem + kTmS + bf * 128, tmem + kTmQ + kk * 8, bd, idesc_s, kk > 0);
+          }
+          mma_commit_pair(&ctl->s_full[bf], 3);
+          mma_commit_pair(&ctl->k_empty[st], 3);
+          AF_PTRACE(i, 19);
+        }
+      } else {
+        constexpr uint32_t idesc_o = idesc_bf16_f32(256, kPD, 0, 1);
+        const uint32_t sV = smem_u32(smem + kOffV);
+        for (int i = 0; ok && i < n; ++i) {
+          const int vs = i % kPVSt;
+          ok = mbar_wait_cluster(&ctl->v_ready[vs], (i / kPVSt) & 1, status, abort_flag);
+          AF_PTRACE(i, 6);
+          if (ok) ok = mbar_wait_cluster(&ctl->p_full, i & 1, status, abort_flag);
+          if (!ok) break;
+          AF_PTRACE(i, 7);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kPBN / 16; ++kk) {
+            const uint64_t bd = smem_desc_sw128(sV + vs * kVHalf + kk * 2048, kVHalf, 1024);
+            mma_ts_pair(tmem + kTmO, tmem + kTmP + kk * 8, bd, idesc_o, (i > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit_pair(&ctl->pv_done[i & 1], 3);
+          mma_commit_pair(&ctl->v_empty[vs], 3);
+          AF_PTRACE(i, 20);
+        }
       }
-      // All issued MMAs must finish before TMEM is released.
+      // All MMAs of both issuers must finish before TMEM is released.
       mma_commit_pair(&ctl->mma_final, 3);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
-    } else if (warp == 2 && lane == 0 && !ROPE) {
-      // ======================= K relay =======================
-      int i = 0;
-      for (int j = jb; j < je; j = tile_next(T, j), ++i) {
-        const int st = i % kPKSt;
-        if (!mbar_wait(&ctl->k_full[st], (i / kPKSt) & 1, status, abort_flag)) break;
-        arrive_leader(&ctl->k_ready[st], rank);
-      }
     } else if (warp == 3 && lane == 0) {
-      // ======================= V relay =======================
-      int i = 0;
-      for (int j = jb; j < je; j = tile_next(T, j), ++i) {
-        const int st = i % kPVSt;
-        if (!mbar_wait(&ctl->v_full[st], (i / kPVSt) & 1, status, abort_flag)) break;
-        AF_PTRACE(i, 13);
-        arrive_leader(&ctl->v_ready[st], rank);
+      // ======================= K / V relay =======================
+      // Forwards "this CTA's half landed" to the even CTA in the order the MMAs consume the
+      // stages: K(0), then K(i+1) and V(i). With fused RoPE the rotators forward K.
+      int n = 0;
+      for (int j = jb; j < je; j = tile_next(T, j)) ++n;
+      bool good = true;
+      for (int i = 0; good && i <= n; ++i) {
+        if (!ROPE && i < n) {
+          const int st = i % kPKSt;
+          good = mbar_wait(&ctl->k_full[st], (i / kPKSt) & 1, status, abort_flag);
+          if (good) arrive_leader(&ctl->k_ready[st], rank);
+        }
+        if (good && i >= 1) {
+          const int st = (i - 1) % kPVSt;
+          good = mbar_wait(&ctl->v_full[st], ((i - 1) / kPVSt) & 1, status, abort_flag);
+          if (good) arrive_leader(&ctl->v_ready[st], rank);
+        }
       }
     }
   } else if (warp >= 12) {
@@ -393,50 +418,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       const int rt = tid - 384;
       const int c = rt & 7, rg = rt >> 3;
       const int kN = p.N;
-      uint64_t wc2[4], ws2[4], nws2[4];
+      const float2* const cs_tab = p.rope_cs;
+      uint64_t wc2[4], ws2[4];  // (cos, sin) of 16 positions, pairs of dims
       {
         float wc[8], ws[8];
-        load_cs8(p.rope_cs + (size_t)16 * (kPD / 2) + c * 8, wc, ws);
+        load_cs8(cs_tab + (size_t)16 * (kPD / 2) + c * 8, wc, ws);
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
           wc2[w] = f2_pack(wc[2 * w], wc[2 * w + 1]);
           ws2[w] = f2_pack(ws[2 * w], ws[2 * w + 1]);
-          nws2[w] = f2_pack(-ws[2 * w], -ws[2 * w + 1]);
         }
       }
+      // The first row's (cos, sin) of the next tile is read one tile ahead, from a clamped
+      // (always valid) table row so the load never blocks; rows past N are not rotated.
+      float4 pre[4];
+      auto fetch = [&](int jj) {
+        const int pos = min(jj * kPBN + rank * 64 + rg, kN - 1);
+        const float4* src = reinterpret_cast<const float4*>(cs_tab + (size_t)pos * (kPD / 2) + c * 8);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) pre[w] = __ldg(src + w);
+      };
+      fetch(jb);
       int i = 0;
       for (int j = jb; j < je; j = tile_next(T, j), ++i) {
         const int st = i % kPKSt;
         const int n0 = j * kPBN + rank * 64;
-        uint64_t c2[4] = {0, 0, 0, 0}, s2[4] = {0, 0, 0, 0}, ns2[4] = {0, 0, 0, 0};
-        if (n0 + rg < p.N) {
-          float cc[8], ss[8];
-          load_cs8(p.rope_cs + (size_t)(n0 + rg) * (kPD / 2) + c * 8, cc, ss);
+        uint64_t c2[4], s2[4];
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            c2[w] = f2_pack(cc[2 * w], cc[2 * w + 1]);
-            s2[w] = f2_pack(ss[2 * w], ss[2 * w + 1]);
-            ns2[w] = f2_pack(-ss[2 * w], -ss[2 * w + 1]);
-          }
+        for (int w = 0; w < 4; ++w) {
+          c2[w] = f2_pack(pre[w].x, pre[w].z);
+          s2[w] = f2_pack(pre[w].y, pre[w].w);
+        }
+        {
+          const int jn = tile_next(T, j);
+          fetch(jn < je ? jn : j);
         }
         if (!__all_sync(0xffffffffu, mbar_wait(&ctl->k_full[st], (i / kPKSt) & 1, status, abort_flag)))
           break;
         if (rt == 0) AF_PTRACE(i, 2);
         uint8_t* tile = smem + kOffK + st * kKHalf;
+        // all four rows' chunks first, then rotate (rows are independent apart from the angle)
+        uint4 lo[4], hi[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const int row = rg + 16 * k;
-          if (n0 + row < kN) {
-            const uint32_t offl = sw128_offset(row, c);
-            const uint32_t offh = offl + 64 * 128;
-            uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
-            uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
-            rot_chunk_cs2<true>(lo, hi, c2, s2, ns2);
-            *reinterpret_cast<uint4*>(tile + offl) = lo;
-            *reinterpret_cast<uint4*>(tile + offh) = hi;
-          }
-          if (k + 1 < 4) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
+          const uint32_t offl = sw128_offset(rg + 16 * k, c);
+          lo[k] = *reinterpret_cast<const uint4*>(tile + offl);
+          hi[k] = *reinterpret_cast<const uint4*>(tile + offl + 64 * 128);
         }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          uint64_t ns2[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) ns2[w] = s2[w] ^ 0x8000000080000000ull;
+          rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
+          if (k + 1 < 4) {
+            uint64_t nws2[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) nws2[w] = ws2[w] ^ 0x8000000080000000ull;
+            advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
+          }
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          if (n0 + rg + 16 * k < kN) {
+            const uint32_t offl = sw128_offset(rg + 16 * k, c);
+            *reinterpret_cast<uint4*>(tile + offl) = lo[k];
+            *reinterpret_cast<uint4*>(tile + offl + 64 * 128) = hi[k];
+          }
+        }
+        if (rt == 0) AF_PTRACE(i, 9);
         fence_proxy_async_smem();
         __syncwarp();
         if (rt == 0) AF_PTRACE(i, 3);
@@ -478,8 +528,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     const int64_t ab_row = b * var.ab_s[0] + head * var.ab_s[1] + (int64_t)m * var.ab_s[2];
     uint8_t* const visits = var.visits;
     const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
-    const uint32_t tO = tmem + lane_off + kTmO + 64 * h;
-    const uint32_t tP = tmem + lane_off + kTmP + 32 * h;
     bool ok = true;
 
     // ---- Q' = R_m Q (fp16 with fused RoPE) into TMEM: this thread writes chunk pairs
@@ -511,184 +559,192 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
     }
 
-    float m_run = kNegInf, l_run = 0.f;
-    int n_done = 0;
+    // Online softmax over alternate tiles: warpgroup h takes tiles i = h, h+2, ... with full
+    // 128-column rows, so one warpgroup's exponentials overlap the other's loads, maxima and
+    // stores. Both feed the single O accumulator, whose row scale m_sh[r] (log2 units) only
+    // grows, and lazily (by more than 8). A tile's P is computed against this warpgroup's last
+    // scale and reconciled with O's scale once the previous tile's PV has completed; the P
+    // buffer and O belong to one tile at a time.
+    float m_h = kNegInf, l_h = 0.f;  // this warpgroup's partial row sum and its scale
     const float scale_log2 = p.scale_log2;
     const float alibi = (BIAS == 1 && valid) ? var.slopes[head] * kLog2e : 0.f;
     const int blk_row = bs64 ? (r >> 6) : 0;
-    for (int j = jb; ok && j < je; j = tile_next(T, j)) {
-      const int i = n_done;
-      const int bf = i & 1;
+    const uint32_t tP = tmem + lane_off + kTmP;
+    const uint32_t tOall = tmem + lane_off + kTmO;
+    int i = 0;
+    for (int j = jb; ok && j < je; j = tile_next(T, j), ++i) {
+      if ((i & 1) != h) continue;
       const bool act = j >= lo_s && j < hi_s && (!bs || pbit(ctl->tile_bits[s], j));
-      const bool hole = bs64 && !pbit(ctl->row_bits[s][blk_row], 2 * j + h);
+      bool h0 = true, h1 = true;  // block-sparse 64-blocks of this tile present for the row
+      if (bs64) {
+        h0 = pbit(ctl->row_bits[s][blk_row], 2 * j);
+        h1 = pbit(ctl->row_bits[s][blk_row], 2 * j + 1);
+      }
       // Every wait result is voted across the warp so TMEM collectives never diverge.
-      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->s_full[bf], (i >> 1) & 1, status, abort_flag))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->s_full[h], (i >> 1) & 1, status, abort_flag))) {
         ok = false;
         break;
       }
       if (lane == 0 && wq == 0) AF_PTRACE(i, h ? 14 : 8);
       tc_fence_after();
-      uint32_t xr[64];
-      tmem_ld32<0>(tmem + lane_off + kTmS + bf * 128 + 64 * h, xr);
-      tmem_ld32<32>(tmem + lane_off + kTmS + bf * 128 + 64 * h + 32, xr);
+      uint32_t xr[128];
+      tmem_ld32<0>(tmem + lane_off + kTmS + h * 128, xr);
+      tmem_ld32<32>(tmem + lane_off + kTmS + h * 128 + 32, xr);
+      tmem_ld32<64>(tmem + lane_off + kTmS + h * 128 + 64, xr);
+      tmem_ld32<96>(tmem + lane_off + kTmS + h * 128 + 96, xr);
       tmem_wait_ld();
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 16);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) arrive_leader(&ctl->s_free[bf], rank);
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 17);
-      float x[64];
+      if (lane == 0) arrive_leader(&ctl->s_free[h], rank);
+      float x[128];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(xr[c]);
-      if (lane == 0 && wq == 0 && h == 0 && __float_as_uint(x[0]) != 0x7fc00001u &&
-          __float_as_uint(x[63]) != 0x7fc00001u)
-        AF_PTRACE(i, 22);
-      const int kh = j * kPBN + 64 * h;  // first key of this half
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
+      const int k0 = j * kPBN;
       // ---- score combinators (log2 domain) ----
       float mul = scale_log2;
       if constexpr (BIAS != 0) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] *= scale_log2;
+        for (int c = 0; c < 128; ++c) x[c] *= scale_log2;
         mul = 1.f;
         if constexpr (BIAS == 1) {
-          const float base = alibi * static_cast<float>(kh - m);
+          const float base = alibi * static_cast<float>(k0 - m);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) x[c] = __fmaf_rn(alibi, static_cast<float>(c), x[c] + base);
+          for (int c = 0; c < 128; ++c) x[c] = __fmaf_rn(alibi, static_cast<float>(c), x[c] + base);
         } else if (act) {
           if (vab16) {
             const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(add_bias) + ab_row;
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (kh + c < N && m < N) x[c] += __bfloat162float(ab[(int64_t)(kh + c) * ab_s3]) * kLog2e;
+            for (int c = 0; c < 128; ++c)
+              if (k0 + c < N && m < N) x[c] += __bfloat162float(ab[(int64_t)(k0 + c) * ab_s3]) * kLog2e;
           } else {
             const float* ab = static_cast<const float*>(add_bias) + ab_row;
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (kh + c < N && m < N) x[c] += ab[(int64_t)(kh + c) * ab_s3] * kLog2e;
+            for (int c = 0; c < 128; ++c)
+              if (k0 + c < N && m < N) x[c] += ab[(int64_t)(k0 + c) * ab_s3] * kLog2e;
           }
         }
       }
-      if (__builtin_expect(!act || hole || j < jm_lo || j >= jm_hi, 0)) {
+      if (__builtin_expect(!act || !h0 || !h1 || j < jm_lo || j >= jm_hi, 0)) {
         // per-element mask (cold: sequence end, causal diagonal, window edges, holes)
-        int c_lo = 0, c_hi = (act && !hole) ? min(63, N - 1 - kh) : -1;
-        if (var.causal) c_hi = min(c_hi, m - kh);
+        int c_lo = 0, c_hi = act ? min(kPBN - 1, N - 1 - k0) : -1;
+        if (var.causal) c_hi = min(c_hi, m - k0);
         if (var.mask == 2) {
-          c_lo = max(c_lo, m - var.window + 1 - kh);
-          if (!var.causal) c_hi = min(c_hi, m + var.window - 1 - kh);
+          c_lo = max(c_lo, m - var.window + 1 - k0);
+          if (!var.causal) c_hi = min(c_hi, m + var.window - 1 - k0);
         }
 #pragma unroll
-        for (int c = 0; c < 64; ++c) x[c] = (c >= c_lo && c <= c_hi) ? x[c] : kNegInf;
+        for (int c = 0; c < 128; ++c)
+          x[c] = (c >= c_lo && c <= c_hi && (c < 64 ? h0 : h1)) ? x[c] : kNegInf;
       }
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 18);
-      // row max of this half: 8 independent chains, then a small tree
+      // row max: 8 independent chains, then a small tree
       float mp[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mp[k] = fmaxf(x[2 * k], x[2 * k + 1]);
 #pragma unroll
-      for (int i2 = 1; i2 < 4; ++i2)
+      for (int i2 = 1; i2 < 8; ++i2)
 #pragma unroll
         for (int k = 0; k < 8; ++k) mp[k] = max3f(mp[k], x[16 * i2 + 2 * k], x[16 * i2 + 2 * k + 1]);
-      const float mx_h =
-          max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7]));
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 21);
-      // ---- exchange with the other column half of the same row ----
-      ctl->red_m[bf][h][r] = mx_h;
-      __syncwarp();
-      if (lane == 0) AF_PTRACE(i, 24 + (warp - 4));
-      if (lane == 0) mbar_arrive(&ctl->xchg[bf]);
-      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->xchg[bf], (i >> 1) & 1, status, abort_flag))) {
-        ok = false;
-        break;
-      }
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 9);
-      const float mx = fmaxf(mx_h, ctl->red_m[bf][h ^ 1][r]) * mul;
-      // ---- online softmax with lazy rescaling (exact after the final division); both halves
-      // take identical decisions from identical inputs ----
-      const float m_new = fmaxf(m_run, mx);
-      float m_use = m_run;
-      bool rescale = false;
-      if (n_done == 0) {
-        m_use = m_new;
-      } else if (m_new > m_run + 8.0f) {
-        m_use = m_new;
-        rescale = true;
-      }
-      const float nb = (m_use == kNegInf) ? 0.f : -m_use;
+      const float mx =
+          max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]), fmaxf(mp[6], mp[7])) * mul;
+      // exponentials against this warpgroup's scale unless the tile exceeds it by more than 8
+      const float m_base = (mx > m_h + 8.0f) ? mx : m_h;
+      const float nb = (m_base == kNegInf) ? 0.f : -m_base;
       const uint64_t mul2v = f2_pack(mul, mul), nb2 = f2_pack(nb, nb);
       uint64_t acc2[4] = {0, 0, 0, 0};
-      uint32_t pk[32];
+      uint32_t pk[64];
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 64; ++c) {
         const uint64_t a = fma2(f2_pack(x[2 * c], x[2 * c + 1]), mul2v, nb2);
         const float p0 = ex2_approx(f2_lo(a)), p1 = ex2_approx(f2_hi(a));
         acc2[c & 3] = add2(acc2[c & 3], f2_pack(p0, p1));
         pk[c] = pack_bf16x2(p0, p1);
       }
       const uint64_t acc = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
-      const float sum = f2_lo(acc) + f2_hi(acc);
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 10);
-      // P and O may be touched only after the previous PV has finished with them.
-      if (n_done > 0) {
+      float sum = f2_lo(acc) + f2_hi(acc);
+      if (lane == 0 && wq == 0) AF_PTRACE(i, 10 + h);
+      // ---- P buffer and O become this tile's once PV(i-1) has completed ----
+      float m_cur = kNegInf;  // O's row scale
+      if (i > 0) {
         if (!__all_sync(0xffffffffu,
-                        mbar_wait(&ctl->pv_done, (n_done - 1) & 1, status, abort_flag))) {
+                        mbar_wait(&ctl->pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, status, abort_flag) &&
+                            mbar_wait(&ctl->msync[(i - 1) & 1], ((i - 1) >> 1) & 1, status, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
+        m_cur = ctl->m_sh[r];
       }
-      if (lane == 0 && wq == 0 && h == 0) AF_PTRACE(i, 11);
-      // tcgen05.ld/st are warp-collective: rescale the whole warp's rows when any row needs
-      // it (alpha = 1 for rows that do not).
-      if (__builtin_expect(__any_sync(0xffffffffu, rescale), 0)) {
-        const float alpha = rescale ? ex2_approx(m_run - m_use) : 1.f;
-        l_run *= alpha;
+      const float m_fin = fmaxf(m_cur, m_base);
+      if (__builtin_expect(m_base < m_fin, 0)) {
+        // O is at a larger scale than this tile's exponentials: bring P down to it (rare)
+        const float beta = ex2_approx(m_base - m_fin);
 #pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
+        for (int c = 0; c < 64; ++c)
+          pk[c] = pack_bf16x2(bf16lo_to_f32(pk[c]) * beta, bf16hi_to_f32(pk[c]) * beta);
+        sum *= beta;
+      }
+      // tcgen05.ld/st are warp-collective: rescale O for the whole warp when any row's scale
+      // grows (alpha = 1 for rows that do not)
+      const bool grow = i > 0 && m_cur < m_fin;
+      if (__builtin_expect(__any_sync(0xffffffffu, grow), 0)) {
+        const float alpha = grow ? ex2_approx(m_cur - m_fin) : 1.f;
+#pragma unroll 1
+        for (int ch = 0; ch < 4; ++ch) {
           uint32_t o[32];
-          tmem_ld32(tO + ch * 32, o);
+          tmem_ld32(tOall + ch * 32, o);
           tmem_wait_ld();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(tO + ch * 32, o);
+          tmem_st32(tOall + ch * 32, o);
         }
       }
-      tmem_st32(tP, pk);
+      l_h = ((m_h == m_fin || m_h == kNegInf) ? l_h : l_h * ex2_approx(m_h - m_fin)) + sum;
+      m_h = m_fin;
+      ctl->m_sh[r] = m_fin;
+      tmem_st32<0>(tP, pk);
+      tmem_st32<32>(tP + 32, pk);
       tmem_wait_st();
-      l_run += sum;
-      m_run = m_use;
       tc_fence_before();
       __syncwarp();
       if (lane == 0 && wq == 0) AF_PTRACE(i, h ? 15 : 12);
-      if (lane == 0) arrive_leader(&ctl->p_full, rank);
-      if (act && visits && h == 0 && r == 0) {
+      if (lane == 0) {
+        arrive_leader(&ctl->p_full, rank);
+        mbar_arrive(&ctl->msync[i & 1]);
+      }
+      if (act && visits && r == 0) {
         const int TQ = (N + kPBM - 1) / kPBM;
         visits[((static_cast<int64_t>(b) * p.Hq + head) * TQ + q0 / kPBM) * TK + j] = 1;
       }
-      ++n_done;
     }
-    // ---- epilogue: O = acc / l, LSE = ln(sum) ----
-    if (ok && n_done > 0) {
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&ctl->pv_done, (n_done - 1) & 1, status, abort_flag));
+    const int n = i;  // kv tiles of the pair
+    // ---- epilogue: wait for the last PV, combine the two partial sums, O / l, LSE ----
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[(n - 1) & 1], ((n - 1) >> 1) & 1,
+                                             status, abort_flag));
       tc_fence_after();
     }
-    float l_tot = l_run;
+    float m_fin = m_h, l_tot = l_h;
     if (ok) {
-      const int bf = n_done & 1;
-      ctl->red_l[h][r] = l_run;
+      ctl->red_m[h][r] = m_h;
+      ctl->red_l[h][r] = l_h;
       __syncwarp();
-      if (lane == 0) mbar_arrive(&ctl->xchg[bf]);
-      ok = __all_sync(0xffffffffu,
-                      mbar_wait(&ctl->xchg[bf], (n_done >> 1) & 1, status, abort_flag));
-      if (ok) l_tot = l_run + ctl->red_l[h ^ 1][r];
+      if (lane == 0) mbar_arrive(&ctl->xchg);
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->xchg, 0, status, abort_flag));
+      if (ok) {
+        const float m_o = ctl->red_m[h ^ 1][r], l_o = ctl->red_l[h ^ 1][r];
+        m_fin = fmaxf(m_h, m_o);
+        l_tot = (m_h == kNegInf ? 0.f : l_h * ex2_approx(m_h - m_fin)) +
+                (m_o == kNegInf ? 0.f : l_o * ex2_approx(m_o - m_fin));
+      }
     }
     if (valid) {
       const float inv = (l_tot > 0.f) ? 1.f / l_tot : 0.f;
+      const uint32_t tO = tOall + 64 * h;
       __nv_bfloat16* orow = p.out + b * p.o_sb + head * p.o_sh + (int64_t)m * p.o_sn + 64 * h;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint32_t o[32];
-        if (ok && n_done > 0) {
+        if (ok && n > 0) {
           tmem_ld32(tO + ch * 32, o);
           tmem_wait_ld();
         } else {
@@ -710,7 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       }
       if (h == 0 && p.lse && m < N)
         p.lse[(static_cast<int64_t>(b) * p.Hq + head) * N + m] =
-            (l_tot > 0.f) ? (m_run + log2f(l_tot)) * kLn2 : kNegInf;
+            (l_tot > 0.f) ? (m_fin + log2f(l_tot)) * kLn2 : kNegInf;
     }
   }
 
