@@ -75,9 +75,14 @@ constexpr uint32_t kOffV = kOffK + kPKSt * kKHalf;
 constexpr uint32_t kOffCtl = kOffV + kPVSt * kVHalf;
 constexpr uint32_t kTmS = 0, kTmO = 256, kTmQ = 384, kTmP = 448;
 
-constexpr uint32_t kRegsLow = 48;     // warpgroup 0: TMA, MMA, relays
-constexpr uint32_t kRegsRot = 96;     // warpgroup 3: K rotation
-constexpr uint32_t kRegsSm = 184;     // warpgroups 1, 2: softmax
+#ifndef ATTNFUSE_REGS_LOW
+#define ATTNFUSE_REGS_LOW 40
+#define ATTNFUSE_REGS_ROT 104
+#define ATTNFUSE_REGS_SM 184
+#endif
+constexpr uint32_t kRegsLow = ATTNFUSE_REGS_LOW;  // warpgroup 0: TMA, MMA, relays
+constexpr uint32_t kRegsRot = ATTNFUSE_REGS_ROT;  // warpgroup 3: K rotation
+constexpr uint32_t kRegsSm = ATTNFUSE_REGS_SM;    // warpgroups 1, 2: softmax
 static_assert(kRegsLow + kRegsRot + 2 * kRegsSm <= 4 * (65536 / kPThreads),
               "register split exceeds the registers the CTA is launched with");
 
@@ -457,33 +462,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           break;
         if (rt == 0) AF_PTRACE(i, 2);
         uint8_t* tile = smem + kOffK + st * kKHalf;
-        // all four rows' chunks first, then rotate (rows are independent apart from the angle)
-        uint4 lo[4], hi[4];
+        // two rows at a time: both rows' chunks first, then rotate and store them
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t offl = sw128_offset(rg + 16 * k, c);
-          lo[k] = *reinterpret_cast<const uint4*>(tile + offl);
-          hi[k] = *reinterpret_cast<const uint4*>(tile + offl + 64 * 128);
-        }
+        for (int k2 = 0; k2 < 4; k2 += 2) {
+          uint4 lo[2], hi[2];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          uint64_t ns2[4];
-#pragma unroll
-          for (int w = 0; w < 4; ++w) ns2[w] = s2[w] ^ 0x8000000080000000ull;
-          rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
-          if (k + 1 < 4) {
-            uint64_t nws2[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) nws2[w] = ws2[w] ^ 0x8000000080000000ull;
-            advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
+          for (int k = 0; k < 2; ++k) {
+            const uint32_t offl = sw128_offset(rg + 16 * (k2 + k), c);
+            lo[k] = *reinterpret_cast<const uint4*>(tile + offl);
+            hi[k] = *reinterpret_cast<const uint4*>(tile + offl + 64 * 128);
           }
-        }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          if (n0 + rg + 16 * k < kN) {
-            const uint32_t offl = sw128_offset(rg + 16 * k, c);
-            *reinterpret_cast<uint4*>(tile + offl) = lo[k];
-            *reinterpret_cast<uint4*>(tile + offl + 64 * 128) = hi[k];
+          for (int k = 0; k < 2; ++k) {
+            uint64_t ns2[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) ns2[w] = s2[w] ^ 0x8000000080000000ull;
+            rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
+            if (k2 + k + 1 < 4) {
+              uint64_t nws2[4];
+#pragma unroll
+              for (int w = 0; w < 4; ++w) nws2[w] = ws2[w] ^ 0x8000000080000000ull;
+              advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
+            }
+          }
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            if (n0 + rg + 16 * (k2 + k) < kN) {
+              const uint32_t offl = sw128_offset(rg + 16 * (k2 + k), c);
+              *reinterpret_cast<uint4*>(tile + offl) = lo[k];
+              *reinterpret_cast<uint4*>(tile + offl + 64 * 128) = hi[k];
+            }
           }
         }
         if (rt == 0) AF_PTRACE(i, 9);
