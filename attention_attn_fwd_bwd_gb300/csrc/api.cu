@@ -259,7 +259,7 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
   float2* cs = static_cast<float2*>(workspace);
   cudaError_t e = launch_rope_table(cs, rope_table_rows(N), d / 2, make_freqs(d, rope_theta), stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
-  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, false, stream);
+  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, 0, stream);
   if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
   return ok();
 }
@@ -315,8 +315,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
     void* qr = base;
     void* kr = base + align_up((size_t)B * Hq * N * d * 2, 256);
-    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, false, stream);
-    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, true, stream);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, 0, stream);
+    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
     qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
@@ -377,6 +377,10 @@ attnfuse_status attnfuse_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d
   size_t n = 0;
   if (rope_mode != ATTNFUSE_ROPE_NONE) n += rope_table_bytes(N, d);
   n += align_up((size_t)B * Hq * N * 4, 256);  // D = rowsum(dO * O)
+  if (rope_mode == ATTNFUSE_ROPE_PREROTATE) {     // Q' and K' (bf16, contiguous)
+    n += align_up((size_t)B * Hq * N * d * 2, 256);
+    n += align_up((size_t)B * Hkv * N * d * 2, 256);
+  }
   *bytes = n;
   return ok();
 }
@@ -438,8 +442,25 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
     ws += rope_table_bytes(N, d);
   }
   p.Dvec = reinterpret_cast<float*>(ws);
-  if ((rc = encode_bhnd(&p.tmQ, q, q_strides, B, Hq, N, d, "q"))) return rc;
-  if ((rc = encode_bhnd(&p.tmK, k, k_strides, B, Hkv, N, d, "k"))) return rc;
+  ws += align_up((size_t)B * Hq * N * 4, 256);
+  const void* qa = q;
+  const void* ka = k;
+  const int64_t* qs = q_strides;
+  const int64_t* ks = k_strides;
+  int64_t qs_c[4], ks_c[4];
+  if (rope_mode == ATTNFUSE_ROPE_PREROTATE) {
+    // Q' and K' once, in the backward kernels' in-tile recurrence (bit-identical to FUSED)
+    void* qr = ws;
+    void* kr = ws + align_up((size_t)B * Hq * N * d * 2, 256);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, p.rope_cs, false, 128, stream);
+    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, p.rope_cs, false, 128, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
+    qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
+    ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
+    qa = qr; ka = kr; qs = qs_c; ks = ks_c;
+  }
+  if ((rc = encode_bhnd(&p.tmQ, qa, qs, B, Hq, N, d, "q"))) return rc;
+  if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k"))) return rc;
   if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v"))) return rc;
   if ((rc = encode_bhnd(&p.tmDO, dout, do_strides, B, Hq, N, d, "dout"))) return rc;
   p.o = static_cast<const __nv_bfloat16*>(out);
@@ -459,7 +480,9 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st;
-  cudaError_t e = launch_bwd(p, rope_mode != ATTNFUSE_ROPE_NONE, stream);
+  const int rk = rope_mode == ATTNFUSE_ROPE_FUSED ? kRopeFused
+                 : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
+  cudaError_t e = launch_bwd(p, rk, stream);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   return ok();
 }

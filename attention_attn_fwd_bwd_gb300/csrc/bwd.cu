@@ -7,12 +7,13 @@
 //                    Epilogue: dK = scale R_n^T dK', dV (GQA sums stay inside the CTA).
 //   dq_kernel        one CTA per (query tile, head, batch): Q' and dO stay in shared memory;
 //                    for every visible key tile: S = Q' K'^T, dP = dO V^T, dS = P (dP - D),
-//                    dQ' += dS K'. Epilogue: dQ = scale R_m^T dQ'.
+//                    dQ' += dS K' (dS double-buffered in TMEM, so the next tile's S and dP
+//                    overlap this tile's element-wise step). Epilogue: dQ = scale R_m^T dQ'.
 // Rotations use the (cos, sin) table; the rotated operands are rounded to bf16 (the other
 // operands of these contractions are bf16). Every wait is bounded (see ptx.cuh).
 //
-// Warp roles (12 warps): 0 TMA, 1 MMA, 4-7 element-wise (one thread per TMEM lane/row),
-// 8-11 rotate Q/K tiles in shared memory.
+// dkdv_kernel warp roles (12 warps): 0 TMA, 1 MMA, 4-7 element-wise (one thread per TMEM
+// lane/row), 8-11 rotate Q/K tiles in shared memory. dq_kernel: see there.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -30,28 +31,38 @@ constexpr int kBwdThreads = 384;
 constexpr int kT = 128;  // tile edge (keys and queries)
 
 // Rotate a [128 x D] bf16 tile (128B-swizzled panels) in place: row r at position pos0 + r.
-// Executed by 128 threads (t = 0..127); rows at or beyond N are left untouched.
+// Executed by 128 threads (t = 0..127): thread t owns chunk pair c = t % CP of rows
+// t / CP + RG k, so it reads the (cos, sin) table once (its first row) and advances the angle
+// by RG positions per row (angle addition), instead of one dependent table read per row.
+// Rows at or beyond N are left untouched.
 template <int D>
 __device__ __forceinline__ void rotate_tile_bf16(uint8_t* tile, int pos0, int N,
                                                  const float2* __restrict__ cs, int t) {
-  constexpr int CP = D / 16;
-  for (int it = t; it < kT * CP; it += 128) {
-    const int row = it / CP, c = it % CP;
-    const int pos = pos0 + row;
-    if (pos >= N) continue;
-    uint32_t offl, offh;
-    if (D == 128) {
-      offl = sw128_offset(row, c);
-      offh = offl + kT * 128;
-    } else {
-      offl = sw128_offset(row, c);
-      offh = sw128_offset(row, c + 4);
+  constexpr int CP = D / 16, RG = 128 / CP, ROWS = kT / RG;
+  const int c = t % CP, rg = t / CP;
+  float cc[8], ss[8], wc[8], ws[8];
+  load_cs8(cs + (size_t)RG * (D / 2) + c * 8, wc, ws);
+  const int p0 = min(pos0 + rg, N - 1);
+  load_cs8(cs + (size_t)p0 * (D / 2) + c * 8, cc, ss);
+#pragma unroll
+  for (int k = 0; k < ROWS; ++k) {
+    const int row = rg + RG * k;
+    if (pos0 + row < N) {
+      uint32_t offl, offh;
+      if (D == 128) {
+        offl = sw128_offset(row, c);
+        offh = offl + kT * 128;
+      } else {
+        offl = sw128_offset(row, c);
+        offh = sw128_offset(row, c + 4);
+      }
+      uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
+      uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
+      rot_chunk_cs<false>(lo, hi, cc, ss);
+      *reinterpret_cast<uint4*>(tile + offl) = lo;
+      *reinterpret_cast<uint4*>(tile + offh) = hi;
     }
-    uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
-    uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
-    rot_chunk<false>(lo, hi, cs + (size_t)pos * (D / 2) + c * 8);
-    *reinterpret_cast<uint4*>(tile + offl) = lo;
-    *reinterpret_cast<uint4*>(tile + offh) = hi;
+    if (k + 1 < ROWS) advance_cs8(cc, ss, wc, ws);
   }
 }
 
@@ -131,10 +142,15 @@ struct DqCfg {
 struct DqCtl {
   uint64_t q_full, do_full, q_ready;
   uint64_t k_full[2], v_full[2], k_ready[2], kv_free[2];
-  uint64_t s_full, p_full, mma_done, mma_final;
+  uint64_t s_full, s_free, p_full, dq_done[2], mma_final;
   uint32_t tmem_base;
   int abort_flag;
 };
+
+constexpr int kDqThreads = 512;
+constexpr uint32_t kDqRegsLow = 56, kDqRegsRot = 88, kDqRegsEw = 184;
+static_assert(kDqRegsLow + kDqRegsRot + 2 * kDqRegsEw <= 4 * (65536 / kDqThreads),
+              "register split exceeds the registers the CTA is launched with");
 
 __host__ __device__ constexpr size_t kv_smem_bytes(int D) {
   return 1024 + (2 + 2 * 2) * (size_t)(kT * D * 2) + 2 * 1024 + sizeof(KvCtl);
@@ -181,8 +197,10 @@ __global__ void bwd_pre_kernel(const __grid_constant__ BwdParams p) {
 // ---------------------------------------------------------------------------------------------
 // dK, dV
 // ---------------------------------------------------------------------------------------------
-template <int D, bool ROPE>
+template <int D, int RK>
 __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
+  constexpr bool ROPE = (RK == kRopeFused);      // rotate Q / K tiles on chip
+  constexpr bool ROPE_OUT = (RK != kRopeNone);   // rotate dK back
   using C = KvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -409,8 +427,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
 #pragma unroll
       for (int c = 0; c < D; ++c) g[c] = 0.f;
     if (n < p.N)
-      store_grad_row<D, ROPE>(g, p.scale, n, p.rope_cs,
-                              p.dk + b * p.dk_s[0] + kvh * p.dk_s[1] + (int64_t)n * p.dk_s[2]);
+      store_grad_row<D, ROPE_OUT>(g, p.scale, n, p.rope_cs,
+                                  p.dk + b * p.dk_s[0] + kvh * p.dk_s[1] + (int64_t)n * p.dk_s[2]);
   }
   tc_fence_before();
   __syncthreads();
@@ -421,15 +439,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
 // ---------------------------------------------------------------------------------------------
 // dQ
 // ---------------------------------------------------------------------------------------------
-template <int D, bool ROPE>
-__global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+// 16 warps: 0 TMA, 1 MMA, 4-11 element-wise (warps 4-7 key columns 0-63 of each tile, 8-11
+// columns 64-127; one query row per thread), 12-15 rotate Q once and each K tile.
+// TMEM: dQ' [0, D), S [128, 256), dP [256, 384), dS (bf16) double-buffered at [384, 448) and
+// [448, 512). dS does not overwrite S, so S(j+1) and dP(j+1) are computed while the
+// element-wise warps still work on tile j.
+template <int D, int RK>
+__global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant__ BwdParams p) {
+  constexpr bool ROPE = (RK == kRopeFused);      // rotate Q / K tiles on chip
+  constexpr bool ROPE_OUT = (RK != kRopeNone);   // rotate dQ back
   using C = DqCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   DqCtl* ctl = reinterpret_cast<DqCtl*>(smem + C::OFF_CTL);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int TQ = (p.N + kT - 1) / kT;
+  const int N = p.N;
+  const int TQ = (N + kT - 1) / kT;
   const int per_i = p.B * p.Hq;
   const int i = TQ - 1 - static_cast<int>(blockIdx.x) / per_i;  // longest first
   const int rem = static_cast<int>(blockIdx.x) % per_i;
@@ -448,10 +474,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
       mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->k_ready[s], 128);
       mbar_init(&ctl->kv_free[s], 1);
+      mbar_init(&ctl->dq_done[s], 1);
     }
     mbar_init(&ctl->s_full, 1);
-    mbar_init(&ctl->p_full, 128);
-    mbar_init(&ctl->mma_done, 1);
+    mbar_init(&ctl->s_free, 8);   // one arrival per element-wise warp
+    mbar_init(&ctl->p_full, 8);
     mbar_init(&ctl->mma_final, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -461,11 +488,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  // TMEM: dQ' [0, D), S [128, 256), dP [256, 384)
-  const uint32_t T_DQ = 0, T_S = 128, T_DP = 256;
+  constexpr uint32_t T_DQ = 0, T_S = 128, T_DP = 256, T_DS = 384;
 
-  if (warp == 0) {
-    if (lane == 0) {
+  if (warp < 4) {
+    setmaxnreg_dec<kDqRegsLow>();
+    if (warp == 0 && lane == 0) {
       tma_prefetch_desc(&p.tmQ);
       tma_prefetch_desc(&p.tmK);
       tma_prefetch_desc(&p.tmV);
@@ -495,21 +522,34 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
         mbar_wait(&ctl->k_full[k & 1], (k >> 1) & 1, status, nullptr);
         mbar_wait(&ctl->v_full[k & 1], (k >> 1) & 1, status, nullptr);
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kT, 0, 0);  // S, dP: both K-major
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);   // dQ': B = K' MN-major
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
+      auto issue_dq = [&](int jq) -> bool {  // dQ' += dS(jq) K'(jq)
+        if (!mbar_wait(&ctl->p_full, jq & 1, status, abort_flag)) return false;
+        tc_fence_after();
+        const int s = jq & 1;
+#pragma unroll
+        for (int kk = 0; kk < kT / 16; ++kk)
+          mma_ts(tmem + T_DQ, tmem + T_DS + s * 64 + kk * 8,
+                 smem_desc_sw128(sK + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
+                 (jq > 0 || kk > 0) ? 1u : 0u);
+        mma_commit(&ctl->dq_done[s]);
+        mma_commit(&ctl->kv_free[s]);
+        return true;
+      };
       bool ok = mbar_wait(&ctl->q_ready, 0, status, abort_flag) &&
                 mbar_wait(&ctl->do_full, 0, status, abort_flag);
       for (int jt = 0; ok && jt < nk; ++jt) {
         const int s = jt & 1;
         const uint32_t ph = (jt >> 1) & 1;
-        if (!mbar_wait(&ctl->k_ready[s], ph, status, abort_flag)) break;
-        if (!mbar_wait(&ctl->v_full[s], ph, status, abort_flag)) break;
-        if (jt > 0 && !mbar_wait(&ctl->mma_done, (jt - 1) & 1, status, abort_flag)) break;
+        ok = mbar_wait(&ctl->k_ready[s], ph, status, abort_flag) &&
+             mbar_wait(&ctl->v_full[s], ph, status, abort_flag);
+        // S and dP of tile jt overwrite those of tile jt-1 once the element-wise warps hold them
+        if (ok && jt > 0) ok = mbar_wait(&ctl->s_free, (jt - 1) & 1, status, abort_flag);
+        if (!ok) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -524,23 +564,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
                  smem_desc_sw128(sV + s * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
         }
         mma_commit(&ctl->s_full);
-        if (!mbar_wait(&ctl->p_full, jt & 1, status, abort_flag)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(tmem + T_DQ, tmem + T_S + kk * 8,
-                 smem_desc_sw128(sK + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
-                 (jt > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->mma_done);
-        mma_commit(&ctl->kv_free[s]);
+        if (jt > 0) ok = issue_dq(jt - 1);
       }
+      if (ok && nk > 0) issue_dq(nk - 1);
       mma_commit(&ctl->mma_final);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
     }
-  } else if (warp >= 8) {
-    const int t = tid - 256;
+  } else if (warp >= 12) {
+    setmaxnreg_dec<kDqRegsRot>();
+    const int t = tid - 384;
     if (mbar_wait(&ctl->q_full, 0, status, abort_flag) && ROPE) {
-      rotate_tile_bf16<D>(smem + C::OFF_Q, i * kT, p.N, p.rope_cs, t);
+      rotate_tile_bf16<D>(smem + C::OFF_Q, i * kT, N, p.rope_cs, t);
       fence_proxy_async_smem();
     }
     mbar_arrive(&ctl->q_ready);
@@ -548,21 +582,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
       const int s = jt & 1;
       if (!mbar_wait(&ctl->k_full[s], (jt >> 1) & 1, status, abort_flag)) break;
       if (ROPE) {
-        rotate_tile_bf16<D>(smem + C::OFF_K + s * C::TILE, jt * kT, p.N, p.rope_cs, t);
+        rotate_tile_bf16<D>(smem + C::OFF_K + s * C::TILE, jt * kT, N, p.rope_cs, t);
         fence_proxy_async_smem();
       }
       mbar_arrive(&ctl->k_ready[s]);
     }
-  } else if (warp >= 4) {
-    // ---- element-wise: thread = query row m ----
-    const int r = (warp - 4) * 32 + lane;
+  } else {
+    // ---- element-wise: thread = query row m, key columns 64 hh .. 64 hh + 63 ----
+    setmaxnreg_inc<kDqRegsEw>();
+    const int hh = (warp - 4) >> 2;
+    const int wq = warp & 3;
+    const int r = wq * 32 + lane;
     const int m = i * kT + r;
-    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+    const bool causal = p.causal != 0;
     float l2 = __int_as_float(0x7f800000), dd = 0.f;
-    if (m < p.N) {
-      const float l = p.lse[((int64_t)b * p.Hq + h) * p.N + m];
+    if (m < N) {
+      const float l = p.lse[((int64_t)b * p.Hq + h) * N + m];
       l2 = (l == kNegInf) ? __int_as_float(0x7f800000) : l * kLog2e;
-      dd = p.Dvec[((int64_t)b * p.Hq + h) * p.N + m];
+      dd = p.Dvec[((int64_t)b * p.Hq + h) * N + m];
     }
     bool ok = true;
     const float c2 = p.scale_log2;
@@ -572,45 +610,65 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
         break;
       }
       tc_fence_after();
-      const int k0 = jt * kT;
-      const bool edge = (p.causal && jt == i) || (k0 + kT > p.N);
+      uint32_t sr[64], dr[64];
+      tmem_ld32<0>(tmem + lane_off + T_S + 64 * hh, sr);
+      tmem_ld32<32>(tmem + lane_off + T_S + 64 * hh + 32, sr);
+      tmem_ld32<0>(tmem + lane_off + T_DP + 64 * hh, dr);
+      tmem_ld32<32>(tmem + lane_off + T_DP + 64 * hh + 32, dr);
+      tmem_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->s_free);
+      const int k0 = jt * kT + 64 * hh;  // first key of this half
+      float pr[64];
+      const uint64_t c22 = f2_pack(c2, c2), nl2 = f2_pack(-l2, -l2);
 #pragma unroll
-      for (int ch = 0; ch < kT / 32; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + T_S + ch * 32, sr);
-        tmem_ld32(tmem + lane_off + T_DP + ch * 32, dr);
-        tmem_wait_ld();
-        uint32_t dk[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = ch * 32 + 2 * c + e;
-            float pr = ex2_approx(__fmaf_rn(__uint_as_float(sr[2 * c + e]), c2, -l2));
-            if (edge && ((p.causal && k0 + col > m) || k0 + col >= p.N)) pr = 0.f;
-            dv[e] = pr * (__uint_as_float(dr[2 * c + e]) - dd);
-          }
-          dk[c] = pack_bf16x2(dv[0], dv[1]);
-        }
-        tmem_st16(tmem + lane_off + T_S + ch * 16, dk);
+      for (int c = 0; c < 32; ++c) {
+        const uint64_t a = fma2(f2_pack(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1])), c22, nl2);
+        pr[2 * c] = ex2_approx(f2_lo(a));
+        pr[2 * c + 1] = ex2_approx(f2_hi(a));
       }
+      if (__builtin_expect((causal && jt == i) || k0 + 64 > N, 0)) {
+        const int c_hi = min(causal ? m - k0 : 63, N - 1 - k0);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pr[c] = (c <= c_hi) ? pr[c] : 0.f;
+      }
+      uint32_t dk[32];
+      const uint64_t ndd = f2_pack(-dd, -dd);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const uint64_t dpm = add2(f2_pack(__uint_as_float(dr[2 * c]), __uint_as_float(dr[2 * c + 1])), ndd);
+        const uint64_t ds = mul2(f2_pack(pr[2 * c], pr[2 * c + 1]), dpm);
+        dk[c] = pack_bf16x2(f2_lo(ds), f2_hi(ds));
+      }
+      // the dS buffer of tile jt was read by dQ(jt-2)
+      if (jt >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&ctl->dq_done[jt & 1], ((jt - 2) >> 1) & 1, status, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      tmem_st32<0>(tmem + lane_off + T_DS + (jt & 1) * 64 + 32 * hh, dk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ctl->p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_full);
     }
-    if (ok && nk > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, (nk - 1) & 1, status, abort_flag));
-      tc_fence_after();
-    }
-    float g[D];
-    if (ok && nk > 0) tmem_row<D>(tmem + lane_off + T_DQ, g);
-    else
+    if (hh == 0) {
+      if (ok && nk > 0) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->dq_done[(nk - 1) & 1], ((nk - 1) >> 1) & 1,
+                                               status, abort_flag));
+        tc_fence_after();
+      }
+      float g[D];
+      if (ok && nk > 0) tmem_row<D>(tmem + lane_off + T_DQ, g);
+      else
 #pragma unroll
-      for (int c = 0; c < D; ++c) g[c] = 0.f;
-    if (m < p.N)
-      store_grad_row<D, ROPE>(g, p.scale, m, p.rope_cs,
-                              p.dq + b * p.dq_s[0] + h * p.dq_s[1] + (int64_t)m * p.dq_s[2]);
+        for (int c = 0; c < D; ++c) g[c] = 0.f;
+      if (m < N)
+        store_grad_row<D, ROPE_OUT>(g, p.scale, m, p.rope_cs,
+                                    p.dq + b * p.dq_s[0] + h * p.dq_s[1] + (int64_t)m * p.dq_s[2]);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -621,7 +679,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dq_kernel(const __grid_constan
 // ---------------------------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------------------------
-cudaError_t launch_bwd(const BwdParams& p, bool rope, cudaStream_t stream) {
+cudaError_t launch_bwd(const BwdParams& p, int rk, cudaStream_t stream) {
   const int d = p.d;
   {
     const int64_t threads = (int64_t)p.B * p.Hq * p.N * (d / 8);
@@ -634,11 +692,15 @@ cudaError_t launch_bwd(const BwdParams& p, bool rope, cudaStream_t stream) {
   void (*kv)(BwdParams) = nullptr;
   void (*dq)(BwdParams) = nullptr;
   if (d == 128) {
-    kv = rope ? dkdv_kernel<128, true> : dkdv_kernel<128, false>;
-    dq = rope ? dq_kernel<128, true> : dq_kernel<128, false>;
+    kv = rk == kRopeFused ? dkdv_kernel<128, kRopeFused>
+         : rk == kRopePrerotated ? dkdv_kernel<128, kRopePrerotated> : dkdv_kernel<128, kRopeNone>;
+    dq = rk == kRopeFused ? dq_kernel<128, kRopeFused>
+         : rk == kRopePrerotated ? dq_kernel<128, kRopePrerotated> : dq_kernel<128, kRopeNone>;
   } else {
-    kv = rope ? dkdv_kernel<64, true> : dkdv_kernel<64, false>;
-    dq = rope ? dq_kernel<64, true> : dq_kernel<64, false>;
+    kv = rk == kRopeFused ? dkdv_kernel<64, kRopeFused>
+         : rk == kRopePrerotated ? dkdv_kernel<64, kRopePrerotated> : dkdv_kernel<64, kRopeNone>;
+    dq = rk == kRopeFused ? dq_kernel<64, kRopeFused>
+         : rk == kRopePrerotated ? dq_kernel<64, kRopePrerotated> : dq_kernel<64, kRopeNone>;
   }
   const size_t s1 = kv_smem_bytes(d), s2 = dq_smem_bytes(d);
   cudaError_t e = cudaFuncSetAttribute(kv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)s1);
@@ -648,7 +710,7 @@ cudaError_t launch_bwd(const BwdParams& p, bool rope, cudaStream_t stream) {
   kv<<<T * p.B * p.Hkv, kBwdThreads, s1, stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  dq<<<T * p.B * p.Hq, kBwdThreads, s2, stream>>>(p);
+  dq<<<T * p.B * p.Hq, kDqThreads, s2, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -133,16 +133,17 @@ __device__ __forceinline__ void advance_cs8(float (&c)[8], float (&s)[8], const 
   }
 }
 
-// Key rows are rotated by a recurrence inside blocks of BLK rows (BLK = 64 for head dim 128,
-// where each CTA of a pair rotates one 64-key half of a tile; 128 for head dim 64): with
-// CP = d/16 chunk pairs per row and RG = 128 / CP row groups, row r of the block at n0 starts
-// from the table entry of position n0 + (r % RG) and advances (r / RG) times by the table
-// entry of position RG. key_cs8 evaluates exactly that sequence for one row, so a kernel that
-// rotates keys row by row reproduces the in-block recurrence bit for bit.
-template <int D>
+// Rows are rotated by a recurrence inside blocks of BLK rows: with CP = d/16 chunk pairs per
+// row and RG = 128 / CP row groups, row r of the block at n0 starts from the table entry of
+// position n0 + (r % RG) and advances (r / RG) times by the table entry of position RG. The
+// forward rotates keys in blocks of 64 (head dim 128: each CTA of a pair rotates one 64-key
+// half of a tile) or 128 (head dim 64); the backward rotates Q and K tiles in blocks of 128.
+// key_cs8 evaluates exactly that sequence for one row, so a kernel that rotates row by row
+// reproduces the in-block recurrence bit for bit.
+template <int D, int BLK>
 __device__ __forceinline__ void key_cs8(const float2* __restrict__ cs, int n, int chunk,
                                         float (&c)[8], float (&s)[8]) {
-  constexpr int CP = D / 16, RG = 128 / CP, BLK = (D == 128) ? 64 : 128;
+  constexpr int CP = D / 16, RG = 128 / CP;
   const int n0 = n & ~(BLK - 1), r = n & (BLK - 1);
   load_cs8(cs + (size_t)(n0 + r % RG) * (D / 2) + chunk * 8, c, s);
   float wc[8], ws[8];

@@ -670,12 +670,12 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int N, int half, Rope
 // Pre-rotation (paper Fig. 1a): out[b,h,n,:] = R_n x[b,h,n,:], out contiguous. One thread per
 // (row, chunk pair); HBM-bound elementwise pass.
 // ---------------------------------------------------------------------------------------------
-template <bool OUT_F16, int KEY_D>
+template <bool OUT_F16, int KEY_D, int BLK>
 __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb, int64_t sh,
                                  int64_t sn, __nv_bfloat16* __restrict__ out, int H, int N, int d,
                                  const float2* __restrict__ cs, int64_t rows) {
-  // KEY_D != 0: keys, whose (cos, sin) follow the fused kernel's in-tile recurrence (key_cs8)
-  // so that fused and pre-rotated attention see bit-identical K'. KEY_D == 0: table entries.
+  // KEY_D != 0: the (cos, sin) follow a kernel's in-block recurrence (key_cs8 with blocks of
+  // BLK rows) so that on-chip and pre-rotated operands are bit-identical. KEY_D == 0: table.
   const int cp = d / 16;
   const int64_t total = rows * cp;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -690,7 +690,7 @@ __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb
     uint4 lo = *reinterpret_cast<const uint4*>(src + c * 8);
     uint4 hi = *reinterpret_cast<const uint4*>(src + d / 2 + c * 8);
     float cc[8], ss[8];
-    if (KEY_D != 0) key_cs8<KEY_D == 0 ? 64 : KEY_D>(cs, n, c, cc, ss);
+    if (KEY_D != 0) key_cs8<KEY_D == 0 ? 64 : KEY_D, BLK>(cs, n, c, cc, ss);
     else load_cs8(cs + (size_t)n * (d / 2) + c * 8, cc, ss);
     rot_chunk_cs<OUT_F16>(lo, hi, cc, ss);
     __nv_bfloat16* dst = out + row * d;
@@ -726,15 +726,20 @@ cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
 }
 
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
-                             int N, int d, const float2* cs, bool out_f16, bool keys,
+                             int N, int d, const float2* cs, bool out_f16, int block,
                              cudaStream_t stream) {
   const int64_t rows = static_cast<int64_t>(B) * H * N;
   const int64_t total = rows * (d / 16);
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<int64_t>((total + threads - 1) / threads, 152 * 16));
-  auto fn = !out_f16 ? prerotate_kernel<false, 0>
-            : !keys ? prerotate_kernel<true, 0>
-            : d == 128 ? prerotate_kernel<true, 128> : prerotate_kernel<true, 64>;
+  void (*fn)(const __nv_bfloat16*, int64_t, int64_t, int64_t, __nv_bfloat16*, int, int, int,
+             const float2*, int64_t) = nullptr;
+  if (block == 0)
+    fn = out_f16 ? prerotate_kernel<true, 0, 128> : prerotate_kernel<false, 0, 128>;
+  else if (out_f16)  // forward keys: blocks of 64 (head dim 128) or 128 (head dim 64)
+    fn = d == 128 ? prerotate_kernel<true, 128, 64> : prerotate_kernel<true, 64, 128>;
+  else               // backward operands: blocks of 128
+    fn = d == 128 ? prerotate_kernel<false, 128, 128> : prerotate_kernel<false, 64, 128>;
   fn<<<blocks, threads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(x), strides[0], strides[1], strides[2],
       static_cast<__nv_bfloat16*>(out), H, N, d, cs, rows);

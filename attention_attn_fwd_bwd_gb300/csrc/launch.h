@@ -57,7 +57,9 @@ struct BwdParams {
   float scale, scale_log2;
   int* status;
 };
-cudaError_t launch_bwd(const BwdParams& p, bool rope, cudaStream_t stream);
+// rope_kind: kRopeNone, kRopeFused (Q / K tiles rotated on chip) or kRopePrerotated (tmQ /
+// tmK point at pre-rotated copies); dQ and dK are rotated back unless kRopeNone.
+cudaError_t launch_bwd(const BwdParams& p, int rope_kind, cudaStream_t stream);
 
 size_t decode_smem_size(int d);
 cudaError_t launch_decode(const DecParams& p, int d, bool rope_q, cudaStream_t stream);
@@ -74,8 +76,11 @@ size_t fwd_pair_smem_size();
 cudaError_t launch_fwd_pair(const FwdParams& p, int rope_kind, int clusters, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
                               cudaStream_t stream);
+// block: 0 = rotate with the table entry of each row; otherwise the in-block recurrence of the
+// kernels (forward keys: fp16 output, blocks of 64 / 128 for head dim 128 / 64; backward Q and
+// K: bf16 output, blocks of 128).
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
-                             int N, int d, const float2* cs, bool out_f16, bool keys,
+                             int N, int d, const float2* cs, bool out_f16, int block,
                              cudaStream_t stream);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
 // Record a message for attnfuse_last_error() and return code.

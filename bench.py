@@ -484,11 +484,14 @@ def run_train_bench(args):
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         wsf = torch.empty(af.fwd_workspace_size(B, Hq, Hkv, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
-        wsb = torch.empty(af.bwd_workspace_size(B, Hq, Hkv, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
+        wsb = torch.empty(af.bwd_workspace_size(B, Hq, Hkv, N, d, af.ROPE_PREROTATE), dtype=torch.uint8, device=dev)
         fwd = lambda: af.fwd(q, k, v, rope_theta=theta, out=out, lse=lse, workspace=wsf)
         bwd = lambda: af.bwd(q, k, v, out, lse, do, rope_theta=theta, dq=dq, dk=dk, dv=dv, workspace=wsb)
+        bwd_pre = lambda: af.bwd(q, k, v, out, lse, do, rope_theta=theta, rope_mode=af.ROPE_PREROTATE,
+                                 dq=dq, dk=dk, dv=dv, workspace=wsb)
         tf, tf_min, tf_p90 = _time_ms(fwd)
         tb, tb_min, tb_p90 = _time_ms(bwd)
+        tbp, _, _ = _time_ms(bwd_pre)
         fl = causal_flops(B, Hq, N, d)
         print(json.dumps({"train": "fused_rope_causal", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                           "fwd_ms": tf, "bwd_ms": tb, "fwd_tflops": fl / tf / 1e9,
@@ -497,7 +500,8 @@ def run_train_bench(args):
                           "bwd_frac_of_peak": 2.5 * fl / tb / 1e9 / peak,
                           "total_frac_of_peak": 3.5 * fl / (tf + tb) / 1e9 / peak,
                           "fwd_min_p90_ms": [tf_min, tf_p90], "bwd_min_p90_ms": [tb_min, tb_p90],
-                          "launches": {"fwd": 2, "bwd": 4}}), flush=True)
+                          "bwd_prerotate_ms": tbp, "bwd_prerotate_tflops": 2.5 * fl / tbp / 1e9,
+                          "launches": {"fwd": 2, "bwd": 4, "bwd_prerotate": 6}}), flush=True)
 
 
 def run_variants_bench(args):
