@@ -463,6 +463,8 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
   if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k"))) return rc;
   if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v"))) return rc;
   if ((rc = encode_bhnd(&p.tmDO, dout, do_strides, B, Hq, N, d, "dout"))) return rc;
+  if ((rc = encode_bhnd(&p.tmQ64, qa, qs, B, Hq, N, d, "q", 64))) return rc;
+  if ((rc = encode_bhnd(&p.tmDO64, dout, do_strides, B, Hq, N, d, "dout", 64))) return rc;
   p.o = static_cast<const __nv_bfloat16*>(out);
   p.dout = static_cast<const __nv_bfloat16*>(dout);
   for (int i = 0; i < 3; ++i) {

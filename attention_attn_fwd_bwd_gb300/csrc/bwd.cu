@@ -1,10 +1,12 @@
 // Backward attention for sm_103a (AttnFuse paper §4.4): three kernels and no atomics.
 //   bwd_pre_kernel   D_m = sum_c dO_mc O_mc                       (HBM-bound row reduction)
 //   dkdv_kernel      one CTA per (key tile, kv head, batch): K' and V stay in shared memory;
-//                    for every query head of the GQA group and every query tile that can see
-//                    the key tile: S^T = K' Q'^T and dP^T = V dO^T (tcgen05, TMEM), then
-//                    P^T = exp(S^T - L), dS^T = P^T (dP^T - D), dV += P^T dO, dK' += dS^T Q'.
-//                    Epilogue: dK = scale R_n^T dK', dV (GQA sums stay inside the CTA).
+//                    for every query head of the GQA group and every 64-row query tile that
+//                    can see the key tile: S^T = K' Q'^T and dP^T = V dO^T (tcgen05, TMEM),
+//                    then P^T = exp(S^T - L), dS^T = P^T (dP^T - D), dV += P^T dO,
+//                    dK' += dS^T Q' (two TMEM buffer sets, so item i+1's S^T / dP^T overlap
+//                    item i's element-wise step). Epilogue: dK = scale R_n^T dK', dV (GQA sums
+//                    stay inside the CTA).
 //   dq_kernel        one CTA per (query tile, head, batch): Q' and dO stay in shared memory;
 //                    for every visible key tile: S = Q' K'^T, dP = dO V^T, dS = P (dP - D),
 //                    dQ' += dS K' (dS double-buffered in TMEM, so the next tile's S and dP
@@ -30,20 +32,23 @@ namespace {
 constexpr int kBwdThreads = 384;
 constexpr int kT = 128;  // tile edge (keys and queries)
 
-// Rotate a [128 x D] bf16 tile (128B-swizzled panels) in place: row r at position pos0 + r.
-// Executed by 128 threads (t = 0..127): thread t owns chunk pair c = t % CP of rows
-// t / CP + RG k, so it reads the (cos, sin) table once (its first row) and advances the angle
-// by RG positions per row (angle addition), instead of one dependent table read per row.
+// Rotate a [TR x D] bf16 tile (TR = 64 or 128 rows, 128B-swizzled panels of TR rows) in place:
+// row r at position pos0 + r. Executed by 128 threads (t = 0..127): thread t owns chunk pair
+// c = t % CP of rows t / CP + RG k, so it reads the (cos, sin) table once and advances the
+// angle by RG positions per row (angle addition) instead of one dependent table read per row.
+// The recurrence runs over blocks of 128 positions (a 64-row tile at pos0 % 128 == 64 starts
+// (64 / RG) steps in), matching the pre-rotation kernel's blocks of 128 bit for bit.
 // Rows at or beyond N are left untouched.
-template <int D>
+template <int D, int TR>
 __device__ __forceinline__ void rotate_tile_bf16(uint8_t* tile, int pos0, int N,
                                                  const float2* __restrict__ cs, int t) {
-  constexpr int CP = D / 16, RG = 128 / CP, ROWS = kT / RG;
+  constexpr int CP = D / 16, RG = 128 / CP, ROWS = TR / RG;
   const int c = t % CP, rg = t / CP;
   float cc[8], ss[8], wc[8], ws[8];
   load_cs8(cs + (size_t)RG * (D / 2) + c * 8, wc, ws);
-  const int p0 = min(pos0 + rg, N - 1);
+  const int p0 = min((pos0 & ~127) + rg, N - 1);
   load_cs8(cs + (size_t)p0 * (D / 2) + c * 8, cc, ss);
+  for (int k = 0; k < (pos0 & 127) / RG; ++k) advance_cs8(cc, ss, wc, ws);
 #pragma unroll
   for (int k = 0; k < ROWS; ++k) {
     const int row = rg + RG * k;
@@ -51,7 +56,7 @@ __device__ __forceinline__ void rotate_tile_bf16(uint8_t* tile, int pos0, int N,
       uint32_t offl, offh;
       if (D == 128) {
         offl = sw128_offset(row, c);
-        offh = offl + kT * 128;
+        offh = offl + TR * 128;
       } else {
         offl = sw128_offset(row, c);
         offh = sw128_offset(row, c + 4);
@@ -106,23 +111,26 @@ __device__ __forceinline__ void tmem_row(uint32_t taddr, float (&g)[D]) {
   }
 }
 
+constexpr int kBq = 64;  // query rows per dK/dV item
+
 template <int D>
 struct KvCfg {
   static constexpr int PANELS = D / 64;
-  static constexpr uint32_t TILE = kT * D * 2;
-  static constexpr int QST = 2;  // query / dO stages
+  static constexpr uint32_t TILE = kT * D * 2;   // K, V: 128 rows
+  static constexpr uint32_t QT = kBq * D * 2;    // Q, dO: 64 rows
+  static constexpr int QST = 4;                  // Q / dO stages
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = TILE;
   static constexpr uint32_t OFF_Q = 2 * TILE;
-  static constexpr uint32_t OFF_DO = OFF_Q + QST * TILE;
-  static constexpr uint32_t OFF_VEC = OFF_DO + QST * TILE;  // per stage: L (128 f32), D (128 f32)
-  static constexpr uint32_t OFF_CTL = OFF_VEC + QST * 1024;
+  static constexpr uint32_t OFF_DO = OFF_Q + QST * QT;
+  static constexpr uint32_t OFF_VEC = OFF_DO + QST * QT;  // per stage: L (64 f32), D (64 f32)
+  static constexpr uint32_t OFF_CTL = OFF_VEC + QST * 512;
 };
 
 struct KvCtl {
   uint64_t k_full, v_full, k_ready;
-  uint64_t q_full[2], do_full[2], q_ready[2], vec_ready[2], stage_free[2];
-  uint64_t st_full, p_full, mma_done, mma_final;
+  uint64_t q_full[4], do_full[4], q_ready[4], vec_full[4], stage_free[4];
+  uint64_t st_full[2], p_full[2], mma_done[2], mma_final;
   uint32_t tmem_base;
   int abort_flag;
 };
@@ -153,7 +161,7 @@ static_assert(kDqRegsLow + kDqRegsRot + 2 * kDqRegsEw <= 4 * (65536 / kDqThreads
               "register split exceeds the registers the CTA is launched with");
 
 __host__ __device__ constexpr size_t kv_smem_bytes(int D) {
-  return 1024 + (2 + 2 * 2) * (size_t)(kT * D * 2) + 2 * 1024 + sizeof(KvCtl);
+  return 1024 + 2 * (size_t)(kT * D * 2) + 2 * 4 * (size_t)(kBq * D * 2) + 4 * 512 + sizeof(KvCtl);
 }
 __host__ __device__ constexpr size_t dq_smem_bytes(int D) {
   return 1024 + (2 + 2 * 2) * (size_t)(kT * D * 2) + sizeof(DqCtl);
@@ -197,27 +205,35 @@ __global__ void bwd_pre_kernel(const __grid_constant__ BwdParams p) {
 // ---------------------------------------------------------------------------------------------
 // dK, dV
 // ---------------------------------------------------------------------------------------------
+// Items are (query head of the GQA group, 64-row query tile). TMEM: dV [0, D), dK' [D, 2D),
+// and two buffer sets b = item & 1 of S^T [256 + 64b, +64) and dP^T [384 + 64b, +64), each
+// overwritten in place by P^T / dS^T (bf16). While the element-wise warps work on item i, the
+// tensor cores compute S^T and dP^T of item i+1 in the other set, then dV and dK' of item i.
 template <int D, int RK>
 __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_constant__ BwdParams p) {
   constexpr bool ROPE = (RK == kRopeFused);      // rotate Q / K tiles on chip
   constexpr bool ROPE_OUT = (RK != kRopeNone);   // rotate dK back
   using C = KvCfg<D>;
+  constexpr int QST = C::QST;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   KvCtl* ctl = reinterpret_cast<KvCtl*>(smem + C::OFF_CTL);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int TK = (p.N + kT - 1) / kT;
-  const int TQ = TK;
+  const int N = p.N;
+  const int TK = (N + kT - 1) / kT;
+  const int TQ64 = (N + kBq - 1) / kBq;
   // Group-major order: the CTAs running together share one (b, kv head) group, so that
   // group's Q and dO (re-read by every key tile) stay in L2. Within a group, key tile 0 (the
   // most query tiles under causal masking) goes first.
   const int grp = static_cast<int>(blockIdx.x) / TK;
   const int j = static_cast<int>(blockIdx.x) % TK;
   const int b = grp / p.Hkv, kvh = grp % p.Hkv;
-  const int i0 = first_q_tile(p, j);
-  const int nq = TQ - i0;             // query tiles per head
-  const int total = p.g * nq;         // (head, query tile) items
+  const bool causal = p.causal != 0;
+  const int i0 = causal ? 2 * j : 0;  // first 64-row query tile that can see key tile j
+  const int nq = TQ64 - i0;           // query tiles per head
+  const int g = p.g;
+  const int total = g * nq;           // (head, query tile) items
   int* status = p.status;
   volatile int* abort_flag = &ctl->abort_flag;
 
@@ -225,16 +241,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
     mbar_init(&ctl->k_full, 1);
     mbar_init(&ctl->v_full, 1);
     mbar_init(&ctl->k_ready, 128);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < QST; ++s) {
       mbar_init(&ctl->q_full[s], 1);
       mbar_init(&ctl->do_full[s], 1);
       mbar_init(&ctl->q_ready[s], 128);
-      mbar_init(&ctl->vec_ready[s], 128);
+      mbar_init(&ctl->vec_full[s], 4);  // one arrival per element-wise warp
       mbar_init(&ctl->stage_free[s], 1);
     }
-    mbar_init(&ctl->st_full, 1);
-    mbar_init(&ctl->p_full, 128);
-    mbar_init(&ctl->mma_done, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl->st_full[s], 1);
+      mbar_init(&ctl->p_full[s], 4);
+      mbar_init(&ctl->mma_done[s], 1);
+    }
     mbar_init(&ctl->mma_final, 1);
     ctl->abort_flag = 0;
     fence_mbar_init();
@@ -244,16 +262,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  // TMEM: dV [0, D), dK' [D, 2D), S^T [2D, 2D+128), dP^T [2D+128, 2D+256)
-  const uint32_t T_DV = 0, T_DK = D, T_S = 2 * D, T_DP = 2 * D + 128;
+  constexpr uint32_t T_DV = 0, T_DK = D, T_S = 256, T_DP = 384;
 
   if (warp == 0) {
     if (lane == 0) {
       // ---- TMA: K, V once; then Q and dO for every (head, query tile) ----
-      tma_prefetch_desc(&p.tmQ);
+      tma_prefetch_desc(&p.tmQ64);
       tma_prefetch_desc(&p.tmK);
       tma_prefetch_desc(&p.tmV);
-      tma_prefetch_desc(&p.tmDO);
+      tma_prefetch_desc(&p.tmDO64);
       mbar_arrive_expect_tx(&ctl->k_full, C::TILE);
       for (int pn = 0; pn < C::PANELS; ++pn)
         tma_load_4d(smem + C::OFF_K + pn * (kT * 128), &p.tmK, &ctl->k_full, pn * 64, j * kT, kvh, b);
@@ -262,68 +279,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
         tma_load_4d(smem + C::OFF_V + pn * (kT * 128), &p.tmV, &ctl->v_full, pn * 64, j * kT, kvh, b);
       int it = 0;
       for (; it < total; ++it) {
-        const int s = it & 1;
-        const int h = kvh * p.g + it / nq, qi = i0 + it % nq;
-        if (it >= 2 && !mbar_wait(&ctl->stage_free[s], ((it >> 1) - 1) & 1, status, abort_flag)) break;
-        mbar_arrive_expect_tx(&ctl->q_full[s], C::TILE);
+        const int s = it % QST;
+        const int h = kvh * g + it / nq, qi = i0 + it % nq;
+        if (it >= QST && !mbar_wait(&ctl->stage_free[s], ((it / QST) - 1) & 1, status, abort_flag)) break;
+        mbar_arrive_expect_tx(&ctl->q_full[s], C::QT);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_Q + s * C::TILE + pn * (kT * 128), &p.tmQ, &ctl->q_full[s],
-                      pn * 64, qi * kT, h, b);
-        mbar_arrive_expect_tx(&ctl->do_full[s], C::TILE);
+          tma_load_4d(smem + C::OFF_Q + s * C::QT + pn * (kBq * 128), &p.tmQ64, &ctl->q_full[s],
+                      pn * 64, qi * kBq, h, b);
+        mbar_arrive_expect_tx(&ctl->do_full[s], C::QT);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_DO + s * C::TILE + pn * (kT * 128), &p.tmDO, &ctl->do_full[s],
-                      pn * 64, qi * kT, h, b);
+          tma_load_4d(smem + C::OFF_DO + s * C::QT + pn * (kBq * 128), &p.tmDO64, &ctl->do_full[s],
+                      pn * 64, qi * kBq, h, b);
       }
       mbar_wait(&ctl->k_full, 0, status, nullptr);
       mbar_wait(&ctl->v_full, 0, status, nullptr);
-      for (int k = max(0, it - 2); k < it; ++k) {
-        mbar_wait(&ctl->q_full[k & 1], (k >> 1) & 1, status, nullptr);
-        mbar_wait(&ctl->do_full[k & 1], (k >> 1) & 1, status, nullptr);
+      for (int k = max(0, it - QST); k < it; ++k) {
+        mbar_wait(&ctl->q_full[k % QST], (k / QST) & 1, status, nullptr);
+        mbar_wait(&ctl->do_full[k % QST], (k / QST) & 1, status, nullptr);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---- MMA ----
-      constexpr uint32_t idesc_st = idesc_bf16_f32(128, kT, 0, 0);  // S^T, dP^T: both K-major
-      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);    // dV, dK': B MN-major
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, kBq, 0, 0);  // S^T, dP^T: K-major
+      constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);     // dV, dK': B MN-major
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
+      auto issue_st = [&](int it) -> bool {  // S^T, dP^T of item it into set it & 1
+        const int s = it % QST, bs = it & 1;
+        const uint32_t ph = (it / QST) & 1;
+        if (!mbar_wait(&ctl->q_ready[s], ph, status, abort_flag)) return false;
+        if (!mbar_wait(&ctl->do_full[s], ph, status, abort_flag)) return false;
+        // the set was last read by dV / dK' of item it-2
+        if (it >= 2 && !mbar_wait(&ctl->mma_done[bs], ((it - 2) >> 1) & 1, status, abort_flag))
+          return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * (kBq * 128) + (kk & 3) * 32;
+          mma_ss(tmem + T_S + 64 * bs, smem_desc_sw128(sK + ko, 16, 1024),
+                 smem_desc_sw128(sQ + s * C::QT + qo, 16, 1024), idesc_st, kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
+          const uint32_t qo = (kk >> 2) * (kBq * 128) + (kk & 3) * 32;
+          mma_ss(tmem + T_DP + 64 * bs, smem_desc_sw128(sV + ko, 16, 1024),
+                 smem_desc_sw128(sDO + s * C::QT + qo, 16, 1024), idesc_st, kk > 0);
+        }
+        mma_commit(&ctl->st_full[bs]);
+        return true;
+      };
+      auto issue_g = [&](int it) -> bool {  // dV += P^T dO ; dK' += dS^T Q'
+        const int s = it % QST, bs = it & 1;
+        if (!mbar_wait(&ctl->p_full[bs], (it >> 1) & 1, status, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kBq / 16; ++kk) {
+          mma_ts(tmem + T_DV, tmem + T_S + 64 * bs + kk * 8,
+                 smem_desc_sw128(sDO + s * C::QT + kk * 2048, kBq * 128, 1024), idesc_g,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + T_DK, tmem + T_DP + 64 * bs + kk * 8,
+                 smem_desc_sw128(sQ + s * C::QT + kk * 2048, kBq * 128, 1024), idesc_g,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&ctl->mma_done[bs]);
+        mma_commit(&ctl->stage_free[s]);
+        return true;
+      };
       bool ok = mbar_wait(&ctl->k_ready, 0, status, abort_flag) &&
                 mbar_wait(&ctl->v_full, 0, status, abort_flag);
+      if (ok && total > 0) ok = issue_st(0);
       for (int it = 0; ok && it < total; ++it) {
-        const int s = it & 1;
-        const uint32_t ph = (it >> 1) & 1;
-        if (!mbar_wait(&ctl->q_ready[s], ph, status, abort_flag)) break;
-        if (!mbar_wait(&ctl->do_full[s], ph, status, abort_flag)) break;
-        if (it > 0 && !mbar_wait(&ctl->mma_done, (it - 1) & 1, status, abort_flag)) break;
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
-          mma_ss(tmem + T_S, smem_desc_sw128(sK + koff, 16, 1024),
-                 smem_desc_sw128(sQ + s * C::TILE + koff, 16, 1024), idesc_st, kk > 0);
-        }
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
-          mma_ss(tmem + T_DP, smem_desc_sw128(sV + koff, 16, 1024),
-                 smem_desc_sw128(sDO + s * C::TILE + koff, 16, 1024), idesc_st, kk > 0);
-        }
-        mma_commit(&ctl->st_full);
-        if (!mbar_wait(&ctl->p_full, it & 1, status, abort_flag)) break;
-        tc_fence_after();
-        // dV += P^T dO ; dK' += dS^T Q'   (A from TMEM, B = dO / Q' MN-major)
-#pragma unroll
-        for (int kk = 0; kk < kT / 16; ++kk) {
-          mma_ts(tmem + T_DV, tmem + T_S + kk * 8,
-                 smem_desc_sw128(sDO + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-          mma_ts(tmem + T_DK, tmem + T_DP + kk * 8,
-                 smem_desc_sw128(sQ + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&ctl->mma_done);
-        mma_commit(&ctl->stage_free[s]);
+        if (it + 1 < total) ok = issue_st(it + 1);
+        if (ok) ok = issue_g(it);
       }
       mma_commit(&ctl->mma_final);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
@@ -333,101 +363,111 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
     const int t = tid - 256;
     if (ROPE) {
       if (mbar_wait(&ctl->k_full, 0, status, abort_flag))
-        rotate_tile_bf16<D>(smem + C::OFF_K, j * kT, p.N, p.rope_cs, t);
+        rotate_tile_bf16<D, kT>(smem + C::OFF_K, j * kT, N, p.rope_cs, t);
       fence_proxy_async_smem();
     } else {
       mbar_wait(&ctl->k_full, 0, status, abort_flag);
     }
     mbar_arrive(&ctl->k_ready);
     for (int it = 0; it < total; ++it) {
-      const int s = it & 1;
+      const int s = it % QST;
       const int qi = i0 + it % nq;
-      if (!mbar_wait(&ctl->q_full[s], (it >> 1) & 1, status, abort_flag)) break;
+      if (!mbar_wait(&ctl->q_full[s], (it / QST) & 1, status, abort_flag)) break;
       if (ROPE) {
-        rotate_tile_bf16<D>(smem + C::OFF_Q + s * C::TILE, qi * kT, p.N, p.rope_cs, t);
+        rotate_tile_bf16<D, kBq>(smem + C::OFF_Q + s * C::QT, qi * kBq, N, p.rope_cs, t);
         fence_proxy_async_smem();
       }
       mbar_arrive(&ctl->q_ready[s]);
     }
   } else if (warp >= 4) {
-    // ---- element-wise: thread = key row n of the tile ----
+    // ---- element-wise: thread = key row n of the tile, 64 query columns per item ----
     const int r = (warp - 4) * 32 + lane;
     const int n = j * kT + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC);
     bool ok = true;
     const float c2 = p.scale_log2;
+    const float* const lse = p.lse;
+    const float* const dvec = p.Dvec;
+    const int Hq = p.Hq;
     for (int it = 0; it < total; ++it) {
-      const int s = it & 1;
-      const int h = kvh * p.g + it / nq, qi = i0 + it % nq;
-      const int m0 = qi * kT;
-      // stage L (log2 units) and D of this query tile; masked rows get L = +inf (P = 0)
+      const int s = it % QST, bs = it & 1;
+      const int h = kvh * g + it / nq, qi = i0 + it % nq;
+      const int m0 = qi * kBq;
+      float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC + s * 512);
+      // stage L (log2 units) and D of the 64 query rows; rows past N get L = +inf (P = 0)
       {
-        const int m = m0 + r;
-        float l2 = __int_as_float(0x7f800000), dd = 0.f;
-        if (m < p.N) {
-          const float l = p.lse[((int64_t)b * p.Hq + h) * p.N + m];
-          l2 = (l == kNegInf) ? __int_as_float(0x7f800000) : l * kLog2e;
-          dd = p.Dvec[((int64_t)b * p.Hq + h) * p.N + m];
+        const int m = m0 + (r & 63);
+        float v = (r < 64) ? __int_as_float(0x7f800000) : 0.f;
+        if (m < N) {
+          const int64_t idx = ((int64_t)b * Hq + h) * N + m;
+          if (r < 64) {
+            const float l = lse[idx];
+            v = (l == kNegInf) ? __int_as_float(0x7f800000) : l * kLog2e;
+          } else {
+            v = dvec[idx];
+          }
         }
-        vec[s * 256 + r] = l2;
-        vec[s * 256 + 128 + r] = dd;
+        vec[r] = v;
       }
-      named_bar_sync(1, 128);
-      if (!__all_sync(0xffffffffu, mbar_wait(&ctl->st_full, it & 1, status, abort_flag))) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->vec_full[s]);
+      if (!__all_sync(0xffffffffu,
+                      mbar_wait(&ctl->vec_full[s], (it / QST) & 1, status, abort_flag) &&
+                          mbar_wait(&ctl->st_full[bs], (it >> 1) & 1, status, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const bool diag = p.causal && (qi == j);
-      // 32 columns at a time; P / dS chunk c lands in columns already read (c/2 < c+1 chunks)
+      uint32_t sr[64], dr[64];
+      tmem_ld32<0>(tmem + lane_off + T_S + 64 * bs, sr);
+      tmem_ld32<32>(tmem + lane_off + T_S + 64 * bs + 32, sr);
+      tmem_ld32<0>(tmem + lane_off + T_DP + 64 * bs, dr);
+      tmem_ld32<32>(tmem + lane_off + T_DP + 64 * bs + 32, dr);
+      tmem_wait_ld();
+      float pr[64];
 #pragma unroll
-      for (int ch = 0; ch < kT / 32; ++ch) {
-        uint32_t sr[32], dr[32];
-        tmem_ld32(tmem + lane_off + T_S + ch * 32, sr);
-        tmem_ld32(tmem + lane_off + T_DP + ch * 32, dr);
-        tmem_wait_ld();
-        uint32_t pk[16], dk[16];
+      for (int c = 0; c < 64; ++c)
+        pr[c] = ex2_approx(__fmaf_rn(__uint_as_float(sr[c]), c2, -vec[c]));
+      if (__builtin_expect(causal && m0 < n, 0)) {
+        // causal diagonal: query m0 + c sees key n only if m0 + c >= n
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int col = ch * 32 + 2 * c + e;
-            float pr = ex2_approx(__fmaf_rn(__uint_as_float(sr[2 * c + e]), c2, -vec[s * 256 + col]));
-            if (diag && m0 + col < n) pr = 0.f;
-            pv[e] = pr;
-            dv[e] = pr * (__uint_as_float(dr[2 * c + e]) - vec[s * 256 + 128 + col]);
-          }
-          pk[c] = pack_bf16x2(pv[0], pv[1]);
-          dk[c] = pack_bf16x2(dv[0], dv[1]);
-        }
-        tmem_st16(tmem + lane_off + T_S + ch * 16, pk);
-        tmem_st16(tmem + lane_off + T_DP + ch * 16, dk);
+        for (int c = 0; c < 64; ++c) pr[c] = (m0 + c >= n) ? pr[c] : 0.f;
       }
+      uint32_t pk[32], dk[32];
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float d0 = pr[2 * c] * (__uint_as_float(dr[2 * c]) - vec[64 + 2 * c]);
+        const float d1 = pr[2 * c + 1] * (__uint_as_float(dr[2 * c + 1]) - vec[64 + 2 * c + 1]);
+        pk[c] = pack_bf16x2(pr[2 * c], pr[2 * c + 1]);
+        dk[c] = pack_bf16x2(d0, d1);
+      }
+      tmem_st32<0>(tmem + lane_off + T_S + 64 * bs, pk);
+      tmem_st32<0>(tmem + lane_off + T_DP + 64 * bs, dk);
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&ctl->p_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_full[bs]);
     }
     // ---- epilogue ----
     if (ok && total > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done, (total - 1) & 1, status, abort_flag));
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->mma_done[(total - 1) & 1], ((total - 1) >> 1) & 1,
+                                             status, abort_flag));
       tc_fence_after();
     }
-    float g[D];
-    if (ok && total > 0) tmem_row<D>(tmem + lane_off + T_DV, g);
+    float gr[D];
+    if (ok && total > 0) tmem_row<D>(tmem + lane_off + T_DV, gr);
     else
 #pragma unroll
-      for (int c = 0; c < D; ++c) g[c] = 0.f;
-    if (n < p.N)
-      store_grad_row<D, false>(g, 1.f, n, p.rope_cs,
+      for (int c = 0; c < D; ++c) gr[c] = 0.f;
+    if (n < N)
+      store_grad_row<D, false>(gr, 1.f, n, p.rope_cs,
                                p.dv + b * p.dv_s[0] + kvh * p.dv_s[1] + (int64_t)n * p.dv_s[2]);
-    if (ok && total > 0) tmem_row<D>(tmem + lane_off + T_DK, g);
+    if (ok && total > 0) tmem_row<D>(tmem + lane_off + T_DK, gr);
     else
 #pragma unroll
-      for (int c = 0; c < D; ++c) g[c] = 0.f;
-    if (n < p.N)
-      store_grad_row<D, ROPE_OUT>(g, p.scale, n, p.rope_cs,
+      for (int c = 0; c < D; ++c) gr[c] = 0.f;
+    if (n < N)
+      store_grad_row<D, ROPE_OUT>(gr, p.scale, n, p.rope_cs,
                                   p.dk + b * p.dk_s[0] + kvh * p.dk_s[1] + (int64_t)n * p.dk_s[2]);
   }
   tc_fence_before();
@@ -574,7 +614,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
     setmaxnreg_dec<kDqRegsRot>();
     const int t = tid - 384;
     if (mbar_wait(&ctl->q_full, 0, status, abort_flag) && ROPE) {
-      rotate_tile_bf16<D>(smem + C::OFF_Q, i * kT, N, p.rope_cs, t);
+      rotate_tile_bf16<D, kT>(smem + C::OFF_Q, i * kT, N, p.rope_cs, t);
       fence_proxy_async_smem();
     }
     mbar_arrive(&ctl->q_ready);
@@ -582,7 +622,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       const int s = jt & 1;
       if (!mbar_wait(&ctl->k_full[s], (jt >> 1) & 1, status, abort_flag)) break;
       if (ROPE) {
-        rotate_tile_bf16<D>(smem + C::OFF_K + s * C::TILE, jt * kT, N, p.rope_cs, t);
+        rotate_tile_bf16<D, kT>(smem + C::OFF_K + s * C::TILE, jt * kT, N, p.rope_cs, t);
         fence_proxy_async_smem();
       }
       mbar_arrive(&ctl->k_ready[s]);

@@ -45,6 +45,7 @@ struct DecParams {
 
 struct BwdParams {
   CUtensorMap tmQ, tmK, tmV, tmDO;  // bf16 [B, H, N, d], box (64, 128, 1, 1)
+  CUtensorMap tmQ64, tmDO64;        // the same Q / dO with box (64, 64, 1, 1) (dK/dV items)
   const __nv_bfloat16* o;           // forward output (for D = rowsum(dO * O))
   const __nv_bfloat16* dout;
   int64_t o_s[3], do_s[3];

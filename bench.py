@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
-    ap.add_argument("--profile-target", default="fwd", choices=["fwd", "decode", "train"],
+    ap.add_argument("--profile-target", default="fwd", choices=["fwd", "decode", "train", "train-prerotate"],
                     help="--profile: forward workload, Llama-3-70B decode (B=8) or fwd+bwd (N=2048)")
     return ap.parse_args()
 
@@ -428,12 +428,13 @@ def run_profile(args):
         q, kc, vc = (x[n].cuda() for n in ("q", "k_cache", "v_cache"))
         for _ in range(2):
             af.decode(q, kc, vc, 32767, rope_theta=5e5)
-    elif args.profile_target == "train":
+    elif args.profile_target in ("train", "train-prerotate"):
         x = inputs.prefill(8, 32, 8, 2048, 128, seed=6048, with_dout=True)
         q, k, v, do = (x[n].cuda() for n in ("q", "k", "v", "dout"))
+        mode = af.ROPE_PREROTATE if args.profile_target == "train-prerotate" else af.ROPE_FUSED
         for _ in range(2):
             out, lse = af.fwd(q, k, v, rope_theta=5e5)
-            af.bwd(q, k, v, out, lse, do, rope_theta=5e5)
+            af.bwd(q, k, v, out, lse, do, rope_theta=5e5, rope_mode=mode)
     else:
         B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
         rope_mode = {"fused": af.ROPE_FUSED, "prerotate": af.ROPE_PREROTATE, "none": af.ROPE_NONE}[mode]
