@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
-    ap.add_argument("--profile-target", default="fwd", choices=["fwd", "decode", "train", "train-prerotate"],
+    ap.add_argument("--profile-target", default="fwd", choices=["fwd", "decode", "decode-b1", "train", "train-prerotate"],
                     help="--profile: forward workload, Llama-3-70B decode (B=8) or fwd+bwd (N=2048)")
     return ap.parse_args()
 
@@ -423,8 +423,8 @@ def run_profile(args):
     import attention_attn_fwd_bwd_gb300 as af
     from attention_attn_fwd_bwd_gb300 import inputs
 
-    if args.profile_target == "decode":
-        x = inputs.decode(8, 64, 8, 32768, 128, seed=5008)
+    if args.profile_target in ("decode", "decode-b1"):
+        x = inputs.decode(8 if args.profile_target == "decode" else 1, 64, 8, 32768, 128, seed=5008)
         q, kc, vc = (x[n].cuda() for n in ("q", "k_cache", "v_cache"))
         for _ in range(2):
             af.decode(q, kc, vc, 32767, rope_theta=5e5)
