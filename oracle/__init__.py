@@ -71,7 +71,7 @@ def _load():
             lib.orc_rope.argtypes = [P, P, I64, I, P, D, I]
             lib.orc_fwd.argtypes = [P, P, P, I, I, I, I64, I, D, D, I, VP, P, P]
             lib.orc_fwd_rows.argtypes = [P, P, P, I, I, I, I64, I, D, D, I, VP, I64, P, P, P]
-            lib.orc_bwd.argtypes = [P, P, P, P, I, I, I, I64, I, D, D, I, VP, I64, P, P, P, P, P, P]
+            lib.orc_bwd.argtypes = [P, P, P, P, I, I, I, I64, I, D, D, I, VP, I64, P, P, P, P, P, P, P]
             lib.orc_bwd_dq_rows.argtypes = [P, P, P, P, I, I, I, I64, I, D, D, I, VP, I64, P, P]
             lib.orc_decode.argtypes = [P, P, P, I, I, I, I64, I, I64, D, D, I, P, P]
             lib.orc_tile_visits.argtypes = [I64, I, I, VP, P]
@@ -180,8 +180,11 @@ def forward_rows(q, k, v, scale, theta, rope_on, variant: Variant, rows):
     return out, lse
 
 
-def backward(q, k, v, dout, scale, theta, rope_on, variant: Variant, groups=None):
-    """(O, LSE, dQ, dK, dV). groups: optional [G, 2] list of (b, kv_head) to compute."""
+def backward(q, k, v, dout, scale, theta, rope_on, variant: Variant, groups=None,
+             with_dbias=False):
+    """(O, LSE, dQ, dK, dV), plus dBias [B, Hq, N, N] (the gradient with respect to an additive
+    bias, before any broadcast is summed out) when with_dbias. groups: optional [G, 2] list of
+    (b, kv_head) to compute."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     B, Hq, N, d = q.shape
     Hkv = k.shape[1]
@@ -190,6 +193,7 @@ def backward(q, k, v, dout, scale, theta, rope_on, variant: Variant, groups=None
     dq = np.zeros_like(q)
     dk = np.zeros_like(k)
     dv = np.zeros_like(v)
+    dbias = np.zeros((B, Hq, N, N)) if with_dbias else None
     g = None
     if groups is not None:
         g = np.ascontiguousarray(groups, np.int64).reshape(-1, 2)
@@ -197,9 +201,12 @@ def backward(q, k, v, dout, scale, theta, rope_on, variant: Variant, groups=None
     rc = _load().orc_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, Hq,
                          Hkv, N, d, float(scale), float(theta), int(rope_on), ctypes.byref(cv),
                          0 if g is None else g.shape[0], _ptr(g), out.ctypes.data,
-                         lse.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data)
+                         lse.ctypes.data, dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                         _ptr(dbias))
     if rc:
         raise RuntimeError(f"orc_bwd failed ({rc})")
+    if with_dbias:
+        return out, lse, dq, dk, dv, dbias
     return out, lse, dq, dk, dv
 
 

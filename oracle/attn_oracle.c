@@ -20,7 +20,8 @@
  *   D_m = <dO_m, O_m>, dP_mn = <dO_m, v_n>, dS_mn = P_mn (dP_mn - D_m),
  *   dq'_m = scale sum_n dS_mn k'_n, dk'_n = scale sum_m dS_mn q'_m, dv_n = sum_m P_mn dO_m,
  *   dq_m = R_m^T dq'_m, dk_n = R_n^T dk'_n  (gradients w.r.t. the un-rotated inputs),
- *   dk, dv summed over the query heads that share a key/value head (GQA).
+ *   dk, dv summed over the query heads that share a key/value head (GQA),
+ *   dBias_mn = dS_mn (the bias enters s_mn with weight 1, after the scaling, §3.1).
  *
  * Readings where the pages are silent (each is also listed in the design notes):
  *   - theta_i = theta^(-2i/d), i < d/2 (RoFormer, the paper's RoPE reference); pair (i, i+d/2).
@@ -255,11 +256,13 @@ int orc_fwd_rows(const double* q, const double* k, const double* v, int B, int H
 /* Backward (paper §4.4), by direct differentiation of the forward definition.              */
 /* groups: optional list of (b, kvh) pairs [2*ngroups]; NULL = every group. Only the heads  */
 /* of the listed groups are computed; other entries of out/lse/dq/dk/dv are left untouched.  */
+/* dbias: optional [B, Hq, N, N] output, the gradient with respect to an additive bias       */
+/* element (b, h, m, n): dS_mn, and 0 where (m, n) is masked.                                */
 /* ---------------------------------------------------------------------------------------- */
 int orc_bwd(const double* q, const double* k, const double* v, const double* dout, int B, int Hq,
             int Hkv, int64_t N, int d, double scale, double theta, int rope,
             const orc_variant* var, int64_t ngroups, const int64_t* groups, double* out,
-            double* lse, double* dq, double* dk, double* dv) {
+            double* lse, double* dq, double* dk, double* dv, double* dbias) {
   if (check_shape(B, Hq, Hkv, N, d)) return 1;
   const int g = Hq / Hkv;
   const int64_t G = groups ? ngroups : (int64_t)B * Hkv;
@@ -308,11 +311,15 @@ int orc_bwd(const double* q, const double* k, const double* v, const double* dou
         const double l = row_forward(var, b, h, m, qr, kr, vh, N, d, scale, s, p, orow);
         lse[bh * N + m] = l;
         const double Dm = dot(dorow, orow, d);
+        double* dbrow = dbias ? dbias + (bh * N + m) * N : NULL;
+        if (dbrow)
+          for (int64_t n = 0; n < N; ++n) dbrow[n] = 0.0;
         for (int c = 0; c < d; ++c) dqr[c] = 0.0;
         for (int64_t n = 0; n < N; ++n) {
           if (p[n] == 0.0) continue;
           const double dP = dot(dorow, vh + n * d, d);
           const double dS = p[n] * (dP - Dm);
+          if (dbrow) dbrow[n] = dS;
           for (int c = 0; c < d; ++c) {
             dqr[c] += scale * dS * kr[n * d + c];
             dk_acc[n * d + c] += scale * dS * qr[c];

@@ -270,10 +270,13 @@ def _variants(orc, H, N):
         orc.Variant(mask=1, bias=1, slopes=inputs.alibi_slopes(H)),
         orc.Variant(mask=0, bias=2, add_bias=_rand((1, H, N, N), 41)),
         orc.Variant(mask=3, bs_block=4, bs_row_ptr=rp, bs_col_idx=ci),
+        orc.Variant(mask=2, window=3, bias=1, slopes=inputs.alibi_slopes(H)),
+        orc.Variant(mask=3, bs_block=4, bs_row_ptr=rp, bs_col_idx=ci, causal=True,
+                    bias=2, add_bias=_rand((1, 1, N, N), 75)),
     ]
 
 
-@pytest.mark.parametrize("vi", range(6))
+@pytest.mark.parametrize("vi", range(8))
 @pytest.mark.parametrize("rope_on", [False, True])
 def test_backward_finite_differences(orc, vi, rope_on):
     B, Hq, Hkv, N, d, theta, scale = 1, 2, 1, 9, 4, 100.0, 0.7
@@ -312,6 +315,64 @@ def test_backward_vs_torch_autograd(orc):
     assert np.allclose(o, ot.detach().numpy(), atol=1e-12)
     for a, b in ((dq, qt), (dk, kt), (dv, vt)):
         assert np.allclose(a, b.grad.numpy(), atol=1e-11)
+
+
+@pytest.mark.parametrize("rope_on", [False, True])
+@pytest.mark.parametrize("causal", [False, True])
+def test_dbias_finite_differences(orc, rope_on, causal):
+    """dBias (the gradient with respect to an additive bias, §3.1 additive_bias) against central
+    differences of the forward in the bias itself."""
+    B, H, N, d, theta, scale = 1, 2, 7, 4, 100.0, 0.6
+    q, k, v = _rand((B, H, N, d), 60), _rand((B, H, N, d), 61), _rand((B, H, N, d), 62)
+    do = _rand((B, H, N, d), 63)
+    ab = _rand((B, H, N, N), 64)
+    var = orc.Variant(mask=1 if causal else 0, bias=2, add_bias=ab)
+    *_, db = orc.backward(q, k, v, do, scale, theta, rope_on, var, with_dbias=True)
+    h = 1e-6
+    num = np.zeros_like(ab)
+    for i in np.ndindex(ab.shape):
+        ap, am = ab.copy(), ab.copy()
+        ap[i] += h
+        am[i] -= h
+        op, _ = orc.forward(q, k, v, scale, theta, rope_on, orc.Variant(mask=var.mask, bias=2, add_bias=ap))
+        om, _ = orc.forward(q, k, v, scale, theta, rope_on, orc.Variant(mask=var.mask, bias=2, add_bias=am))
+        num[i] = (np.sum(op * do) - np.sum(om * do)) / (2 * h)
+    assert np.allclose(db, num, atol=1e-7, rtol=1e-6)
+
+
+def test_dbias_vs_torch_autograd(orc):
+    """dBias equals the autograd gradient of torch's fp64 SDPA with respect to a float mask."""
+    B, H, N, d = 2, 3, 13, 8
+    q, k, v = _rand((B, H, N, d), 65), _rand((B, H, N, d), 66), _rand((B, H, N, d), 67)
+    do = _rand((B, H, N, d), 68)
+    ab = _rand((B, H, N, N), 69)
+    var = orc.Variant(mask=1, bias=2, add_bias=ab)
+    _, _, dq, dk, dv, db = orc.backward(q, k, v, do, 0.4, 1e4, False, var, with_dbias=True)
+    qt, kt, vt = (torch.tensor(a, requires_grad=True) for a in (q, k, v))
+    bt = torch.tensor(ab, requires_grad=True)
+    am = torch.zeros(N, N, dtype=torch.float64)
+    am[~torch.tensor(_dense_mask(N, 1))] = float("-inf")
+    ot = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=am + bt, scale=0.4)
+    ot.backward(torch.tensor(do))
+    assert np.allclose(db, bt.grad.numpy(), atol=1e-12)
+    for a, t in ((dq, qt), (dk, kt), (dv, vt)):
+        assert np.allclose(a, t.grad.numpy(), atol=1e-11)
+
+
+def test_dbias_rows_sum_to_zero_and_masked_zero(orc):
+    """sum_n dS_mn = sum_n P_mn dP_mn - D_m = 0 (softmax Jacobian rows), and dBias is exactly 0
+    wherever the mask forbids (m, n) (§4.3: masked pairs carry no gradient)."""
+    B, H, N, d = 1, 2, 24, 8
+    rp, ci = inputs.bigbird_csr(6, seed=7, n_random=1)
+    ab = _rand((1, H, N, N), 70)
+    for var in (orc.Variant(mask=2, window=5, causal=True, bias=2, add_bias=ab),
+                orc.Variant(mask=3, bs_block=4, bs_row_ptr=rp, bs_col_idx=ci, bias=2, add_bias=ab)):
+        q, k, v = _rand((B, H, N, d), 71), _rand((B, H, N, d), 72), _rand((B, H, N, d), 73)
+        do = _rand((B, H, N, d), 74)
+        *_, db = orc.backward(q, k, v, do, 0.5, 1e4, True, var, with_dbias=True)
+        assert np.allclose(db.sum(-1), 0.0, atol=1e-12)
+        allow = _dense_mask(N, var.mask, var.causal, var.window, row_ptr=rp, col_idx=ci, blk=4)
+        assert np.all(db[:, :, ~allow] == 0.0)
 
 
 def test_backward_groups_and_rows(orc):
