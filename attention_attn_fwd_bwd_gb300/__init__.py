@@ -56,6 +56,8 @@ class CVariant(ctypes.Structure):
         ("add_bias", ctypes.c_void_p),
         ("add_bias_strides", ctypes.c_int64 * 4),
         ("tile_visits", ctypes.c_void_p),
+        ("dbias", ctypes.c_void_p),
+        ("dbias_strides", ctypes.c_int64 * 4),
     ]
 
 
@@ -142,16 +144,19 @@ class Variant:
     mask: MASK_*; causal: also require n <= m; window: W for MASK_WINDOW; bs_row_ptr /
     bs_col_idx: int32 CSR block layout (block edge bs_block, 64 or 128); bias: BIAS_*;
     alibi_slopes: fp32 [Hq]; add_bias: fp32 or bf16 tensor broadcastable to [B, Hq, N, N];
-    tile_visits: uint8 [B, Hq, ceil(N/128), ceil(N/128)] (debug record of computed tiles).
+    tile_visits: uint8 [B, Hq, ceil(N/128), ceil(N/128)] (debug record of computed tiles);
+    dbias: fp32 [B, Hq, N, N] output of the backward with an additive bias (its gradient before
+    any broadcast is summed out).
     """
 
     def __init__(self, mask=MASK_CAUSAL, causal=False, window=0, bs_block=64, bs_row_ptr=None,
                  bs_col_idx=None, bias=BIAS_NONE, alibi_slopes=None, add_bias=None,
-                 tile_visits=None):
+                 tile_visits=None, dbias=None):
         self.mask, self.causal, self.window, self.bs_block = mask, causal, window, bs_block
         self.bs_row_ptr, self.bs_col_idx = bs_row_ptr, bs_col_idx
         self.bias, self.alibi_slopes, self.add_bias = bias, alibi_slopes, add_bias
         self.tile_visits = tile_visits
+        self.dbias = dbias
 
     def c_struct(self):
         v = CVariant()
@@ -173,6 +178,10 @@ class Variant:
                 v.add_bias_strides[i] = ab.stride(i) if ab.size(i) > 1 else 0
         if self.tile_visits is not None:
             v.tile_visits = self.tile_visits.data_ptr()
+        if self.dbias is not None:
+            v.dbias = self.dbias.data_ptr()
+            for i in range(4):
+                v.dbias_strides[i] = self.dbias.stride(i)
         return v
 
 

@@ -220,7 +220,11 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
     e = cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clear status word");
   }
+#ifdef ATTNFUSE_WAIT_DIAG
+  *code = v;  // diagnostic builds: the raw record of the first timeout
+#else
   *code = v ? ATTNFUSE_ERR_TIMEOUT : ATTNFUSE_OK;
+#endif
   return ok();
 }
 
@@ -415,12 +419,18 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
   if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
   if (rope_mode != ATTNFUSE_ROPE_NONE && (!(rope_theta > 0.f) || !std::isfinite(rope_theta)))
     return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
-  int causal = 1;
-  if (variant) {
-    if (variant->bias != ATTNFUSE_BIAS_NONE ||
-        (variant->mask != ATTNFUSE_MASK_FULL && variant->mask != ATTNFUSE_MASK_CAUSAL))
-      return fail(ATTNFUSE_ERR_UNSUPPORTED, "backward supports FULL or CAUSAL masks without bias");
-    causal = (variant->mask == ATTNFUSE_MASK_CAUSAL || variant->causal) ? 1 : 0;
+  VariantDev var;
+  if ((rc = to_dev_variant(variant, N, Hq, &var))) return rc;
+  var.visits = nullptr;  // the tile-visit record belongs to the forward
+  float* dbias = variant ? variant->dbias : nullptr;
+  if (dbias) {
+    if (var.bias != ATTNFUSE_BIAS_ADDITIVE)
+      return fail(ATTNFUSE_ERR_INVALID_ARG, "dbias needs ATTNFUSE_BIAS_ADDITIVE");
+    const int64_t* ds = variant->dbias_strides;
+    if ((reinterpret_cast<uintptr_t>(dbias) & 3u) || ds[3] != 1 || ds[0] < 0 || ds[1] < 0 ||
+        ds[2] < 0)
+      return fail(ATTNFUSE_ERR_INVALID_ARG,
+                  "dbias must be 4-byte aligned with key stride 1 and non-negative strides");
   }
   size_t need = 0;
   if ((rc = attnfuse_bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, &need))) return rc;
@@ -478,7 +488,14 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
   p.dq = static_cast<__nv_bfloat16*>(dq);
   p.dk = static_cast<__nv_bfloat16*>(dk);
   p.dv = static_cast<__nv_bfloat16*>(dv);
-  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.g = Hq / Hkv; p.causal = causal;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.g = Hq / Hkv;
+  p.var = var;
+  p.dbias = dbias;
+  if (dbias) {
+    for (int i = 0; i < 3; ++i) p.db_s[i] = variant->dbias_strides[i];
+    p.db_vec2 = ((reinterpret_cast<uintptr_t>(dbias) & 7u) == 0 && p.db_s[0] % 2 == 0 &&
+                 p.db_s[1] % 2 == 0 && p.db_s[2] % 2 == 0) ? 1 : 0;
+  }
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.status = st;

@@ -505,17 +505,23 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           for (int c = 0; c < BN; ++c) x[c] = __fmaf_rn(alibi, static_cast<float>(c), x[c] + base);
         } else {
           const int64_t rowoff = b * var.ab_s[0] + head * var.ab_s[1] + (int64_t)m * var.ab_s[2];
+          // Branch-free loads (lanes past the sequence end read element 0 and drop it), so the
+          // warp stays converged for the warp-collective TMEM operations that follow.
+          const int c_end = (m < p.N) ? min(BN, p.N - k0) : 0;
           if (var.add_bias_bf16) {
-            const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(var.add_bias) + rowoff;
+            const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(var.add_bias);
 #pragma unroll
-            for (int c = 0; c < BN; ++c)
-              if (k0 + c < p.N && m < p.N)
-                x[c] += __bfloat162float(ab[(int64_t)(k0 + c) * var.ab_s[3]]) * kLog2e;
+            for (int c = 0; c < BN; ++c) {
+              const float raw = __bfloat162float(ab[c < c_end ? rowoff + (int64_t)(k0 + c) * var.ab_s[3] : 0]);
+              x[c] += (c < c_end ? raw : 0.f) * kLog2e;
+            }
           } else {
-            const float* ab = static_cast<const float*>(var.add_bias) + rowoff;
+            const float* ab = static_cast<const float*>(var.add_bias);
 #pragma unroll
-            for (int c = 0; c < BN; ++c)
-              if (k0 + c < p.N && m < p.N) x[c] += ab[(int64_t)(k0 + c) * var.ab_s[3]] * kLog2e;
+            for (int c = 0; c < BN; ++c) {
+              const float raw = ab[c < c_end ? rowoff + (int64_t)(k0 + c) * var.ab_s[3] : 0];
+              x[c] += (c < c_end ? raw : 0.f) * kLog2e;
+            }
           }
         }
       }

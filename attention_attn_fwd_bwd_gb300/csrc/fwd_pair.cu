@@ -619,16 +619,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
 #pragma unroll
           for (int c = 0; c < 128; ++c) x[c] = __fmaf_rn(alibi, static_cast<float>(c), x[c] + base);
         } else if (act) {
+          // Branch-free loads (lanes past the sequence end read element 0 and drop it), so the
+          // warp stays converged for the warp-collective TMEM operations that follow.
+          const int c_end = (m < N) ? min(kPBN, N - k0) : 0;
           if (vab16) {
-            const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(add_bias) + ab_row;
+            const __nv_bfloat16* ab = static_cast<const __nv_bfloat16*>(add_bias);
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (k0 + c < N && m < N) x[c] += __bfloat162float(ab[(int64_t)(k0 + c) * ab_s3]) * kLog2e;
+            for (int c = 0; c < 128; ++c) {
+              const float raw = __bfloat162float(ab[c < c_end ? ab_row + (int64_t)(k0 + c) * ab_s3 : 0]);
+              x[c] += (c < c_end ? raw : 0.f) * kLog2e;
+            }
           } else {
-            const float* ab = static_cast<const float*>(add_bias) + ab_row;
+            const float* ab = static_cast<const float*>(add_bias);
 #pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (k0 + c < N && m < N) x[c] += ab[(int64_t)(k0 + c) * ab_s3] * kLog2e;
+            for (int c = 0; c < 128; ++c) {
+              const float raw = ab[c < c_end ? ab_row + (int64_t)(k0 + c) * ab_s3 : 0];
+              x[c] += (c < c_end ? raw : 0.f) * kLog2e;
+            }
           }
         }
       }

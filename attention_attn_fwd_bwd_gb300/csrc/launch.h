@@ -54,8 +54,12 @@ struct BwdParams {
   __nv_bfloat16 *dq, *dk, *dv;
   int64_t dq_s[3], dk_s[3], dv_s[3];
   const float2* rope_cs;
-  int B, Hq, Hkv, N, d, g, causal;
+  int B, Hq, Hkv, N, d, g;
   float scale, scale_log2;
+  VariantDev var;                   // mask and bias combinators (var.causal: n <= m)
+  float* dbias;                     // additive bias only: dBias [B, Hq, N, N] fp32, or null
+  int64_t db_s[3];                  // its (b, h, m) element strides; the key stride is 1
+  int db_vec2;                      // 1: pointer and strides allow 8-byte pair stores
   int* status;
 };
 // rope_kind: kRopeNone, kRopeFused (Q / K tiles rotated on chip) or kRopePrerotated (tmQ /

@@ -119,7 +119,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if ((++spins & 255u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
+#ifdef ATTNFUSE_WAIT_DIAG
+        // diagnostic builds: the first timeout records where it happened (CTA, warp,
+        // barrier word, parity) instead of the plain code
+        if (status)
+          atomicCAS(status, 0, (int)(0x40000000u | ((a >> 3) & 0x3fffu) | ((threadIdx.x >> 5) << 14) |
+                                     (parity << 18) | (min(blockIdx.x, 2047u) << 19)));
+#else
         if (status) atomicExch(status, kDevTimeout);
+#endif
         if (abort_flag) *abort_flag = 1;
         return false;
       }

@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--train", action="store_true",
                     help="forward + backward at B=8 Hq=32 Hkv=8 d=128, N=2048 and 4096")
     ap.add_argument("--variants", action="store_true",
-                    help="mask-variant forwards at B=2 H=16 N=4096 d=64 (window, ALiBi, BigBird)")
+                    help="mask-variant forwards and backwards at B=2 H=16 N=4096 d=64 (window, ALiBi, BigBird)")
     ap.add_argument("--decode", action="store_true",
                     help="split-KV decode at the Llama-3-70B head shape (B=1, 8; splits sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -531,17 +531,24 @@ def run_variants_bench(args):
                                 oracle.Variant(mask=3, bs_block=64, bs_row_ptr=rp, bs_col_idx=ci)),
         "causal": (af.Variant(mask=af.MASK_CAUSAL), oracle.Variant(mask=1)),
     }
+    do = inputs.prefill(B, H, H, N, d, seed=3000, with_dout=True)["dout"].to(dev)
     for name, (gvar, ovar) in cases.items():
         ws = torch.empty(af.fwd_workspace_size(B, H, H, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
         out = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
         t, tmin, tp90 = _time_ms(lambda: af.fwd(q, k, v, rope_theta=1e4, variant=gvar, out=out, lse=lse, workspace=ws))
+        # backward of the same variant (paper §4.3: only active tiles), 2.5x the forward's FLOPs
+        wsb = torch.empty(af.bwd_workspace_size(B, H, H, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        tb, _, _ = _time_ms(lambda: af.bwd(q, k, v, out, lse, do, rope_theta=1e4, variant=gvar,
+                                           dq=dq, dk=dk, dv=dv, workspace=wsb))
         pairs = oracle.allowed_pairs(N, ovar)
         fl = 4.0 * d * B * H * pairs
         print(json.dumps({"variant": name, "B": B, "H": H, "N": N, "d": d, "ms": t, "min_ms": tmin,
                           "p90_ms": tp90, "allowed_pairs_per_head": pairs,
                           "algorithmic_tflops": fl / t / 1e9,
                           "frac_of_peak": fl / t / 1e9 / float(peaks["bf16_tflops"]),
+                          "bwd_ms": tb, "bwd_algorithmic_tflops": 2.5 * fl / tb / 1e9,
                           **({"active_blocks": int(len(ci)), "active_fraction": len(ci) / (N // 64) ** 2}
                              if name.startswith("bigbird") else {})}), flush=True)
 

@@ -100,6 +100,13 @@ typedef struct {
   uint8_t* tile_visits;        /* debug, nullable: [B, Hq, ceil(N/128), ceil(N/128)] bytes; the
                                   forward writes 1 for every (q-tile, kv-tile) it computes.
                                   The caller zeroes it first. */
+  float* dbias;                /* backward output, nullable, ATTNFUSE_BIAS_ADDITIVE only: the
+                                  gradient of the loss with respect to bias(b, h, m, n), i.e.
+                                  dS_mn = P_mn (dP_mn - D_m), fp32, one element per (b, h, m, n)
+                                  of [B, Hq, N, N] (no broadcast: sum over the dimensions the
+                                  bias broadcasts to obtain its own gradient). Every element is
+                                  written, 0 where (m, n) is masked. 4-byte aligned. */
+  int64_t dbias_strides[4];    /* element strides of dbias: (b, h, m) any, n == 1 */
 } attnfuse_variant;
 
 /* Last error message of this thread (empty string if none). */
@@ -132,10 +139,13 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
  * Backward (paper §4.4): preprocess D = rowsum(dO * O), a dK/dV kernel and a dQ kernel, no
  * atomics. Gradients are with respect to the un-rotated q and k (the inverse rotation is
  * applied in the epilogues) and dk, dv are summed over each GQA group.
- * out and lse are the forward's outputs. Supported variants: FULL or CAUSAL mask, no bias.
- * ROPE_PREROTATE is computed like ROPE_FUSED (the gradients are the same function). The
- * recomputed scores use bf16-rounded rotated operands; workspace holds the (cos, sin) table
- * (rotating modes) and D.
+ * out and lse are the forward's outputs, computed with the same variant. Every variant of
+ * the forward is supported (paper §4.3: both passes visit only the active tiles): causal,
+ * sliding window, block-sparse (the dK/dV kernel reads the CSR layout transposed), ALiBi and
+ * the additive bias, whose gradient is written to variant->dbias when that is non-NULL.
+ * ROPE_PREROTATE rotates Q and K once into the workspace, ROPE_FUSED on chip; both give
+ * bit-identical gradients. The recomputed scores use bf16-rounded rotated operands; workspace
+ * holds the (cos, sin) table (rotating modes), D and, for ROPE_PREROTATE, Q' and K'.
  * ------------------------------------------------------------------------------------------ */
 attnfuse_status attnfuse_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
                                             attnfuse_rope_mode rope_mode, size_t* bytes);

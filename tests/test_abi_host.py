@@ -103,14 +103,24 @@ def test_decode_and_bwd_validation(lib):
     rc = lib.attnfuse_decode_noalloc(FAKE, q_st, FAKE, c_st, FAKE, c_st, FAKE, o_st, None, 8, 64, 8,
                                      32768, 128, 32767, 0.088, 5e5, 1, 128, None)
     assert rc == WS_SMALL and b"4194304" in lib.attnfuse_last_error()
+    s = STR
+    bwd = lambda v: lib.attnfuse_bwd(FAKE, s, FAKE, s, FAKE, s, FAKE, s, FAKE, FAKE, s, FAKE, s,
+                                     FAKE, s, FAKE, s, 1, 4, 4, 1024, 128, 0.1, 1e4, 1,
+                                     ctypes.byref(v), FAKE, 1 << 30, None)
     v = af.CVariant()
     v.mask = 2
     v.window = 16
-    s = STR
-    rc = lib.attnfuse_bwd(FAKE, s, FAKE, s, FAKE, s, FAKE, s, FAKE, FAKE, s, FAKE, s, FAKE, s,
-                          FAKE, s, 1, 4, 4, 1024, 128, 0.1, 1e4, 1, ctypes.byref(v), FAKE, 1 << 30,
-                          None)
-    assert rc == UNSUPPORTED
+    v.dbias = FAKE
+    v.dbias_strides[:] = [4 * 1024 * 1024, 1024 * 1024, 1024, 1]
+    assert bwd(v) == INVALID  # dbias without an additive bias
+    v.bias = 2
+    v.add_bias = FAKE
+    v.dbias_strides[:] = [4 * 1024 * 1024, 1024 * 1024, -1024, 1]
+    assert bwd(v) == INVALID  # negative dbias stride
+    v.dbias_strides[:] = [4 * 1024 * 1024, 1024 * 1024, 1024, 2]
+    assert bwd(v) == INVALID  # dbias key stride must be 1
+    v.bs_block, v.mask = 96, 3
+    assert bwd(v) == UNSUPPORTED  # block edge
 
 
 def test_version(lib):

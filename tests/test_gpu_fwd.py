@@ -14,7 +14,7 @@ import torch
 
 import attention_attn_fwd_bwd_gb300 as af
 from attention_attn_fwd_bwd_gb300 import inputs
-from tests._helpers import check_lse, check_out, f64
+from tests._helpers import variant_pair as _variants, check_lse, check_out, f64
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
@@ -27,43 +27,6 @@ def _lib():
     _build.build()
     af.load()
     assert af.device_status() == 0
-
-
-def _variants(name, N, Hq, dev, seed=0):
-    """(gpu Variant, oracle Variant) for a named combinator set."""
-    import oracle
-
-    if name == "full":
-        return af.Variant(mask=af.MASK_FULL), oracle.Variant(mask=0)
-    if name == "causal":
-        return af.Variant(mask=af.MASK_CAUSAL), oracle.Variant(mask=1)
-    if name.startswith("window"):
-        W = int(name.split("_")[1])
-        causal = name.endswith("_c")
-        return (af.Variant(mask=af.MASK_WINDOW, window=W, causal=causal),
-                oracle.Variant(mask=2, window=W, causal=causal))
-    if name == "alibi":
-        sl = inputs.alibi_slopes(Hq)
-        return (af.Variant(mask=af.MASK_CAUSAL, bias=af.BIAS_ALIBI,
-                           alibi_slopes=torch.tensor(sl, dtype=torch.float32, device=dev)),
-                oracle.Variant(mask=1, bias=1, slopes=sl.astype(np.float32).astype(np.float64)))
-    if name.startswith("addbias"):
-        g = torch.Generator("cpu").manual_seed(seed + 77)
-        dt = torch.bfloat16 if name.endswith("bf16") else torch.float32
-        shape = (1, Hq, N, N) if "bcast" in name else (2, Hq, N, N)
-        ab = (torch.randn(*shape, generator=g) * 2).to(dt)
-        return (af.Variant(mask=af.MASK_FULL, bias=af.BIAS_ADDITIVE, add_bias=ab.to(dev)),
-                oracle.Variant(mask=0, bias=2, add_bias=f64(ab)))
-    if name.startswith("bs"):
-        blk = int(name.split("_")[1])
-        causal = name.endswith("_c")
-        nb = -(-N // blk)
-        rp, ci = inputs.bigbird_csr(nb, seed=seed + 11, n_random=2)
-        return (af.Variant(mask=af.MASK_BLOCK_SPARSE, bs_block=blk, causal=causal,
-                           bs_row_ptr=torch.tensor(rp, device=dev),
-                           bs_col_idx=torch.tensor(ci, device=dev)),
-                oracle.Variant(mask=3, bs_block=blk, causal=causal, bs_row_ptr=rp, bs_col_idx=ci))
-    raise ValueError(name)
 
 
 def _run(B, Hq, Hkv, N, d, rope_mode, vname, seed, theta=10000.0, rows=None, visits=False):
