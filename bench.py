@@ -365,55 +365,82 @@ def run_ours(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def _median_ms(fn, reps=30, warm=5):
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    samples = []
+    for _ in range(reps):
+        evs[0].record()
+        fn()
+        evs[1].record()
+        torch.cuda.synchronize()
+        samples.append(evs[0].elapsed_time(evs[1]))
+    return statistics.median(samples)
+
+
+def _crossover(res, key):
+    """N where res[key] (t_prerotate / t_fused) crosses 1, log-linear in N; None if it does not."""
+    for a, b in zip(res, res[1:]):
+        ra, rb = a[key] - 1, b[key] - 1
+        if ra >= 0 > rb or ra <= 0 < rb:
+            t = ra / (ra - rb)
+            return math.exp(math.log(a["N"]) + t * (math.log(b["N"]) - math.log(a["N"])))
+    return None
+
+
 def run_sweep(args):
-    """Fused vs pre-rotated vs no RoPE over N at B*N = 16384 tokens (the Rotation Calculus)."""
+    """The Rotation Calculus on GB300: fused vs pre-rotated vs no RoPE over N at B*N = 16384
+    tokens, forward for head dims 128 (Hq=32, Hkv=8) and 64 (H=16), and the d=128 backward."""
     import torch
 
     import attention_attn_fwd_bwd_gb300 as af
     from attention_attn_fwd_bwd_gb300 import inputs
 
     dev = torch.device("cuda")
-    Hq, Hkv, d, theta = 32, 8, 128, 5e5
-    res = []
-    for N in (1024, 2048, 4096, 8192, 16384):
-        B = 16384 // N
-        x = inputs.prefill(B, Hq, Hkv, N, d, seed=N)
-        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
-        out = torch.empty_like(q)
-        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
-        times = {}
-        for name, mode in (("fused", af.ROPE_FUSED), ("prerotate", af.ROPE_PREROTATE),
-                           ("none", af.ROPE_NONE)):
-            ws = torch.empty(max(16, af.fwd_workspace_size(B, Hq, Hkv, N, d, mode)),
-                             dtype=torch.uint8, device=dev)
-            for _ in range(5):
-                af.fwd(q, k, v, rope_theta=theta, rope_mode=mode, out=out, lse=lse, workspace=ws)
-            torch.cuda.synchronize()
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
-            reps = 30
-            samples = []
-            for _ in range(reps):
-                evs[0].record()
-                af.fwd(q, k, v, rope_theta=theta, rope_mode=mode, out=out, lse=lse, workspace=ws)
-                evs[1].record()
-                torch.cuda.synchronize()
-                samples.append(evs[0].elapsed_time(evs[1]))
-            times[name] = statistics.median(samples)
-        fl = causal_flops(B, Hq, N, d)
-        res.append({"N": N, "B": B, **{f"{k}_ms": v for k, v in times.items()},
-                    "fused_over_prerotate": times["prerotate"] / times["fused"],
-                    "fused_tflops": fl / times["fused"] / 1e9,
-                    "none_tflops": fl / times["none"] / 1e9})
-        print(json.dumps({"sweep": "rotation_calculus", **res[-1]}), flush=True)
-    # crossover: where prerotate/fused crosses 1 (log-linear interpolation in N)
-    nstar = None
-    for a, b in zip(res, res[1:]):
-        ra, rb = a["fused_over_prerotate"] - 1, b["fused_over_prerotate"] - 1
-        if ra >= 0 > rb or ra <= 0 < rb:
-            t = ra / (ra - rb)
-            nstar = math.exp(math.log(a["N"]) + t * (math.log(b["N"]) - math.log(a["N"])))
-    print(json.dumps({"sweep": "rotation_calculus_crossover", "N_star": nstar,
-                      "note": "speedup = t_prerotate / t_fused; >1 means fusion wins"}), flush=True)
+    theta = 5e5
+    for d, Hq, Hkv in ((128, 32, 8), (64, 16, 16)):
+        res = []
+        for N in (256, 512, 1024, 2048, 4096, 8192, 16384):
+            B = 16384 // N
+            x = inputs.prefill(B, Hq, Hkv, N, d, seed=N, with_dout=(d == 128 and N <= 4096))
+            q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+            out = torch.empty_like(q)
+            lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+            times = {}
+            for name, mode in (("fused", af.ROPE_FUSED), ("prerotate", af.ROPE_PREROTATE),
+                               ("none", af.ROPE_NONE)):
+                ws = torch.empty(max(16, af.fwd_workspace_size(B, Hq, Hkv, N, d, mode)),
+                                 dtype=torch.uint8, device=dev)
+                times[name] = _median_ms(lambda: af.fwd(q, k, v, rope_theta=theta, rope_mode=mode,
+                                                        out=out, lse=lse, workspace=ws))
+            fl = causal_flops(B, Hq, N, d)
+            row = {"d": d, "N": N, "B": B, **{f"{k}_ms": v for k, v in times.items()},
+                   "fused_over_prerotate": times["prerotate"] / times["fused"],
+                   "fused_tflops": fl / times["fused"] / 1e9,
+                   "none_tflops": fl / times["none"] / 1e9}
+            if "dout" in x:
+                do = x["dout"].to(dev)
+                dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+                bt = {}
+                for name, mode in (("fused", af.ROPE_FUSED), ("prerotate", af.ROPE_PREROTATE)):
+                    af.fwd(q, k, v, rope_theta=theta, rope_mode=mode, out=out, lse=lse)
+                    ws = torch.empty(af.bwd_workspace_size(B, Hq, Hkv, N, d, mode), dtype=torch.uint8, device=dev)
+                    bt[name] = _median_ms(lambda: af.bwd(q, k, v, out, lse, do, rope_theta=theta, rope_mode=mode,
+                                                         dq=dq, dk=dk, dv=dv, workspace=ws), reps=15)
+                row.update({"bwd_fused_ms": bt["fused"], "bwd_prerotate_ms": bt["prerotate"],
+                            "bwd_fused_over_prerotate": bt["prerotate"] / bt["fused"]})
+            res.append(row)
+            print(json.dumps({"sweep": "rotation_calculus", **row}), flush=True)
+        bwd_rows = [r for r in res if "bwd_fused_over_prerotate" in r]
+        print(json.dumps({"sweep": "rotation_calculus_crossover", "d": d,
+                          "N_star_fwd": _crossover(res, "fused_over_prerotate"),
+                          "N_star_bwd": _crossover(bwd_rows, "bwd_fused_over_prerotate") if bwd_rows else None,
+                          "note": "speedup = t_prerotate / t_fused; >1 means fusion wins; "
+                                  "None: no crossing inside the measured N"}), flush=True)
 
 
 def run_profile(args):
