@@ -22,7 +22,7 @@ __all__ = [
     "fwd_workspace_size", "bwd_workspace_size", "decode_workspace_size",
 ]
 
-ROPE_NONE, ROPE_FUSED, ROPE_PREROTATE = 0, 1, 2
+ROPE_NONE, ROPE_FUSED, ROPE_PREROTATE, ROPE_AUTO = 0, 1, 2, 3
 ROPE_REUSE_TABLE = 0x100
 MASK_FULL, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK_SPARSE = 0, 1, 2, 3
 BIAS_NONE, BIAS_ALIBI, BIAS_ADDITIVE = 0, 1, 2
@@ -96,6 +96,7 @@ def load():
             "attnfuse_rope_prerotate": ([P, ST, P, I, I, I, I, F, P, S, P], I),
             "attnfuse_debug_wait_timeout": ([ctypes.c_uint64, P], I),
             "attnfuse_rope_table": ([P, S, I, I, F, P], I),
+            "attnfuse_rope_auto_mode": ([I, I, I, ctypes.POINTER(I)], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -183,6 +184,13 @@ class Variant:
             for i in range(4):
                 v.dbias_strides[i] = self.dbias.stride(i)
         return v
+
+
+def rope_auto_mode(N, d, backward=False):
+    """The mode ROPE_AUTO resolves to (ROPE_FUSED or ROPE_PREROTATE) for N and head dim d."""
+    m = ctypes.c_int()
+    _check(load().attnfuse_rope_auto_mode(N, d, int(bool(backward)), ctypes.byref(m)))
+    return m.value
 
 
 def fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode):

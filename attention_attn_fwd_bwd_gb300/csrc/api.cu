@@ -228,9 +228,34 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
   return ok();
 }
 
+// ATTNFUSE_ROPE_AUTO: the faster of on-chip rotation and pre-rotation, by the crossover
+// N* measured on GB300 (the paper's Rotation Calculus, §5.3; B*N = 16384 tokens, causal).
+// Head dim 64: fusion wins below N* ~ 1.26k (forward; two sweeps gave 1240 and 1285) and
+// ~ 280 (backward, which re-reads each K tile once per query tile). Head dim 128: pre-rotation
+// was faster at every N from 256 to 16384, forward and backward.
+constexpr int kAutoFusedBelowN64Fwd = 1260;
+constexpr int kAutoFusedBelowN64Bwd = 284;
+
+static attnfuse_rope_mode resolve_rope(attnfuse_rope_mode m, int N, int d, bool backward) {
+  if (m != ATTNFUSE_ROPE_AUTO) return m;
+  if (d == 64 && N < (backward ? kAutoFusedBelowN64Bwd : kAutoFusedBelowN64Fwd))
+    return ATTNFUSE_ROPE_FUSED;
+  return ATTNFUSE_ROPE_PREROTATE;
+}
+
+attnfuse_status attnfuse_rope_auto_mode(int N, int d, int backward, attnfuse_rope_mode* mode) {
+  if (!mode) return fail(ATTNFUSE_ERR_INVALID_ARG, "mode is NULL");
+  if (N < 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "N=%d", N);
+  if (d != 64 && d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "head dim %d (need 64 or 128)", d);
+  *mode = resolve_rope(ATTNFUSE_ROPE_AUTO, N, d, backward != 0);
+  return ok();
+}
+
 attnfuse_status attnfuse_fwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
                                             attnfuse_rope_mode rope_mode, size_t* bytes) {
   if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
+  rope_mode = resolve_rope(static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE),
+                           N, d, false);
   attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
   if (rc) return rc;
   size_t n = 0;
@@ -276,7 +301,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
                              const attnfuse_variant* variant, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
   const bool reuse_table = (rope_mode & ATTNFUSE_ROPE_REUSE_TABLE) != 0;
-  rope_mode = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
+  rope_mode = resolve_rope(static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE),
+                           N, d, false);
   attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
   if (rc) return rc;
   if ((rc = check_tensor(q, q_strides, "q"))) return rc;
@@ -374,7 +400,8 @@ attnfuse_status attnfuse_rope_table(void* table, size_t table_bytes, int N, int 
 attnfuse_status attnfuse_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
                                             attnfuse_rope_mode rope_mode, size_t* bytes) {
   if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
-  rope_mode = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
+  rope_mode = resolve_rope(static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE),
+                           N, d, true);
   attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
   if (rc) return rc;
   if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
@@ -404,7 +431,8 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
                              const attnfuse_variant* variant, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream) {
   const bool reuse_table = (rope_mode & ATTNFUSE_ROPE_REUSE_TABLE) != 0;
-  rope_mode = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
+  rope_mode = resolve_rope(static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE),
+                           N, d, true);
   attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
   if (rc) return rc;
   if ((rc = check3(q, q_strides, "q")) || (rc = check3(k, k_strides, "k")) ||
@@ -580,6 +608,7 @@ attnfuse_status attnfuse_decode(const void* q, const int64_t q_strides[3], const
     return fail(ATTNFUSE_ERR_INVALID_ARG, "lse is not 4-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale))
     return fail(ATTNFUSE_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (rope_mode == ATTNFUSE_ROPE_AUTO) rope_mode = ATTNFUSE_ROPE_FUSED;  // only q is rotated
   if (rope_mode != ATTNFUSE_ROPE_NONE && rope_mode != ATTNFUSE_ROPE_FUSED)
     return fail(ATTNFUSE_ERR_UNSUPPORTED, "decode rotates q only: rope_mode NONE or FUSED");
   if (rope_mode == ATTNFUSE_ROPE_FUSED && (!(rope_theta > 0.f) || !std::isfinite(rope_theta)))

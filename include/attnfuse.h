@@ -58,8 +58,12 @@ typedef int attnfuse_status;
 typedef enum {
   ATTNFUSE_ROPE_NONE = 0,      /* no rotation: plain scaled_dot_product */
   ATTNFUSE_ROPE_FUSED = 1,     /* rotate the Q tile once and each K tile in shared memory */
-  ATTNFUSE_ROPE_PREROTATE = 2  /* separate rotate kernel writes Q', K' to the workspace, then
+  ATTNFUSE_ROPE_PREROTATE = 2, /* separate rotate kernel writes Q', K' to the workspace, then
                                   attention runs without rotation (the paper's baseline) */
+  ATTNFUSE_ROPE_AUTO = 3       /* the faster of FUSED and PREROTATE for this call's N, head dim
+                                  and direction, by the crossover N* measured on GB300 (the
+                                  paper's Rotation Calculus, §5.3); see attnfuse_rope_auto_mode.
+                                  The result is identical to the mode chosen. Decode: FUSED. */
 } attnfuse_rope_mode;
 
 /* Flag OR-ed into rope_mode: the workspace already holds the (cos, sin) table, built by an
@@ -220,6 +224,14 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
                                         int B, int H, int N, int d, float rope_theta,
                                         void* workspace, size_t workspace_bytes,
                                         cudaStream_t stream);
+
+/* The mode ATTNFUSE_ROPE_AUTO resolves to for sequence length N and head dim d, for the
+ * forward (backward = 0) or the backward (backward = 1). Measured on GB300 with B*N = 16384
+ * tokens, causal: fusion wins only for head dim 64, below N ~ 1.26k (forward) and N ~ 280
+ * (backward); for head dim 128 the pre-rotation pass is cheaper than rotating each K tile once
+ * per query tile at every N from 256 up. The workspace size functions accept
+ * ATTNFUSE_ROPE_AUTO and size for the resolved mode. */
+attnfuse_status attnfuse_rope_auto_mode(int N, int d, int backward, attnfuse_rope_mode* mode);
 
 /* Build the (cos, sin) table that the rotating modes keep at the start of their workspace:
  * entry (p, i) = (cos, sin)(p * theta_i) for p < N, i < d/2, fp32 pairs, computed in-kernel
