@@ -49,6 +49,8 @@ def parse():
                     help="forward + backward at B=8 Hq=32 Hkv=8 d=128, N=2048 and 4096")
     ap.add_argument("--variants", action="store_true",
                     help="mask-variant forwards and backwards at B=2 H=16 N=4096 d=64 (window, ALiBi, BigBird)")
+    ap.add_argument("--tables", action="store_true",
+                    help="the paper's GPT-2-small forwards and Llama-3-8B / Mistral-7B decodes")
     ap.add_argument("--decode", action="store_true",
                     help="split-KV decode at the Llama-3-70B head shape (B=1, 8; splits sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -532,12 +534,40 @@ def run_train_bench(args):
                           "launches": {"fwd": 2, "bwd": 4, "bwd_prerotate": 6}}), flush=True)
 
 
+def allowed_pairs(N, mask, causal=False, window=0, row_ptr=None, col_idx=None, blk=64):
+    """Allowed (m, n) pairs of one head, counted from the mask definitions (the algorithmic
+    work of a masked forward): mask "full", "causal", "window" (|m - n| < W, n <= m if causal)
+    or "block_sparse" (CSR of active blocks, n <= m if causal)."""
+    import numpy as np
+
+    m = np.arange(N, dtype=np.int64)
+    if mask == "full":
+        return N * N
+    if mask == "causal":
+        return int((m + 1).sum())
+    if mask == "window":
+        lo = np.maximum(0, m - window + 1)
+        hi = m if causal else np.minimum(N - 1, m + window - 1)
+        return int((hi - lo + 1).sum())
+    total = 0
+    nb = -(-N // blk)
+    for br in range(nb):
+        r0, r1 = br * blk, min(N, (br + 1) * blk)
+        for bc in col_idx[row_ptr[br]:row_ptr[br + 1]]:
+            c0, c1 = int(bc) * blk, min(N, (int(bc) + 1) * blk)
+            if causal:
+                rows = np.arange(r0, r1)
+                total += int(np.clip(np.minimum(rows, c1 - 1) - c0 + 1, 0, None).sum())
+            else:
+                total += (r1 - r0) * (c1 - c0)
+    return total
+
+
 def run_variants_bench(args):
     """Mask-variant forwards at B=2, H=16, N=4096, d=64, theta=1e4, fused RoPE."""
     import torch
 
     import attention_attn_fwd_bwd_gb300 as af
-    import oracle
     from attention_attn_fwd_bwd_gb300 import inputs
 
     dev = torch.device("cuda")
@@ -548,18 +578,18 @@ def run_variants_bench(args):
     rp, ci = inputs.bigbird_csr(N // 64, seed=3003)
     cases = {
         "window1024_causal": (af.Variant(mask=af.MASK_WINDOW, window=1024, causal=True),
-                              oracle.Variant(mask=2, window=1024, causal=True)),
+                              allowed_pairs(N, "window", causal=True, window=1024)),
         "alibi_causal": (af.Variant(mask=af.MASK_CAUSAL, bias=af.BIAS_ALIBI,
                                     alibi_slopes=torch.tensor(inputs.alibi_slopes(H), dtype=torch.float32, device=dev)),
-                         oracle.Variant(mask=1)),
+                         allowed_pairs(N, "causal")),
         "bigbird_blocksparse": (af.Variant(mask=af.MASK_BLOCK_SPARSE, bs_block=64,
                                            bs_row_ptr=torch.tensor(rp, device=dev),
                                            bs_col_idx=torch.tensor(ci, device=dev)),
-                                oracle.Variant(mask=3, bs_block=64, bs_row_ptr=rp, bs_col_idx=ci)),
-        "causal": (af.Variant(mask=af.MASK_CAUSAL), oracle.Variant(mask=1)),
+                                allowed_pairs(N, "block_sparse", row_ptr=rp, col_idx=ci)),
+        "causal": (af.Variant(mask=af.MASK_CAUSAL), allowed_pairs(N, "causal")),
     }
     do = inputs.prefill(B, H, H, N, d, seed=3000, with_dout=True)["dout"].to(dev)
-    for name, (gvar, ovar) in cases.items():
+    for name, (gvar, pairs) in cases.items():
         ws = torch.empty(af.fwd_workspace_size(B, H, H, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
         out = torch.empty_like(q)
         lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
@@ -569,7 +599,6 @@ def run_variants_bench(args):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         tb, _, _ = _time_ms(lambda: af.bwd(q, k, v, out, lse, do, rope_theta=1e4, variant=gvar,
                                            dq=dq, dk=dk, dv=dv, workspace=wsb))
-        pairs = oracle.allowed_pairs(N, ovar)
         fl = 4.0 * d * B * H * pairs
         print(json.dumps({"variant": name, "B": B, "H": H, "N": N, "d": d, "ms": t, "min_ms": tmin,
                           "p90_ms": tp90, "allowed_pairs_per_head": pairs,
@@ -578,6 +607,103 @@ def run_variants_bench(args):
                           "bwd_ms": tb, "bwd_algorithmic_tflops": 2.5 * fl / tb / 1e9,
                           **({"active_blocks": int(len(ci)), "active_fraction": len(ci) / (N // 64) ** 2}
                              if name.startswith("bigbird") else {})}), flush=True)
+
+
+def _graph_of(fn):
+    """Capture fn() (library calls on the current stream, buffers preallocated) in a CUDA
+    graph, so small problems are timed without host-side launch latency."""
+    import torch
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def run_tables_bench(args):
+    """The paper's other workloads (§6.1-§6.3) on GB300, each one JSON line:
+    GPT-2-small geometry forwards (B=4, H=12, d=64; N = 512..4096): dense, causal, causal
+    sliding window 256, causal + ALiBi, and RoPE (fused, theta 1e4) + dense / causal /
+    sliding window; decode at the Llama-3-8B (L=4096) and Mistral-7B (L=16384) head shapes
+    (Hq=32, Hkv=8, d=128), B=1 and 8, q at L-1, cold L2."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    dev = torch.device("cuda")
+    peaks, _ = measured_peaks()
+    B, H, d = 4, 12, 64
+    slopes = torch.tensor(inputs.alibi_slopes(H), dtype=torch.float32, device=dev)
+    cells = [("dense", af.ROPE_NONE, dict(mask=af.MASK_FULL), ("full",)),
+             ("causal", af.ROPE_NONE, dict(mask=af.MASK_CAUSAL), ("causal",)),
+             ("sw256", af.ROPE_NONE, dict(mask=af.MASK_WINDOW, window=256, causal=True), ("window", True, 256)),
+             ("causal_alibi", af.ROPE_NONE, dict(mask=af.MASK_CAUSAL, bias=af.BIAS_ALIBI, alibi_slopes=slopes), ("causal",)),
+             ("rope_dense", af.ROPE_FUSED, dict(mask=af.MASK_FULL), ("full",)),
+             ("rope_causal", af.ROPE_FUSED, dict(mask=af.MASK_CAUSAL), ("causal",)),
+             ("rope_sw256", af.ROPE_FUSED, dict(mask=af.MASK_WINDOW, window=256, causal=True), ("window", True, 256))]
+    for N in (512, 1024, 2048, 4096):
+        x = inputs.prefill(B, H, H, N, d, seed=6000 + N)
+        q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+        out = torch.empty_like(q)
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+        for name, mode, vkw, pk in cells:
+            var = af.Variant(**vkw)
+            ws = torch.empty(max(16, af.fwd_workspace_size(B, H, H, N, d, mode)), dtype=torch.uint8, device=dev)
+            call = lambda: af.fwd(q, k, v, rope_theta=1e4, rope_mode=mode, variant=var,
+                                  out=out, lse=lse, workspace=ws)
+            t, tmin, tp90 = _time_ms(call)
+            g = _graph_of(call)
+            tg, _, _ = _time_ms(g.replay)
+            pairs = allowed_pairs(N, pk[0], causal=pk[1] if len(pk) > 1 else False,
+                                  window=pk[2] if len(pk) > 2 else 0)
+            fl = 4.0 * d * B * H * pairs
+            print(json.dumps({"table": "gpt2_small_forward", "variant": name, "B": B, "H": H, "N": N, "d": d,
+                              "ms": t, "min_ms": tmin, "p90_ms": tp90, "algorithmic_tflops": fl / t / 1e9,
+                              "frac_of_peak": fl / t / 1e9 / float(peaks["bf16_tflops"]),
+                              "ms_graph": tg, "algorithmic_tflops_graph": fl / tg / 1e9}), flush=True)
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x the L2
+    Hq, Hkv, d = 32, 8, 128
+    for geom, L in (("llama3_8b", 4096), ("mistral_7b", 16384)):
+        for Bd in (1, 8):
+            x = inputs.decode(Bd, Hq, Hkv, L, d, seed=7000 + L + Bd)
+            q, kc, vc = (x[n].to(dev) for n in ("q", "k_cache", "v_cache"))
+            out = torch.empty_like(q)
+            lse = torch.empty((Bd, Hq), dtype=torch.float32, device=dev)
+            ws = torch.empty(af.decode_workspace_size(Bd, Hq, Hkv, L, d, 0), dtype=torch.uint8, device=dev)
+            call = lambda: af.decode(q, kc, vc, L - 1, rope_theta=5e5, out=out, lse=lse, workspace=ws)
+            for _ in range(3):
+                call()
+            g = _graph_of(call)
+            meds = []
+            for fn in (call, g.replay):
+                samples = []
+                for _ in range(30):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    fn()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    samples.append(e0.elapsed_time(e1) * 1e3)
+                samples.sort()
+                meds.append(samples)
+            samples = meds[0]
+            med, medg = samples[len(samples) // 2], meds[1][len(meds[1]) // 2]
+            nbytes = 2 * Bd * Hkv * L * d * 2
+            print(json.dumps({"table": "decode", "geometry": geom, "B": Bd, "Hq": Hq, "Hkv": Hkv, "d": d,
+                              "L": L, "splits_used": af.decode_auto_splits(Bd, Hkv, L),
+                              "us_median_cold_l2": med, "us_min_cold_l2": samples[0],
+                              "gbs_cold": nbytes / (med * 1e-6) / 1e9,
+                              "frac_of_hbm": nbytes / (med * 1e-6) / 1e9 / float(peaks["hbm_gbs"]),
+                              "us_graph_cold_l2": medg,
+                              "frac_of_hbm_graph": nbytes / (medg * 1e-6) / 1e9 / float(peaks["hbm_gbs"])}), flush=True)
 
 
 def run_decode_bench(args):
@@ -662,6 +788,10 @@ def main():
     if args.variants:
         if rank == 0:
             run_variants_bench(args)
+        return
+    if args.tables:
+        if rank == 0:
+            run_tables_bench(args)
         return
     run_ours(args, rank, world)
     if world > 1:

@@ -52,3 +52,25 @@ def test_reference_arm_json_line():
     assert line["impl"] == "reference" and line["unit"] == "TFLOP/s" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["higher_is_better"] is True
+
+
+def test_bench_pair_counts_match_oracle():
+    """bench.py counts the algorithmic work (allowed pairs) without the oracle; the counts agree
+    with the oracle's brute-force count for every mask kind."""
+    import bench
+    import oracle
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    for N in (1, 100, 517, 1024):
+        assert bench.allowed_pairs(N, "full") == oracle.allowed_pairs(N, oracle.Variant(mask=0))
+        assert bench.allowed_pairs(N, "causal") == oracle.allowed_pairs(N, oracle.Variant(mask=1))
+        for W in (1, 7, 300):
+            for c in (False, True):
+                assert bench.allowed_pairs(N, "window", causal=c, window=W) == oracle.allowed_pairs(
+                    N, oracle.Variant(mask=2, window=W, causal=c))
+        for blk in (64, 128):
+            rp, ci = inputs.bigbird_csr(-(-N // blk), seed=3, n_random=2)
+            for c in (False, True):
+                assert bench.allowed_pairs(N, "block_sparse", causal=c, row_ptr=rp, col_idx=ci,
+                                           blk=blk) == oracle.allowed_pairs(
+                    N, oracle.Variant(mask=3, bs_block=blk, bs_row_ptr=rp, bs_col_idx=ci, causal=c))
