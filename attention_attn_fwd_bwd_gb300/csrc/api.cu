@@ -345,7 +345,7 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
     void* qr = base;
     void* kr = base + align_up((size_t)B * Hq * N * d * 2, 256);
-    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, 0, stream);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, -1, stream);
     if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, 1, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
     qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;

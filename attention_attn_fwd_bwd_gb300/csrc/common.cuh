@@ -151,6 +151,21 @@ __device__ __forceinline__ void key_cs8(const float2* __restrict__ cs, int n, in
   for (int k = 0; k < r / RG; ++k) advance_cs8(c, s, wc, ws);
 }
 
+// Query rows of a 128-row tile are rotated with a recurrence too: row r of the tile at n0
+// (n0 a multiple of 128) starts from the table entry of position n0 + (r % 8) and advances
+// r / 8 times by the entry of position 8, so a tile needs 9 table rows instead of 128.
+// query_cs8 evaluates that sequence for chunk `chunk` (8 pairs) of row n; the forward kernels
+// run the same per-pair steps while rotating their Q tiles.
+template <int D>
+__device__ __forceinline__ void query_cs8(const float2* __restrict__ cs, int n, int chunk,
+                                          float (&c)[8], float (&s)[8]) {
+  const int n0 = n & ~127, r = n & 127;
+  load_cs8(cs + (size_t)(n0 + (r & 7)) * (D / 2) + chunk * 8, c, s);
+  float wc[8], ws[8];
+  load_cs8(cs + (size_t)8 * (D / 2) + chunk * 8, wc, ws);
+  for (int k = 0; k < (r >> 3); ++k) advance_cs8(c, s, wc, ws);
+}
+
 // Variant descriptor as seen by the kernels (host fills it from attnfuse_variant).
 struct VariantDev {
   int mask;    // 0 full, 1 causal, 2 window, 3 block-sparse

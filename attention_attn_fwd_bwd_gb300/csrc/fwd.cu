@@ -445,25 +445,47 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     const uint32_t tO = tmem + lane_off + 256 + s * D;
     bool ok = true;
     if (valid) {
+      // Rotate this sub-tile's Q in place, with coalesced table reads: a warp instruction
+      // covers whole table rows (lane f holds entries 2f, 2f+1 of its row, i.e. dims 2f, 2f+1
+      // and their partners d/2+2f, d/2+2f+1). The reads are issued before Q lands. Same
+      // arithmetic per element as a row-per-thread rotation; rows past N are not rotated.
+      constexpr int F4 = D / 4;           // float4 table entries per row
+      constexpr int RPI = 32 / F4;        // rows per warp instruction
+      constexpr int RPT = BM / (4 * RPI); // rows per thread: rows RPI wq + rsub + 8 k
+      static_assert(4 * RPI == 8, "rows of a thread are 8 positions apart");
+      const int f = lane % F4, rsub = lane / F4;
+      // the query-tile recurrence (query_cs8): start at position q0 + (row % 8), step 8
+      float4 cs = make_float4(0.f, 0.f, 0.f, 0.f), wstep = cs;
+      if (ROPE) {
+        const uint64_t pol_tab = l2_policy_evict_last();  // the table stays in L2
+        const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
+        cs = ldg_f4_hint(tab + (size_t)min(q0 + RPI * wq + rsub, p.N - 1) * F4 + f, pol_tab);
+        wstep = ldg_f4_hint(tab + (size_t)8 * F4 + f, pol_tab);
+      }
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full[s], 0, status, abort_flag));
-      if (ok && ROPE && m < p.N) {
+      if (ok && ROPE) {
         uint8_t* tile = smem + C::OFF_Q + s * C::TILE;
-        constexpr int CP = D / 16;
+        const uint32_t within = static_cast<uint32_t>(f & 3) * 4u;
 #pragma unroll
-        for (int c = 0; c < CP; ++c) {
-          uint32_t offl, offh;
-          if (D == 128) {
-            offl = sw128_offset(r, c);
-            offh = offl + BM * 128;
-          } else {
-            offl = sw128_offset(r, c);
-            offh = sw128_offset(r, c + 4);
+        for (int k = 0; k < RPT; ++k) {
+          const int rr = RPI * wq + rsub + 4 * RPI * k;
+          if (q0 + rr < p.N) {
+            const uint32_t offl = sw128_offset(rr, f >> 2) + within;
+            const uint32_t offh = (D == 128) ? offl + BM * 128 : sw128_offset(rr, (f >> 2) + 4) + within;
+            const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + offl);
+            const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + offh);
+            float yl0, yh0, yl1, yh1;
+            rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
+            rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
+            *reinterpret_cast<uint32_t*>(tile + offl) = pack_f16x2_sat(yl0, yl1);
+            *reinterpret_cast<uint32_t*>(tile + offh) = pack_f16x2_sat(yh0, yh1);
           }
-          uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
-          uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
-          rot_chunk<true>(lo, hi, p.rope_cs + (size_t)m * (D / 2) + c * 8);
-          *reinterpret_cast<uint4*>(tile + offl) = lo;
-          *reinterpret_cast<uint4*>(tile + offh) = hi;
+          if (k + 1 < RPT) {  // next row of this thread: 8 positions on (advance_cs8 order)
+            float c0, s0, c1, s1;
+            rot_pair(cs.x, cs.y, wstep.x, wstep.y, c0, s0);
+            rot_pair(cs.z, cs.w, wstep.z, wstep.w, c1, s1);
+            cs = make_float4(c0, s0, c1, s1);
+          }
         }
         fence_proxy_async_smem();
       }
@@ -676,12 +698,13 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int N, int half, Rope
 // Pre-rotation (paper Fig. 1a): out[b,h,n,:] = R_n x[b,h,n,:], out contiguous. One thread per
 // (row, chunk pair); HBM-bound elementwise pass.
 // ---------------------------------------------------------------------------------------------
-template <bool OUT_F16, int KEY_D, int BLK>
+template <bool OUT_F16, int KEY_D, int BLK, bool QUERY = false>
 __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb, int64_t sh,
                                  int64_t sn, __nv_bfloat16* __restrict__ out, int H, int N, int d,
                                  const float2* __restrict__ cs, int64_t rows) {
   // KEY_D != 0: the (cos, sin) follow a kernel's in-block recurrence (key_cs8 with blocks of
-  // BLK rows) so that on-chip and pre-rotated operands are bit-identical. KEY_D == 0: table.
+  // BLK rows, or query_cs8 for the forward's query tiles) so that on-chip and pre-rotated
+  // operands are bit-identical. KEY_D == 0: table.
   const int cp = d / 16;
   const int64_t total = rows * cp;
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
@@ -696,7 +719,8 @@ __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb
     uint4 lo = *reinterpret_cast<const uint4*>(src + c * 8);
     uint4 hi = *reinterpret_cast<const uint4*>(src + d / 2 + c * 8);
     float cc[8], ss[8];
-    if (KEY_D != 0) key_cs8<KEY_D == 0 ? 64 : KEY_D, BLK>(cs, n, c, cc, ss);
+    if (KEY_D != 0 && QUERY) query_cs8<KEY_D == 0 ? 64 : KEY_D>(cs, n, c, cc, ss);
+    else if (KEY_D != 0) key_cs8<KEY_D == 0 ? 64 : KEY_D, BLK>(cs, n, c, cc, ss);
     else load_cs8(cs + (size_t)n * (d / 2) + c * 8, cc, ss);
     rot_chunk_cs<OUT_F16>(lo, hi, cc, ss);
     __nv_bfloat16* dst = out + row * d;
@@ -742,6 +766,8 @@ cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, i
              const float2*, int64_t) = nullptr;
   if (block == 0)
     fn = out_f16 ? prerotate_kernel<true, 0, 128> : prerotate_kernel<false, 0, 128>;
+  else if (block < 0)  // forward queries: the 128-row query-tile recurrence
+    fn = d == 128 ? prerotate_kernel<true, 128, 128, true> : prerotate_kernel<true, 64, 128, true>;
   else if (out_f16)  // forward keys: blocks of 64 (head dim 128) or 128 (head dim 64)
     fn = d == 128 ? prerotate_kernel<true, 128, 64> : prerotate_kernel<true, 64, 128>;
   else               // backward operands: blocks of 128

@@ -280,6 +280,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       tma_prefetch_desc(&p.tmV);
       const uint64_t pol_stream = l2_policy_evict_first();
       const uint64_t pol_keep = l2_policy_evict_last();
+      // (cos, sin) rows this CTA reads soon: the 8 its Q rotation starts from, then per K tile
+      // the 16 rows its rotators start from; pulled into L2 ahead of the reads.
+      auto prefetch_rows = [&](int row0, int rows) {
+        rows = min(rows, p.N - row0);
+        if (ROPE && rows > 0)
+          prefetch_l2_bulk(p.rope_cs + (size_t)row0 * (kPD / 2), static_cast<uint32_t>(rows) * (kPD / 2) * 8u);
+      };
+      if (ctl->valid[rank]) prefetch_rows(ctl->q0[rank], 8);
       if (ctl->valid[rank]) {
         mbar_arrive_expect_tx(&ctl->q_full, kQTile);
         for (int pn = 0; pn < 2; ++pn)
@@ -299,6 +307,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
           const int s = ik % kPKSt;
           if (ik < kPKSt || mbar_test(&ctl->k_empty[s], ((ik / kPKSt) - 1) & 1)) {
             AF_PTRACE(ik, 0);
+            prefetch_rows(jk * kPBN + rank * 64, 16);
             mbar_arrive_expect_tx(&ctl->k_full[s], kKHalf);
             for (int pn = 0; pn < 2; ++pn)
               tma_load_4d_hint(smem + kOffK + s * kKHalf + pn * (64 * 128), &p.tmK,
@@ -348,6 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       int n = 0;
       for (int j = jb; j < je; j = tile_next(T, j)) ++n;
       bool ok = mbar_wait_cluster(&ctl->q_ready, 0, status, abort_flag);
+      if (warp == 1) AF_PTRACE(0, 24);
       if (warp == 1) {
         constexpr uint32_t idesc_s = idesc_f32acc(256, kPBN, 0, 0, RK != kRopeNone);
         const uint32_t sK = smem_u32(smem + kOffK);
@@ -437,11 +447,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       // The first row's (cos, sin) of the next tile is read one tile ahead, from a clamped
       // (always valid) table row so the load never blocks; rows past N are not rotated.
       float4 pre[4];
+      const uint64_t pol_tab = l2_policy_evict_last();  // the table stays in L2
       auto fetch = [&](int jj) {
         const int pos = min(jj * kPBN + rank * 64 + rg, kN - 1);
         const float4* src = reinterpret_cast<const float4*>(cs_tab + (size_t)pos * (kPD / 2) + c * 8);
 #pragma unroll
-        for (int w = 0; w < 4; ++w) pre[w] = __ldg(src + w);
+        for (int w = 0; w < 4; ++w) pre[w] = ldg_f4_hint(src + w, pol_tab);
       };
       fetch(jb);
       int i = 0;
@@ -506,6 +517,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
     setmaxnreg_inc<kRegsSm>();
     const int h = (warp - 4) >> 2;           // key columns 64h .. 64h+63 of each tile
     const int wq = warp & 3;                 // TMEM lane quarter
+    if (lane == 0 && wq == 0) AF_PTRACE(h, 26);
     const int r = wq * 32 + lane;            // row within this CTA's 128 rows
     const int s = rank;
     const int q0 = ctl->q0[s];
@@ -544,15 +556,57 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
       uint32_t qlo[16], qhi[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) qlo[e] = qhi[e] = 0u;
-      if (valid) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full, 0, status, abort_flag));
+      if (ROPE) {
+        // Rotate the Q tile in place first, one row per warp instruction: softmax warp w takes
+        // rows w, w + 8, ..., and lane f the table entries 2f, 2f+1 of the row (one coalesced
+        // 16-byte read) and dims 2f, 2f+1 with their partners 64+2f, 64+2f+1. The table reads
+        // are issued before Q lands. Same arithmetic per element as a row-per-thread rotation.
+        const int sw = warp - 4;
+        const uint64_t pol_tab = l2_policy_evict_last();  // the table stays in L2
+        // the query-tile recurrence (query_cs8): start at position q0 + sw, step 8 positions
+        const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
+        float4 cs = ldg_f4_hint(tab + (size_t)min(q0 + sw, N - 1) * (kPD / 4) + lane, pol_tab);
+        const float4 wstep = ldg_f4_hint(tab + (size_t)8 * (kPD / 4) + lane, pol_tab);
+        if (lane == 0 && wq == 0) AF_PTRACE(h, 25);
+        if (valid) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full, 0, status, abort_flag));
+        if (lane == 0 && wq == 0) AF_PTRACE(h, 21);
+        if (valid && ok) {
+          uint8_t* tile = smem + kOffQ;
+          const uint32_t within = static_cast<uint32_t>(lane & 3) * 4u;
+#pragma unroll
+          for (int k = 0; k < kPBM / 8; ++k) {
+            const int rr = sw + 8 * k;
+            if (q0 + rr < N) {
+              const uint32_t off = sw128_offset(rr, lane >> 2) + within;
+              const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + off);
+              const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + kPBM * 128 + off);
+              float yl0, yh0, yl1, yh1;
+              rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
+              rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
+              *reinterpret_cast<uint32_t*>(tile + off) = pack_f16x2_sat(yl0, yl1);
+              *reinterpret_cast<uint32_t*>(tile + kPBM * 128 + off) = pack_f16x2_sat(yh0, yh1);
+            }
+            if (k + 1 < kPBM / 8) {  // next row of this warp: 8 positions on (advance_cs8 order)
+              float c0, s0, c1, s1;
+              rot_pair(cs.x, cs.y, wstep.x, wstep.y, c0, s0);
+              rot_pair(cs.z, cs.w, wstep.z, wstep.w, c1, s1);
+              cs = make_float4(c0, s0, c1, s1);
+            }
+          }
+        }
+        if (lane == 0 && wq == 0) AF_PTRACE(h, 23);
+        named_bar_sync(1, 256);  // the eight softmax warps: rows rotated by other warps
+        if (lane == 0 && wq == 0) AF_PTRACE(h, 27);
+      } else {
+        if (valid) ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full, 0, status, abort_flag));
+      }
       if (valid && ok) {
         const uint8_t* tile = smem + kOffQ;
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int c = 4 * h + cc;
-          uint4 lo = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c));
-          uint4 hi = *reinterpret_cast<const uint4*>(tile + kPBM * 128 + sw128_offset(r, c));
-          if (ROPE && m < N) rot_chunk<true>(lo, hi, p.rope_cs + (size_t)m * (kPD / 2) + c * 8);
+          const uint4 lo = *reinterpret_cast<const uint4*>(tile + sw128_offset(r, c));
+          const uint4 hi = *reinterpret_cast<const uint4*>(tile + kPBM * 128 + sw128_offset(r, c));
           qlo[4 * cc + 0] = lo.x; qlo[4 * cc + 1] = lo.y; qlo[4 * cc + 2] = lo.z; qlo[4 * cc + 3] = lo.w;
           qhi[4 * cc + 0] = hi.x; qhi[4 * cc + 1] = hi.y; qhi[4 * cc + 2] = hi.z; qhi[4 * cc + 3] = hi.w;
         }
@@ -563,6 +617,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPThreads, 1)
         tmem_wait_st();
         tc_fence_before();
         __syncwarp();
+        if (lane == 0 && wq == 0) AF_PTRACE(h, 22);
         if (lane == 0) arrive_leader(&ctl->q_ready, rank);
       }
     }

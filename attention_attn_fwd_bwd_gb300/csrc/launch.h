@@ -81,9 +81,10 @@ size_t fwd_pair_smem_size();
 cudaError_t launch_fwd_pair(const FwdParams& p, int rope_kind, int clusters, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
                               cudaStream_t stream);
-// block: 0 = rotate with the table entry of each row; otherwise the in-block recurrence of the
-// kernels (forward keys: fp16 output, blocks of 64 / 128 for head dim 128 / 64; backward Q and
-// K: bf16 output, blocks of 128).
+// block: 0 = rotate with the table entry of each row; -1 = the forward kernels' query-tile
+// recurrence (fp16 output); otherwise the in-block key recurrence of the kernels (forward keys:
+// fp16 output, blocks of 64 / 128 for head dim 128 / 64; backward Q and K: bf16 output, blocks
+// of 128).
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
                              int N, int d, const float2* cs, bool out_f16, int block,
                              cudaStream_t stream);

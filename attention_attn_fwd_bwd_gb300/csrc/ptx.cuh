@@ -242,11 +242,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // Re-balance registers between warpgroups (all warps of a warpgroup execute the same value).
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N) : "memory");
 }
+// The memory clobber keeps loads of the following role code below the register release: a
+// load hoisted above it would hold the release (and every warp waiting to grow) until it returns.
 template <uint32_t N>
 __device__ __forceinline__ void setmaxnreg_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N) : "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
@@ -280,6 +282,22 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+
+// Start pulling `bytes` (a multiple of 16, 16-byte aligned address) of global memory into L2
+// without waiting for it (bulk copy engine; no completion to track).
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+// Read-only 16-byte load with an L2 eviction-priority hint (for small tables that many CTAs
+// re-read while large operands stream through L2).
+__device__ __forceinline__ float4 ldg_f4_hint(const float4* ptr, uint64_t pol) {
+  float4 v;
+  asm volatile("ld.global.nc.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
 }
 
 __device__ __forceinline__ void tma_load_4d_hint(void* dst, const void* tmap, uint64_t* bar,
