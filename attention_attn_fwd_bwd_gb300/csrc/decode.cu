@@ -26,6 +26,22 @@
 
 namespace afx {
 
+// Optional pipeline tracing (compile with -DATTNFUSE_TRACE_DEC=<split>; off by default): the CTA
+// (split, kv head 0, batch 0) records clock64() at pipeline events of its first 32 tiles; row 32
+// holds the start, q-ready and end events.
+#ifdef ATTNFUSE_TRACE_DEC
+__device__ unsigned long long g_dec_trace[33 * 8];
+#define AF_DTRACE(i, e)                                                                        \
+  do {                                                                                         \
+    if (blockIdx.x == (ATTNFUSE_TRACE_DEC) && blockIdx.y == 0 && blockIdx.z == 0 && (i) <= 32) \
+      g_dec_trace[(i) * 8 + (e)] = clock64();                                                  \
+  } while (0)
+#else
+#define AF_DTRACE(i, e) \
+  do {                  \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kDecThreads = 128;
@@ -48,6 +64,7 @@ struct DecCtl {
   uint64_t k_full[kDecST], k_empty[kDecST], v_full[kDecST], v_empty[kDecST];
   uint32_t tmem_base;
   int abort_flag;
+  float2 qcs[64];  // (cos, sin) of q_pos per pair: every query head sits at the same position
 };
 
 __host__ __device__ constexpr size_t dec_smem_bytes(int D) {
@@ -91,30 +108,51 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   // zero the query tile (rows >= g stay zero)
   for (int i = tid; i < (int)(C::TILE / 16); i += kDecThreads)
     reinterpret_cast<uint4*>(smem + C::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+  if (tid == 0) AF_DTRACE(32, 0);
   if (warp == 2) tmem_alloc(&ctl->tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  if (tid == 0) AF_DTRACE(32, 1);
 
   if (warp == 3) {
     // ---- query tile: row h = R_{q_pos} q[b, kvh*g + h], bf16, 128B-swizzled ----
+    // Every chunk of the row is loaded (read-only path) first, so the global-load latency is
+    // paid once and overlaps the angle computation, not once per chunk behind a store.
+    constexpr int CP = D / 16;
     const int h = lane;
+    uint4 lo[CP], hi[CP];
     if (h < p.g) {
       const __nv_bfloat16* qrow = p.q + b * p.q_sb + (int64_t)(kvh * p.g + h) * p.q_sh;
-      uint8_t* tile = smem + C::OFF_Q;
-      constexpr int CP = D / 16;
 #pragma unroll
       for (int c = 0; c < CP; ++c) {
-        uint4 lo = *reinterpret_cast<const uint4*>(qrow + c * 8);
-        uint4 hi = *reinterpret_cast<const uint4*>(qrow + D / 2 + c * 8);
+        lo[c] = __ldg(reinterpret_cast<const uint4*>(qrow + c * 8));
+        hi[c] = __ldg(reinterpret_cast<const uint4*>(qrow + D / 2 + c * 8));
+      }
+    }
+    if (ROPE_Q) {
+      // the D/2 angles of q_pos, computed once by the whole warp
+      for (int e = lane; e < D / 2; e += 32) {
+        float c, sn;
+        rope_cossin(static_cast<float>(p.q_pos), p.freqs.hi[e], p.freqs.lo[e], &c, &sn);
+        ctl->qcs[e] = make_float2(c, sn);
+      }
+      __syncwarp();
+    }
+    if (h < p.g) {
+      uint8_t* tile = smem + C::OFF_Q;
+#pragma unroll
+      for (int c = 0; c < CP; ++c) {
         if (ROPE_Q) {
           float cc[8], ss[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            rope_cossin(static_cast<float>(p.q_pos), p.freqs.hi[c * 8 + e], p.freqs.lo[c * 8 + e],
-                        &cc[e], &ss[e]);
-          rot_chunk_cs<false>(lo, hi, cc, ss);
+          for (int e = 0; e < 8; ++e) {
+            const float2 t = ctl->qcs[c * 8 + e];
+            cc[e] = t.x;
+            ss[e] = t.y;
+          }
+          rot_chunk_cs<false>(lo[c], hi[c], cc, ss);
         }
         uint32_t offl, offh;
         if (D == 128) {
@@ -124,11 +162,12 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
           offl = sw128_offset(h, c);
           offh = sw128_offset(h, c + 4);
         }
-        *reinterpret_cast<uint4*>(tile + offl) = lo;
-        *reinterpret_cast<uint4*>(tile + offh) = hi;
+        *reinterpret_cast<uint4*>(tile + offl) = lo[c];
+        *reinterpret_cast<uint4*>(tile + offh) = hi[c];
       }
     }
     fence_proxy_async_smem();
+    if (lane == 0) AF_DTRACE(32, 2);
     mbar_arrive(&ctl->q_ready);
   } else if (warp == 1) {
     // ---- TMA producer: K then V of every tile of the chunk, through kDecST-deep rings ----
@@ -142,6 +181,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         const int st = i % kDecST;
         const uint32_t ph = ((i / kDecST) - 1) & 1;
         if (i >= kDecST && !mbar_wait(&ctl->k_empty[st], ph, status, abort_flag)) break;
+        AF_DTRACE(i, 0);
         mbar_arrive_expect_tx(&ctl->k_full[st], C::TILE);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d_hint(smem + C::OFF_K + st * C::TILE + pn * (kDecBN * 128), &p.tmK,
@@ -173,6 +213,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       auto issue_s = [&](int i) {
         const int st = i % kDecST;
         const uint32_t d_tmem = tmem + (i & 1) * 128;
+        AF_DTRACE(i, 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
@@ -195,6 +236,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         const int st = i % kDecST;
         if (!mbar_wait(&ctl->p_full, i & 1, status, abort_flag)) break;
         if (!mbar_wait(&ctl->v_full[st], (i / kDecST) & 1, status, abort_flag)) break;
+        AF_DTRACE(i, 2);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kDecBN / 16; ++kk)
@@ -227,6 +269,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         ok = false;
         break;
       }
+      if (lane == 0) AF_DTRACE(i, 3);
       tc_fence_after();
       uint32_t xr[kDecBN];
       tmem_ld32<0>(tS, xr);
@@ -298,6 +341,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       l_run += f2_lo(acc) + f2_hi(acc);
       m_run = m_use;
       tc_fence_before();
+      if (lane == 0) AF_DTRACE(i, 4);
       mbar_arrive(&ctl->p_full);
     }
     if (ok && ntiles > 0) {
@@ -328,6 +372,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       p.part_m[part] = (ok && l_run > 0.f) ? m_run : kNegInf;
       p.part_l[part] = ok ? l_run : 0.f;
     }
+    if (lane == 0) AF_DTRACE(32, 3);
   }
   // Let the combine kernel launch while this grid drains (its reads wait for our completion).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -459,3 +504,10 @@ extern "C" attnfuse_status attnfuse_decode_noalloc(
                          B, Hq, Hkv, L, d, q_pos, scale, rope_theta, rope_mode, num_splits,
                          scratch, afx::kNoAllocScratchBytes, stream);
 }
+
+#ifdef ATTNFUSE_TRACE_DEC
+// Copy the decode pipeline trace (33 rows x 8 events of clock64) to host memory.
+extern "C" int attnfuse_dec_trace_read(unsigned long long* dst) {
+  return (int)cudaMemcpyFromSymbol(dst, afx::g_dec_trace, sizeof(unsigned long long) * 33 * 8);
+}
+#endif
