@@ -38,6 +38,20 @@
 
 namespace afx {
 
+// Optional pipeline tracing of the dQ kernel (compile with -DATTNFUSE_TRACE_DQ=<block>; off by
+// default): that CTA records clock64() at pipeline events of its first 64 key tiles.
+#ifdef ATTNFUSE_TRACE_DQ
+static __device__ unsigned long long g_dq_trace[65 * 8];
+#define AF_QTRACE(i, e)                                                                   \
+  do {                                                                                    \
+    if (blockIdx.x == (ATTNFUSE_TRACE_DQ) && (i) <= 64) g_dq_trace[(i) * 8 + (e)] = clock64(); \
+  } while (0)
+#else
+#define AF_QTRACE(i, e) \
+  do {                  \
+  } while (0)
+#endif
+
 namespace {
 
 constexpr int kBwdThreads = 384;
@@ -154,17 +168,19 @@ template <int D>
 struct DqCfg {
   static constexpr int PANELS = D / 64;
   static constexpr uint32_t TILE = kT * D * 2;
-  static constexpr int ST = 2;  // K/V stages
+  // K stages are released by dQ (the last MMA to read K), V stages by dP, which completes a
+  // whole group earlier: three K stages and two V stages fill shared memory for head dim 128.
+  static constexpr int KST = 3, VST = 2;
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_DO = TILE;
   static constexpr uint32_t OFF_K = 2 * TILE;
-  static constexpr uint32_t OFF_V = OFF_K + ST * TILE;
-  static constexpr uint32_t OFF_CTL = OFF_V + ST * TILE;
+  static constexpr uint32_t OFF_V = OFF_K + KST * TILE;
+  static constexpr uint32_t OFF_CTL = OFF_V + VST * TILE;
 };
 
 struct DqCtl {
   uint64_t q_full, do_full, q_ready;
-  uint64_t k_full[2], v_full[2], k_ready[2], kv_free[2];
+  uint64_t k_full[3], k_ready[3], k_free[3], v_full[2], v_free[2];
   uint64_t s_full, s_free, p_full[2], dq_done[2], mma_final;
   uint32_t tmem_base;
   int abort_flag;
@@ -184,8 +200,9 @@ __host__ __device__ constexpr size_t kv_smem_bytes(int D) {
 static_assert(1024 + 2 * 32768 + 8 * 16384 + 4 * 512 + sizeof(KvCtl) <= 232448,
               "dK/dV shared memory budget (head dim 128)");
 __host__ __device__ constexpr size_t dq_smem_bytes(int D) {
-  return 1024 + (2 + 2 * 2) * (size_t)(kT * D * 2) + sizeof(DqCtl);
+  return 1024 + (2 + 3 + 2) * (size_t)(kT * D * 2) + sizeof(DqCtl);
 }
+static_assert(1024 + 7 * 32768 + sizeof(DqCtl) <= 232448, "dQ shared memory budget (head dim 128)");
 
 __device__ __forceinline__ bool bit_get(const uint32_t* w, int i) {
   return (w[i >> 5] >> (i & 31)) & 1u;
@@ -618,11 +635,14 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
     mbar_init(&ctl->q_full, 1);
     mbar_init(&ctl->do_full, 1);
     mbar_init(&ctl->q_ready, 128);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&ctl->k_full[s], 1);
-      mbar_init(&ctl->v_full[s], 1);
       mbar_init(&ctl->k_ready[s], 128);
-      mbar_init(&ctl->kv_free[s], 1);
+      mbar_init(&ctl->k_free[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&ctl->v_full[s], 1);
+      mbar_init(&ctl->v_free[s], 1);
       mbar_init(&ctl->dq_done[s], 1);
     }
     mbar_init(&ctl->s_full, 1);
@@ -682,72 +702,108 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       mbar_arrive_expect_tx(&ctl->do_full, C::TILE);
       for (int pn = 0; pn < C::PANELS; ++pn)
         tma_load_4d(smem + C::OFF_DO + pn * (kT * 128), &p.tmDO, &ctl->do_full, pn * 64, i * kT, h, b);
-      int it = 0;
+      int it = 0, iv = 0;
       for (int jt = next_k(k_lo); jt < k_hi; jt = next_k(jt + 1), ++it) {
-        const int s = it & 1;
-        if (it >= 2 && !mbar_wait(&ctl->kv_free[s], ((it >> 1) - 1) & 1, status, abort_flag)) break;
-        mbar_arrive_expect_tx(&ctl->k_full[s], C::TILE);
+        const int sk = it % C::KST, sv = it % C::VST;
+        if (it >= C::KST && !mbar_wait(&ctl->k_free[sk], ((it / C::KST) - 1) & 1, status, abort_flag)) break;
+        AF_QTRACE(it, 6);
+        mbar_arrive_expect_tx(&ctl->k_full[sk], C::TILE);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_K + s * C::TILE + pn * (kT * 128), &p.tmK, &ctl->k_full[s],
+          tma_load_4d(smem + C::OFF_K + sk * C::TILE + pn * (kT * 128), &p.tmK, &ctl->k_full[sk],
                       pn * 64, jt * kT, kvh, b);
-        mbar_arrive_expect_tx(&ctl->v_full[s], C::TILE);
+        if (it >= C::VST && !mbar_wait(&ctl->v_free[sv], ((it / C::VST) - 1) & 1, status, abort_flag)) {
+          ++it;  // K(it) is in flight
+          break;
+        }
+        mbar_arrive_expect_tx(&ctl->v_full[sv], C::TILE);
         for (int pn = 0; pn < C::PANELS; ++pn)
-          tma_load_4d(smem + C::OFF_V + s * C::TILE + pn * (kT * 128), &p.tmV, &ctl->v_full[s],
+          tma_load_4d(smem + C::OFF_V + sv * C::TILE + pn * (kT * 128), &p.tmV, &ctl->v_full[sv],
                       pn * 64, jt * kT, kvh, b);
+        iv = it + 1;
       }
       mbar_wait(&ctl->q_full, 0, status, nullptr);
       mbar_wait(&ctl->do_full, 0, status, nullptr);
-      for (int k = max(0, it - 2); k < it; ++k) {
-        mbar_wait(&ctl->k_full[k & 1], (k >> 1) & 1, status, nullptr);
-        mbar_wait(&ctl->v_full[k & 1], (k >> 1) & 1, status, nullptr);
-      }
+      for (int k = max(0, it - C::KST); k < it; ++k)
+        mbar_wait(&ctl->k_full[k % C::KST], (k / C::KST) & 1, status, nullptr);
+      for (int k = max(0, iv - C::VST); k < iv; ++k)
+        mbar_wait(&ctl->v_full[k % C::VST], (k / C::VST) & 1, status, nullptr);
     } else if (warp == 1 && lane == 0) {
       constexpr uint32_t idesc_s = idesc_bf16_f32(128, kT, 0, 0);  // S, dP: both K-major
       constexpr uint32_t idesc_g = idesc_bf16_f32(128, D, 0, 1);   // dQ': B = K' MN-major
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
-      auto issue_dq = [&](int jq) -> bool {  // dQ' += dS(jq) K'(jq)
-        if (!mbar_wait(&ctl->p_full[jq & 1], (jq >> 1) & 1, status, abort_flag)) return false;
+      auto issue_dq = [&](int jq) {  // dQ' += dS(jq) K'(jq); dS(jq) is in TMEM
+        AF_QTRACE(jq, 1);
         tc_fence_after();
-        const int s = jq & 1;
+        const int sk = jq % C::KST;
 #pragma unroll
         for (int kk = 0; kk < kT / 16; ++kk)
-          mma_ts(tmem + T_DQ, tmem + T_DS + s * 64 + kk * 8,
-                 smem_desc_sw128(sK + s * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
+          mma_ts(tmem + T_DQ, tmem + T_DS + (jq & 1) * 64 + kk * 8,
+                 smem_desc_sw128(sK + sk * C::TILE + kk * 2048, kT * 128, 1024), idesc_g,
                  (jq > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(&ctl->dq_done[s]);
-        mma_commit(&ctl->kv_free[s]);
-        return true;
+        mma_commit(&ctl->dq_done[jq & 1]);
+        mma_commit(&ctl->k_free[sk]);
       };
-      bool ok = mbar_wait(&ctl->q_ready, 0, status, abort_flag) &&
-                mbar_wait(&ctl->do_full, 0, status, abort_flag);
-      int nk = 0;  // visible key tiles (jt below counts them, not tile indices)
-      for (int kt = next_k(k_lo); kt < k_hi; kt = next_k(kt + 1)) ++nk;
-      for (int jt = 0; ok && jt < nk; ++jt) {
-        const int s = jt & 1;
-        const uint32_t ph = (jt >> 1) & 1;
-        ok = mbar_wait(&ctl->k_ready[s], ph, status, abort_flag) &&
-             mbar_wait(&ctl->v_full[s], ph, status, abort_flag);
-        // S and dP of tile jt overwrite those of tile jt-1 once the element-wise warps hold them
-        if (ok && jt > 0) ok = mbar_wait(&ctl->s_free, (jt - 1) & 1, status, abort_flag);
-        if (!ok) break;
+      auto issue_s = [&](int js) {  // S(js) = Q' K'(js)^T, dP(js) = dO V(js)^T
+        const int sk = js % C::KST, sv = js % C::VST;
+        AF_QTRACE(js, 0);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
           mma_ss(tmem + T_S, smem_desc_sw128(sQ + koff, 16, 1024),
-                 smem_desc_sw128(sK + s * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
+                 smem_desc_sw128(sK + sk * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (kT * 128) + (kk & 3) * 32;
           mma_ss(tmem + T_DP, smem_desc_sw128(sDO + koff, 16, 1024),
-                 smem_desc_sw128(sV + s * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
+                 smem_desc_sw128(sV + sv * C::TILE + koff, 16, 1024), idesc_s, kk > 0);
         }
         mma_commit(&ctl->s_full);
-        if (jt > 0) ok = issue_dq(jt - 1);
+        mma_commit(&ctl->v_free[sv]);  // V is read by dP only
+      };
+      bool ok = mbar_wait(&ctl->q_ready, 0, status, abort_flag) &&
+                mbar_wait(&ctl->do_full, 0, status, abort_flag);
+      int nk = 0;  // visible key tiles (js / jq below count them, not tile indices)
+      for (int kt = next_k(k_lo); kt < k_hi; kt = next_k(kt + 1)) ++nk;
+      // Poll-driven issue: dQ(jq) goes as soon as its dS is in TMEM (its completion frees the
+      // K/V stage of tile jq + 2), S(js) and dP(js) as soon as their tile has landed and the
+      // element-wise warps hold S(js - 1) and dP(js - 1). Neither waits behind the other; dQ
+      // goes first when both can. The poll is bounded like every wait.
+      int js = 0, jq = 0;
+      uint64_t t0 = 0;
+      uint32_t idle = 0;
+      while (ok && jq < nk) {
+        bool moved = false;
+        if (jq < js && mbar_test(&ctl->p_full[jq & 1], (jq >> 1) & 1)) {
+          issue_dq(jq);
+          ++jq;
+          moved = true;
+        } else if (js < nk) {
+          const int sk = js % C::KST, sv = js % C::VST;
+          if (mbar_test(&ctl->k_ready[sk], (js / C::KST) & 1) &&
+              mbar_test(&ctl->v_full[sv], (js / C::VST) & 1) &&
+              (js == 0 || mbar_test(&ctl->s_free, (js - 1) & 1))) {
+            issue_s(js);
+            ++js;
+            moved = true;
+          }
+        }
+        if (moved) {
+          idle = 0;
+        } else if ((++idle & 255u) == 1u) {
+          const uint64_t now = globaltimer_ns();
+          if (idle == 1u) t0 = now;
+          if (*abort_flag) {
+            ok = false;
+          } else if (now - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
+            atomicExch(status, kDevTimeout);
+            *abort_flag = 1;
+            ok = false;
+          }
+        }
       }
-      if (ok && nk > 0) issue_dq(nk - 1);
       mma_commit(&ctl->mma_final);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
     }
@@ -761,8 +817,8 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
     mbar_arrive(&ctl->q_ready);
     int it = 0;
     for (int jt = next_k(k_lo); jt < k_hi; jt = next_k(jt + 1), ++it) {
-      const int s = it & 1;
-      if (!mbar_wait(&ctl->k_full[s], (it >> 1) & 1, status, abort_flag)) break;
+      const int s = it % C::KST;
+      if (!mbar_wait(&ctl->k_full[s], (it / C::KST) & 1, status, abort_flag)) break;
       if (ROPE) {
         rotate_tile_bf16<D, kT>(smem + C::OFF_K + s * C::TILE, jt * kT, N, p.rope_cs, t);
         fence_proxy_async_smem();
@@ -803,6 +859,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
         ok = false;
         break;
       }
+      if (lane == 0 && wq == 0) AF_QTRACE(jt, 2 + hh);
       tc_fence_after();
       uint32_t sr[64], dr[64];
       tmem_ld32<0>(tmem + lane_off + T_S + 64 * hh, sr);
@@ -890,6 +947,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
+      if (lane == 0 && wq == 0) AF_QTRACE(jt, 4 + hh);
       if (lane == 0) mbar_arrive(&ctl->p_full[jt & 1]);
     }
     const int nk = jt;
