@@ -56,8 +56,10 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
-    ap.add_argument("--profile-target", default="fwd", choices=["fwd", "decode", "decode-b1", "train", "train-prerotate"],
-                    help="--profile: forward workload, Llama-3-70B decode (B=8) or fwd+bwd (N=2048)")
+    ap.add_argument("--profile-target", default="fwd",
+                    choices=["fwd", "decode", "decode-b1", "train", "train-prerotate", "d64-causal"],
+                    help="--profile: forward workload, Llama-3-70B decode (B=8), fwd+bwd (N=2048) "
+                         "or the head-dim-64 causal forward (B=2, H=16, N=4096, fused RoPE)")
     return ap.parse_args()
 
 
@@ -464,6 +466,12 @@ def run_profile(args):
         for _ in range(2):
             out, lse = af.fwd(q, k, v, rope_theta=5e5)
             af.bwd(q, k, v, out, lse, do, rope_theta=5e5, rope_mode=mode)
+    elif args.profile_target == "d64-causal":
+        x = inputs.prefill(2, 16, 16, 4096, 64, seed=3000)
+        q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+        for _ in range(2):
+            af.fwd(q, k, v, rope_theta=1e4, rope_mode=af.ROPE_FUSED,
+                   variant=af.Variant(mask=af.MASK_CAUSAL))
     else:
         B, Hq, Hkv, N, d, theta, mode, _ = WORKLOADS[args.workload]
         rope_mode = {"fused": af.ROPE_FUSED, "prerotate": af.ROPE_PREROTATE, "none": af.ROPE_NONE}[mode]
