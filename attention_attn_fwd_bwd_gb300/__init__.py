@@ -127,6 +127,26 @@ def _ptr(t):
     return ctypes.c_void_p(0 if t is None else t.data_ptr())
 
 
+def _need(t, name, dtypes, shape=None, device=None, contiguous=False, ndim=None, dims=""):
+    """Reject what the C ABI cannot see through a bare pointer: a tensor that is not on the
+    CUDA device of the call (its address would reach a kernel), of another element type, of
+    another shape, or (where the call takes no strides) not contiguous."""
+    import torch
+
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name}: expected {dims}, got shape {tuple(t.shape)}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {' or '.join(str(x) for x in dtypes)}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+    if t.device.type != "cuda" or (device is not None and t.device != device):
+        raise ValueError(f"{name}: on {t.device}, expected {device or 'a CUDA device'}")
+
+
 # ------------------------------------------------------------------------------------------
 # C names (raw pointers)
 # ------------------------------------------------------------------------------------------
@@ -158,6 +178,41 @@ class Variant:
         self.bias, self.alibi_slopes, self.add_bias = bias, alibi_slopes, add_bias
         self.tile_visits = tile_visits
         self.dbias = dbias
+
+    def check(self, device, B, Hq, N):
+        """Validate the variant's tensors for a call on `device` with B, Hq and N (lengths
+        the kernels index by; the values of a block-sparse layout are the caller's to keep in
+        range, since reading them here would synchronise the stream)."""
+        import torch
+
+        if self.mask == MASK_BLOCK_SPARSE:
+            if self.bs_row_ptr is None or self.bs_col_idx is None:
+                raise ValueError("block-sparse variant: bs_row_ptr and bs_col_idx are required")
+            if self.bs_block in (64, 128):
+                rows = -(-N // self.bs_block)
+                if self.bs_row_ptr.numel() < rows + 1:
+                    raise ValueError(f"bs_row_ptr: {self.bs_row_ptr.numel()} entries, "
+                                     f"the layout has {rows} block rows (needs {rows + 1})")
+            _need(self.bs_row_ptr, "bs_row_ptr", (torch.int32,), device=device, contiguous=True)
+            _need(self.bs_col_idx, "bs_col_idx", (torch.int32,), device=device, contiguous=True)
+        if self.alibi_slopes is not None:
+            if self.alibi_slopes.numel() < Hq:
+                raise ValueError(f"alibi_slopes: {self.alibi_slopes.numel()} entries for {Hq} heads")
+            _need(self.alibi_slopes, "alibi_slopes", (torch.float32,), device=device, contiguous=True)
+        if self.add_bias is not None:
+            if self.add_bias.dim() > 4:
+                raise ValueError("add_bias: at most 4 dimensions ([B, Hq, N, N])")
+            full = (B, Hq, N, N)[4 - self.add_bias.dim():]
+            for have, want in zip(self.add_bias.shape, full):
+                if have not in (1, want):
+                    raise ValueError(f"add_bias: shape {tuple(self.add_bias.shape)} does not "
+                                     f"broadcast to {(B, Hq, N, N)}")
+            _need(self.add_bias, "add_bias", (torch.float32, torch.bfloat16), device=device)
+        if self.tile_visits is not None:
+            t = -(-N // 128)
+            _need(self.tile_visits, "tile_visits", (torch.uint8,), (B, Hq, t, t), device, True)
+        if self.dbias is not None:
+            _need(self.dbias, "dbias", (torch.float32,), (B, Hq, N, N), device)
 
     def c_struct(self):
         v = CVariant()
@@ -216,8 +271,10 @@ def _workspace(nbytes, device, workspace=None):
 
     if nbytes == 0:
         return None
-    if workspace is not None and workspace.numel() * workspace.element_size() >= nbytes:
-        return workspace
+    if workspace is not None:
+        _need(workspace, "workspace", (workspace.dtype,), device=device)
+        if workspace.numel() * workspace.element_size() >= nbytes:
+            return workspace
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 
@@ -226,14 +283,25 @@ def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=N
     """Forward: q [B,Hq,N,d], k/v [B,Hkv,N,d] bf16 CUDA tensors -> (out, lse)."""
     import torch
 
+    bf16, f32 = (torch.bfloat16,), (torch.float32,)
+    _need(q, "q", bf16, ndim=4, dims="[B, Hq, N, d]")
     B, Hq, N, d = q.shape
+    dev = q.device
+    _need(k, "k", bf16, ndim=4, dims="[B, Hkv, N, d]")
     Hkv = k.shape[1]
+    _need(k, "k", bf16, (B, Hkv, N, d), dev)
+    _need(v, "v", bf16, (B, Hkv, N, d), dev)
     if scale is None:
         scale = d ** -0.5
     if out is None:
         out = torch.empty_like(q)
+    _need(out, "out", bf16, (B, Hq, N, d), dev)
     if with_lse and lse is None:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", f32, (B, Hq, N), dev, contiguous=True)
+    if variant is not None:
+        variant.check(dev, B, Hq, N)
     ws_n = fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode & 0xFF)
     ws = _workspace(ws_n, q.device, workspace)
     cv = (variant or Variant()).c_struct()
@@ -249,13 +317,27 @@ def bwd(q, k, v, out, lse, dout, scale=None, rope_theta=10000.0, rope_mode=ROPE_
     """Backward (paper §4.4): returns (dq, dk, dv) w.r.t. the un-rotated q, k and v."""
     import torch
 
+    bf16, f32 = (torch.bfloat16,), (torch.float32,)
+    _need(q, "q", bf16, ndim=4, dims="[B, Hq, N, d]")
     B, Hq, N, d = q.shape
+    dev = q.device
+    _need(k, "k", bf16, ndim=4, dims="[B, Hkv, N, d]")
     Hkv = k.shape[1]
+    _need(k, "k", bf16, (B, Hkv, N, d), dev)
+    _need(v, "v", bf16, (B, Hkv, N, d), dev)
+    _need(out, "out", bf16, (B, Hq, N, d), dev)
+    _need(lse, "lse", f32, (B, Hq, N), dev, contiguous=True)
+    _need(dout, "dout", bf16, (B, Hq, N, d), dev)
     if scale is None:
         scale = d ** -0.5
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _need(dq, "dq", bf16, (B, Hq, N, d), dev)
+    _need(dk, "dk", bf16, (B, Hkv, N, d), dev)
+    _need(dv, "dv", bf16, (B, Hkv, N, d), dev)
+    if variant is not None:
+        variant.check(dev, B, Hq, N)
     ws_n = bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode)
     ws = _workspace(ws_n, q.device, workspace)
     cv = (variant or Variant()).c_struct()
@@ -273,14 +355,23 @@ def decode(q, k_cache, v_cache, q_pos, scale=None, rope_theta=10000.0, rope_mode
     """Split-KV decode (paper §4.2): q [B,Hq,d], caches [B,Hkv,L,d] -> (out [B,Hq,d], lse)."""
     import torch
 
+    bf16 = (torch.bfloat16,)
+    _need(q, "q", bf16, ndim=3, dims="[B, Hq, d]")
     B, Hq, d = q.shape
+    dev = q.device
+    _need(k_cache, "k_cache", bf16, ndim=4, dims="[B, Hkv, L, d]")
     Hkv, L = k_cache.shape[1], k_cache.shape[2]
+    _need(k_cache, "k_cache", bf16, (B, Hkv, L, d), dev)
+    _need(v_cache, "v_cache", bf16, (B, Hkv, L, d), dev)
     if scale is None:
         scale = d ** -0.5
     if out is None:
         out = torch.empty_like(q)
+    _need(out, "out", bf16, (B, Hq, d), dev)
     if with_lse and lse is None:
         lse = torch.empty((B, Hq), dtype=torch.float32, device=q.device)
+    if lse is not None:
+        _need(lse, "lse", (torch.float32,), (B, Hq), dev, contiguous=True)
     ws_n = decode_workspace_size(B, Hq, Hkv, L, d, num_splits)
     ws = _workspace(ws_n, q.device, workspace)
     _check(load().attnfuse_decode(
@@ -301,8 +392,10 @@ def rope_prerotate(x, rope_theta, out=None, workspace=None, stream=None):
     """x [B,H,N,d] bf16 -> R_n x (contiguous)."""
     import torch
 
+    _need(x, "x", (torch.bfloat16,), ndim=4, dims="[B, H, N, d]")
     B, H, N, d = x.shape
     out = torch.empty((B, H, N, d), dtype=x.dtype, device=x.device) if out is None else out
+    _need(out, "out", (torch.bfloat16,), (B, H, N, d), x.device, contiguous=True)
     ws_n = fwd_workspace_size(B, H, H, N, d, ROPE_FUSED)
     ws = _workspace(ws_n, x.device, workspace)
     _check(load().attnfuse_rope_prerotate(_ptr(x), _strides(x, 4), _ptr(out), B, H, N, d,
