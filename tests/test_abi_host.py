@@ -125,3 +125,38 @@ def test_decode_and_bwd_validation(lib):
 
 def test_version(lib):
     assert lib.attnfuse_version() >= 100
+
+
+def test_rope_entry_points_validation(lib):
+    x_st = _st(4 * 1024 * 64, 1024 * 64, 64, 1)
+    pre = lambda x=FAKE, out=FAKE, d=64, theta=1e4, ws=FAKE, ws_bytes=1 << 20: \
+        lib.attnfuse_rope_prerotate(x, x_st, out, 1, 4, 1024, d, theta, ws, ws_bytes, None)
+    assert pre(d=96) == UNSUPPORTED
+    assert pre(x=None) == INVALID
+    assert pre(out=ctypes.c_void_p(0x100008)) == INVALID  # output must be 16-byte aligned
+    assert pre(theta=0.0) == INVALID
+    assert pre(ws_bytes=1024) == WS_SMALL  # the (cos, sin) table of 1024 x 32 pairs
+    table = lambda t=FAKE, nbytes=1 << 20, N=1024, d=64, theta=1e4: \
+        lib.attnfuse_rope_table(t, nbytes, N, d, theta, None)
+    assert table(N=0) == UNSUPPORTED
+    assert table(d=32) == UNSUPPORTED
+    assert table(theta=-1.0) == INVALID
+    assert table(t=None) == WS_SMALL
+    assert table(nbytes=1024 * 32 * 8 - 1) == WS_SMALL
+
+
+def test_rope_auto_mode_rule(lib):
+    m = ctypes.c_int()
+    auto = lambda N, d, bwd: (lib.attnfuse_rope_auto_mode(N, d, bwd, ctypes.byref(m)), m.value)
+    FUSED, PRE = af.ROPE_FUSED, af.ROPE_PREROTATE
+    # head dim 128: the pre-rotation pass is cheaper at every measured N
+    assert auto(256, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
+    # head dim 64: fusion wins below the measured crossovers (forward 1260, backward 284)
+    assert auto(1259, 64, 0) == (OK, FUSED) and auto(1260, 64, 0) == (OK, PRE)
+    assert auto(283, 64, 1) == (OK, FUSED) and auto(284, 64, 1) == (OK, PRE)
+    assert lib.attnfuse_rope_auto_mode(0, 64, 0, ctypes.byref(m)) == INVALID
+    assert lib.attnfuse_rope_auto_mode(512, 80, 0, ctypes.byref(m)) == UNSUPPORTED
+    assert lib.attnfuse_rope_auto_mode(512, 64, 0, None) == INVALID
+    n = ctypes.c_int()
+    assert lib.attnfuse_decode_auto_splits(0, 8, 32768, ctypes.byref(n)) == INVALID
+    assert lib.attnfuse_decode_auto_splits(1, 8, 32768, None) == INVALID
