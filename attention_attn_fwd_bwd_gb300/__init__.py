@@ -116,11 +116,19 @@ def _strides(t, n):
     return arr
 
 
-def _stream(stream=None):
+def _launch_context(device, stream=None):
+    """(context manager, stream handle) for a call whose tensors live on `device`.
+
+    The C ABI works on the current CUDA device (its status word, tensor maps and launches), so
+    every call runs with the tensors' device made current and, unless the caller passes one,
+    on that device's current stream. A stream of another device is rejected."""
     import torch
 
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return ctypes.c_void_p(s.cuda_stream)
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    elif stream.device != device:
+        raise ValueError(f"stream is on {stream.device}, the tensors on {device}")
+    return torch.cuda.device(device), ctypes.c_void_p(stream.cuda_stream)
 
 
 def _ptr(t):
@@ -266,14 +274,21 @@ def decode_workspace_size(B, Hq, Hkv, L, d, num_splits):
     return n.value
 
 
-def _workspace(nbytes, device, workspace=None):
+def _workspace(nbytes, device, workspace=None, reuse_table=False):
+    """The caller's workspace if it holds nbytes, else a new one. With ROPE_REUSE_TABLE the
+    (cos, sin) table must already sit in the caller's workspace, so a missing or too small one
+    is an error (a new buffer would hold no table)."""
     import torch
 
+    have = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if reuse_table and (workspace is None or have < nbytes):
+        raise ValueError(f"ROPE_REUSE_TABLE needs the workspace that holds the table "
+                         f"({nbytes} bytes); got {'none' if workspace is None else f'{have} bytes'}")
     if nbytes == 0:
         return None
     if workspace is not None:
         _need(workspace, "workspace", (workspace.dtype,), device=device)
-        if workspace.numel() * workspace.element_size() >= nbytes:
+        if have >= nbytes:
             return workspace
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
@@ -303,12 +318,14 @@ def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=N
     if variant is not None:
         variant.check(dev, B, Hq, N)
     ws_n = fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode & 0xFF)
-    ws = _workspace(ws_n, q.device, workspace)
+    ws = _workspace(ws_n, dev, workspace, bool(rope_mode & ROPE_REUSE_TABLE))
     cv = (variant or Variant()).c_struct()
-    _check(load().attnfuse_fwd(
-        _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
-        _ptr(out), _strides(out, 4), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
-        float(rope_theta), rope_mode, ctypes.byref(cv), _ptr(ws), ws_n, _stream(stream)))
+    ctx, st = _launch_context(dev, stream)
+    with ctx:
+        _check(load().attnfuse_fwd(
+            _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
+            _ptr(out), _strides(out, 4), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+            float(rope_theta), rope_mode, ctypes.byref(cv), _ptr(ws), ws_n, st))
     return out, lse
 
 
@@ -338,15 +355,17 @@ def bwd(q, k, v, out, lse, dout, scale=None, rope_theta=10000.0, rope_mode=ROPE_
     _need(dv, "dv", bf16, (B, Hkv, N, d), dev)
     if variant is not None:
         variant.check(dev, B, Hq, N)
-    ws_n = bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode)
-    ws = _workspace(ws_n, q.device, workspace)
+    ws_n = bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode & 0xFF)
+    ws = _workspace(ws_n, dev, workspace, bool(rope_mode & ROPE_REUSE_TABLE))
     cv = (variant or Variant()).c_struct()
-    _check(load().attnfuse_bwd(
-        _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
-        _ptr(out), _strides(out, 4), _ptr(lse), _ptr(dout), _strides(dout, 4),
-        _ptr(dq), _strides(dq, 4), _ptr(dk), _strides(dk, 4), _ptr(dv), _strides(dv, 4),
-        B, Hq, Hkv, N, d, float(scale), float(rope_theta), rope_mode, ctypes.byref(cv),
-        _ptr(ws), ws_n, _stream(stream)))
+    ctx, st = _launch_context(dev, stream)
+    with ctx:
+        _check(load().attnfuse_bwd(
+            _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
+            _ptr(out), _strides(out, 4), _ptr(lse), _ptr(dout), _strides(dout, 4),
+            _ptr(dq), _strides(dq, 4), _ptr(dk), _strides(dk, 4), _ptr(dv), _strides(dv, 4),
+            B, Hq, Hkv, N, d, float(scale), float(rope_theta), rope_mode, ctypes.byref(cv),
+            _ptr(ws), ws_n, st))
     return dq, dk, dv
 
 
@@ -373,12 +392,14 @@ def decode(q, k_cache, v_cache, q_pos, scale=None, rope_theta=10000.0, rope_mode
     if lse is not None:
         _need(lse, "lse", (torch.float32,), (B, Hq), dev, contiguous=True)
     ws_n = decode_workspace_size(B, Hq, Hkv, L, d, num_splits)
-    ws = _workspace(ws_n, q.device, workspace)
-    _check(load().attnfuse_decode(
-        _ptr(q), _strides(q, 3), _ptr(k_cache), _strides(k_cache, 4), _ptr(v_cache),
-        _strides(v_cache, 4), _ptr(out), _strides(out, 3), _ptr(lse), B, Hq, Hkv, L, d,
-        int(q_pos), float(scale), float(rope_theta), rope_mode, int(num_splits), _ptr(ws), ws_n,
-        _stream(stream)))
+    ws = _workspace(ws_n, dev, workspace)
+    ctx, st = _launch_context(dev, stream)
+    with ctx:
+        _check(load().attnfuse_decode(
+            _ptr(q), _strides(q, 3), _ptr(k_cache), _strides(k_cache, 4), _ptr(v_cache),
+            _strides(v_cache, 4), _ptr(out), _strides(out, 3), _ptr(lse), B, Hq, Hkv, L, d,
+            int(q_pos), float(scale), float(rope_theta), rope_mode, int(num_splits), _ptr(ws),
+            ws_n, st))
     return out, lse
 
 
@@ -398,13 +419,22 @@ def rope_prerotate(x, rope_theta, out=None, workspace=None, stream=None):
     _need(out, "out", (torch.bfloat16,), (B, H, N, d), x.device, contiguous=True)
     ws_n = fwd_workspace_size(B, H, H, N, d, ROPE_FUSED)
     ws = _workspace(ws_n, x.device, workspace)
-    _check(load().attnfuse_rope_prerotate(_ptr(x), _strides(x, 4), _ptr(out), B, H, N, d,
-                                          float(rope_theta), _ptr(ws), ws_n, _stream(stream)))
+    ctx, st = _launch_context(x.device, stream)
+    with ctx:
+        _check(load().attnfuse_rope_prerotate(_ptr(x), _strides(x, 4), _ptr(out), B, H, N, d,
+                                              float(rope_theta), _ptr(ws), ws_n, st))
     return out
 
 
-def device_status(clear=True, stream=None):
-    """Synchronise and return the device status word (0 OK, 5 TIMEOUT)."""
+def device_status(clear=True, stream=None, device=None):
+    """Synchronise and return the device status word (0 OK, 5 TIMEOUT) of `device` (default:
+    the stream's device, else the current device)."""
+    import torch
+
+    if device is None:
+        device = stream.device if stream is not None else torch.device("cuda", torch.cuda.current_device())
     code = ctypes.c_int()
-    _check(load().attnfuse_device_status(_stream(stream), int(clear), ctypes.byref(code)))
+    ctx, st = _launch_context(device, stream)
+    with ctx:
+        _check(load().attnfuse_device_status(st, int(clear), ctypes.byref(code)))
     return code.value

@@ -366,12 +366,13 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   p.num_t = p.pair_heads ? TQ : (TQ + 1) / 2;
   p.pairs = p.pair_heads ? Hq / 2 : Hq;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
   p.status = st;
   const int64_t grid = (int64_t)p.num_t * B * p.pairs;
   if (grid > 0x7fffffff) return fail(ATTNFUSE_ERR_UNSUPPORTED, "problem too large (grid %lld)", (long long)grid);
   const int rk = rope_mode == ATTNFUSE_ROPE_FUSED ? kRopeFused
                  : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
-  cudaError_t e = d == 128 ? launch_fwd_pair(p, rk, (int)grid, stream)
+  cudaError_t e = d == 128 ? launch_fwd_pp(p, rk, 0, stream)
                            : launch_fwd(p, d, rk, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ok();

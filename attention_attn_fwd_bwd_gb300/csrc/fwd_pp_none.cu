@@ -1,0 +1,8 @@
+// Instances of the persistent head-dim-128 forward (fwd_pp.cuh) for RoPE kind kRopeNone.
+#include "fwd_pp.cuh"
+
+namespace afx {
+
+FwdFn fwd_pp_pick_none(int bias, int norm) { return fwd_pp_pick<kRopeNone>(bias, norm); }
+
+}  // namespace afx

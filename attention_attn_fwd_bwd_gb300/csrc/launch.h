@@ -20,6 +20,9 @@ struct FwdParams {
   int num_t;                  // q tiles (pair_heads) or q-tile pairs
   int pairs;                  // head pairs (Hq/2) or heads (Hq)
   float scale_log2;           // scale * log2(e)
+  float scale;
+  int pp_hp;                  // persistent head-dim-128 forward: query heads per unit (1, 2, 4)
+  int pp_clusters;            // and the number of 2-CTA clusters launched
   VariantDev var;
   int* status;
 };
@@ -79,6 +82,10 @@ cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaS
 // Head dim 128: clusters of two CTAs, one per 256 query rows (tmK box of 64 rows).
 size_t fwd_pair_smem_size();
 cudaError_t launch_fwd_pair(const FwdParams& p, int rope_kind, int clusters, cudaStream_t stream);
+// Head dim 128, persistent: clusters of two CTAs walk units of four 128-row query tiles of
+// one KV head (two independent softmax slots per CTA). norm: 0 softmax, 1 ReLU (P = relu(s)/N).
+size_t fwd_pp_smem_size();
+cudaError_t launch_fwd_pp(FwdParams p, int rope_kind, int norm, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
                               cudaStream_t stream);
 // block: 0 = rotate with the table entry of each row; -1 = the forward kernels' query-tile

@@ -30,6 +30,9 @@
  *   - Supported head dims: d in {64, 128}. Hq % Hkv == 0.
  *   - Kernels give up on any internal wait after a bounded time instead of hanging; the
  *     device status word then reads ATTNFUSE_ERR_TIMEOUT (see attnfuse_device_status).
+ *   - The library looks up its device-side words (status word, decode scratch) once per device
+ *     and keeps their addresses for the life of the process: it must not be used on a device
+ *     after a cudaDeviceReset of that device.
  */
 #ifndef ATTNFUSE_H_
 #define ATTNFUSE_H_
@@ -199,7 +202,9 @@ attnfuse_status attnfuse_decode(const void* q, const int64_t q_strides[3], const
  *   - Problems whose partials need more than 4 MiB (attnfuse_decode_workspace_size) are
  *     rejected with ATTNFUSE_ERR_WORKSPACE_TOO_SMALL and a message naming both sizes.
  *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress)
- *     with that device current; make that first call before any stream capture.
+ *     with that device current; make that first call before any stream capture. The address
+ *     is kept for the life of the process: after a cudaDeviceReset of that device the array
+ *     is reloaded elsewhere, so do not call this entry point on a device that was reset.
  *   - All calls share the array, which keeps the last call's contents (every value a call
  *     reads is written by that same call first). Calls that overlap on the GPU, on one or
  *     several streams, race on the array and must be serialised by the caller. */

@@ -63,3 +63,49 @@ def test_variant_tensors_are_checked():
     v = af.Variant(mask=af.MASK_CAUSAL, dbias=torch.zeros(B, Hq, N, N - 1))
     with pytest.raises(ValueError, match="dbias: shape"):
         v.check(dev, B, Hq, N)
+
+
+class _FakeStream:
+    def __init__(self, device, handle):
+        self.device, self.cuda_stream = device, handle
+
+
+def test_calls_run_on_the_tensors_device_and_its_stream(monkeypatch):
+    """The C ABI works on the current device; the binding makes the tensors' device current
+    and takes that device's stream, so tensors on cuda:1 never reach a launch on cuda:0."""
+    seen = {}
+
+    class _Dev:
+        def __init__(self, device):
+            seen["device"] = device
+
+        def __enter__(self):
+            seen["entered"] = True
+
+        def __exit__(self, *exc):
+            return False
+
+    monkeypatch.setattr(torch.cuda, "device", _Dev)
+    monkeypatch.setattr(torch.cuda, "current_stream",
+                        lambda device=None: _FakeStream(device, 1234))
+    dev1 = torch.device("cuda", 1)
+    ctx, st = af._launch_context(dev1)
+    with ctx:
+        pass
+    assert seen == {"device": dev1, "entered": True}
+    assert st.value == 1234
+    # an explicit stream of another device is refused
+    with pytest.raises(ValueError, match="stream is on cuda:0"):
+        af._launch_context(dev1, _FakeStream(torch.device("cuda", 0), 99))
+    ctx, st = af._launch_context(dev1, _FakeStream(dev1, 77))
+    assert st.value == 77
+
+
+def test_reuse_table_needs_the_callers_workspace():
+    """ROPE_REUSE_TABLE reads the (cos, sin) table from the caller's workspace: a missing or
+    too small workspace is refused instead of replaced by a new (table-less) buffer."""
+    with pytest.raises(ValueError, match="ROPE_REUSE_TABLE.*got none"):
+        af._workspace(4096, torch.device("cuda", 0), None, reuse_table=True)
+    small = torch.zeros(100, dtype=torch.uint8)
+    with pytest.raises(ValueError, match="ROPE_REUSE_TABLE.*got 100 bytes"):
+        af._workspace(4096, torch.device("cuda", 0), small, reuse_table=True)

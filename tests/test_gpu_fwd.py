@@ -6,6 +6,7 @@ BLOCK_SPARSE, ALiBi and additive bias, GQA ratios, head dims 64 and 128, ragged 
 129, ...), the tiny and full-size workloads (full size on sampled rows), bit-exact tile-visit
 sets, and bitwise equality of FUSED and PREROTATE (same rotation code, same tables).
 """
+import ctypes
 import math
 
 import numpy as np
@@ -239,7 +240,7 @@ def test_full_size_mask_variants_sampled(vname):
 
 def test_timeout_path_reports_status():
     """A wait that can never complete gives up after its limit and sets the status word."""
-    af.load().attnfuse_debug_wait_timeout(2_000_000, af._stream())
+    af.load().attnfuse_debug_wait_timeout(2_000_000, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
     assert af.device_status(clear=True) == 5
     assert af.device_status(clear=True) == 0
     # the context is still usable

@@ -429,6 +429,23 @@ def test_tile_visits(orc):
     assert orc.allowed_pairs(N, orc.Variant(mask=1)) == N * (N + 1) // 2
 
 
+@pytest.mark.parametrize("BM,BN", [(256, 128), (128, 256), (64, 128)])
+def test_tile_visits_rectangular_tiles(orc, BM, BN):
+    """Query and key tiles of different heights. A causal (window) tile pair is visited iff the
+    key tile's first key is at or before the query tile's last row (and its last key is still
+    inside the first row's window): interval bounds, not the element loop of the oracle."""
+    N, W = 1000, 300
+    TQ, TK = -(-N // BM), -(-N // BN)
+    i, j = np.meshgrid(np.arange(TQ), np.arange(TK), indexing="ij")
+    m_lo, m_hi = BM * i, np.minimum(BM * i + BM - 1, N - 1)
+    n_lo, n_hi = BN * j, np.minimum(BN * j + BN - 1, N - 1)
+    vis = orc.tile_visits(N, BM, BN, orc.Variant(mask=1))
+    assert vis.shape == (TQ, TK)
+    assert np.array_equal(vis, (n_lo <= m_hi).astype(np.uint8))
+    vw = orc.tile_visits(N, BM, BN, orc.Variant(mask=2, window=W, causal=True))
+    assert np.array_equal(vw, ((n_lo <= m_hi) & (n_hi > m_lo - W)).astype(np.uint8))
+
+
 def test_bigbird_layout_structure():
     rp, ci = inputs.bigbird_csr(64, seed=3003)
     for r in range(64):
