@@ -26,6 +26,7 @@ ROPE_NONE, ROPE_FUSED, ROPE_PREROTATE, ROPE_AUTO = 0, 1, 2, 3
 ROPE_REUSE_TABLE = 0x100
 MASK_FULL, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK_SPARSE = 0, 1, 2, 3
 BIAS_NONE, BIAS_ALIBI, BIAS_ADDITIVE = 0, 1, 2
+NORM_SOFTMAX, NORM_RELU = 0, 1
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
            4: "CUDA_ERROR", 5: "TIMEOUT"}
 
@@ -58,6 +59,9 @@ class CVariant(ctypes.Structure):
         ("tile_visits", ctypes.c_void_p),
         ("dbias", ctypes.c_void_p),
         ("dbias_strides", ctypes.c_int64 * 4),
+        ("normalizer", ctypes.c_int32),
+        ("bwd_dq_visits", ctypes.c_void_p),
+        ("bwd_dkdv_visits", ctypes.c_void_p),
     ]
 
 
@@ -174,13 +178,19 @@ class Variant:
     bs_col_idx: int32 CSR block layout (block edge bs_block, 64 or 128); bias: BIAS_*;
     alibi_slopes: fp32 [Hq]; add_bias: fp32 or bf16 tensor broadcastable to [B, Hq, N, N];
     tile_visits: uint8 [B, Hq, ceil(N/128), ceil(N/128)] (debug record of computed tiles);
+    bwd_dq_visits / bwd_dkdv_visits: the backward's records, uint8 [B, Hq, ceil(N/128),
+    ceil(N/128)] (dQ kernel) and [B, Hq, ceil(N/64), ceil(N/128)] (dK/dV kernel, 64-row blocks);
     dbias: fp32 [B, Hq, N, N] output of the backward with an additive bias (its gradient before
-    any broadcast is summed out).
+    any broadcast is summed out); norm: NORM_SOFTMAX or NORM_RELU (relu_attention: O_m =
+    (1/N) sum_n max(s_mn, 0) v_n, forward only, no LSE).
     """
 
     def __init__(self, mask=MASK_CAUSAL, causal=False, window=0, bs_block=64, bs_row_ptr=None,
                  bs_col_idx=None, bias=BIAS_NONE, alibi_slopes=None, add_bias=None,
-                 tile_visits=None, dbias=None):
+                 tile_visits=None, dbias=None, norm=NORM_SOFTMAX, bwd_dq_visits=None,
+                 bwd_dkdv_visits=None):
+        self.norm = norm
+        self.bwd_dq_visits, self.bwd_dkdv_visits = bwd_dq_visits, bwd_dkdv_visits
         self.mask, self.causal, self.window, self.bs_block = mask, causal, window, bs_block
         self.bs_row_ptr, self.bs_col_idx = bs_row_ptr, bs_col_idx
         self.bias, self.alibi_slopes, self.add_bias = bias, alibi_slopes, add_bias
@@ -221,6 +231,12 @@ class Variant:
             _need(self.tile_visits, "tile_visits", (torch.uint8,), (B, Hq, t, t), device, True)
         if self.dbias is not None:
             _need(self.dbias, "dbias", (torch.float32,), (B, Hq, N, N), device)
+        if self.bwd_dq_visits is not None:
+            t = -(-N // 128)
+            _need(self.bwd_dq_visits, "bwd_dq_visits", (torch.uint8,), (B, Hq, t, t), device, True)
+        if self.bwd_dkdv_visits is not None:
+            _need(self.bwd_dkdv_visits, "bwd_dkdv_visits", (torch.uint8,),
+                  (B, Hq, -(-N // 64), -(-N // 128)), device, True)
 
     def c_struct(self):
         v = CVariant()
@@ -228,6 +244,7 @@ class Variant:
         if self.bs_row_ptr is not None:
             v.bs_row_ptr, v.bs_col_idx = self.bs_row_ptr.data_ptr(), self.bs_col_idx.data_ptr()
         v.bias = self.bias
+        v.normalizer = self.norm
         if self.alibi_slopes is not None:
             v.alibi_slopes = self.alibi_slopes.data_ptr()
         if self.add_bias is not None:
@@ -242,6 +259,10 @@ class Variant:
                 v.add_bias_strides[i] = ab.stride(i) if ab.size(i) > 1 else 0
         if self.tile_visits is not None:
             v.tile_visits = self.tile_visits.data_ptr()
+        if self.bwd_dq_visits is not None:
+            v.bwd_dq_visits = self.bwd_dq_visits.data_ptr()
+        if self.bwd_dkdv_visits is not None:
+            v.bwd_dkdv_visits = self.bwd_dkdv_visits.data_ptr()
         if self.dbias is not None:
             v.dbias = self.dbias.data_ptr()
             for i in range(4):
@@ -311,7 +332,10 @@ def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=N
     if out is None:
         out = torch.empty_like(q)
     _need(out, "out", bf16, (B, Hq, N, d), dev)
-    if with_lse and lse is None:
+    relu = variant is not None and variant.norm == NORM_RELU
+    if relu and lse is not None:
+        raise ValueError("relu_attention has no LSE: pass lse=None")
+    if with_lse and lse is None and not relu:
         lse = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
     if lse is not None:
         _need(lse, "lse", f32, (B, Hq, N), dev, contiguous=True)

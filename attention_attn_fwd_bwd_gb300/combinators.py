@@ -95,8 +95,9 @@ def softmax():
 
 
 def relu_attention():
-    """Named by the paper among its ten combinators without a definition; composing it raises
-    NotImplementedError rather than guessing its semantics."""
+    """ReLU normaliser instead of softmax. The paper names it among its ten combinators without
+    a definition; this library reads it as O_m = (1/N) sum_n max(s_mn, 0) v_n over the visible
+    keys, N the sequence length. Forward only (no LSE, no gradient); head dim 128."""
     return Combinator("relu_attention")
 
 
@@ -111,9 +112,8 @@ class Attention:
         for k in set(kinds):
             if kinds.count(k) > 1:
                 raise ValueError(f"{k} given twice")
-        if "relu_attention" in kinds:
-            raise NotImplementedError(
-                "relu_attention: the paper names it but gives no semantics to implement")
+        if "relu_attention" in kinds and "softmax" in kinds:
+            raise ValueError("one normaliser per variant (softmax or relu_attention)")
         by = {c.kind: c for c in combinators}
         masks = [k for k in ("full", "sliding_window", "block_sparse") if k in by]
         if len(masks) > 1:
@@ -155,6 +155,8 @@ class Attention:
             v.bias, v.alibi_slopes = af.BIAS_ALIBI, slopes
         elif self.bias is not None:
             v.bias, v.add_bias = af.BIAS_ADDITIVE, self.bias
+        if "relu_attention" in by:
+            v.norm = af.NORM_RELU
         return v
 
     def __call__(self, q, k, v):
@@ -179,6 +181,11 @@ def _autograd_function():
             var = spec.variant(q.shape[1], q.device)
             out, lse = af.fwd(q, k, v, scale=scale, rope_theta=spec.rope_theta,
                               rope_mode=spec.rope_mode, variant=var)
+            if lse is None:  # relu_attention: forward only
+                lse = torch.empty(0, device=q.device)
+                ctx.relu = True
+            else:
+                ctx.relu = False
             ctx.save_for_backward(q, k, v, out, lse)
             ctx.spec, ctx.scale, ctx.bias = spec, scale, bias
             return out
@@ -186,6 +193,8 @@ def _autograd_function():
         @staticmethod
         def backward(ctx, dout):
             q, k, v, out, lse = ctx.saved_tensors
+            if ctx.relu:
+                raise NotImplementedError("relu_attention has no backward in this library")
             spec, bias = ctx.spec, ctx.bias
             var = spec.variant(q.shape[1], q.device)
             dbias = None

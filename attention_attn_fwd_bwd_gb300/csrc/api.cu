@@ -183,6 +183,9 @@ attnfuse_status to_dev_variant(const attnfuse_variant* v, int N, int Hq, Variant
     }
   }
   out->visits = v->tile_visits;
+  if (v->normalizer != ATTNFUSE_NORM_SOFTMAX && v->normalizer != ATTNFUSE_NORM_RELU)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "normalizer %d", v->normalizer);
+  out->norm = v->normalizer;
   (void)Hq;
   return ATTNFUSE_OK;
 }
@@ -220,11 +223,7 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
     e = cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clear status word");
   }
-#ifdef ATTNFUSE_WAIT_DIAG
-  *code = v;  // diagnostic builds: the raw record of the first timeout
-#else
   *code = v ? ATTNFUSE_ERR_TIMEOUT : ATTNFUSE_OK;
-#endif
   return ok();
 }
 
@@ -319,6 +318,10 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   FwdParams p;
   memset(&p, 0, sizeof(p));
   if ((rc = to_dev_variant(variant, N, Hq, &p.var))) return rc;
+  if (p.var.norm == ATTNFUSE_NORM_RELU) {
+    if (lse) return fail(ATTNFUSE_ERR_INVALID_ARG, "relu_attention has no LSE: pass lse = NULL");
+    if (d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "relu_attention needs head dim 128");
+  }
   size_t need = 0;
   if ((rc = attnfuse_fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, &need))) return rc;
   if (need && (!workspace || workspace_bytes < need || !aligned16(workspace)))
@@ -372,7 +375,7 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   if (grid > 0x7fffffff) return fail(ATTNFUSE_ERR_UNSUPPORTED, "problem too large (grid %lld)", (long long)grid);
   const int rk = rope_mode == ATTNFUSE_ROPE_FUSED ? kRopeFused
                  : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
-  cudaError_t e = d == 128 ? launch_fwd_pp(p, rk, 0, stream)
+  cudaError_t e = d == 128 ? launch_fwd_pp(p, rk, p.var.norm, stream)
                            : launch_fwd(p, d, rk, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ok();
@@ -450,6 +453,8 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
     return fail(ATTNFUSE_ERR_INVALID_ARG, "rope_theta must be positive");
   VariantDev var;
   if ((rc = to_dev_variant(variant, N, Hq, &var))) return rc;
+  if (var.norm != ATTNFUSE_NORM_SOFTMAX)
+    return fail(ATTNFUSE_ERR_UNSUPPORTED, "the backward supports the softmax normaliser only");
   var.visits = nullptr;  // the tile-visit record belongs to the forward
   float* dbias = variant ? variant->dbias : nullptr;
   if (dbias) {
@@ -520,6 +525,10 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
   p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.d = d; p.g = Hq / Hkv;
   p.var = var;
   p.dbias = dbias;
+  if (variant) {
+    p.visits_dq = variant->bwd_dq_visits;
+    p.visits_kv = variant->bwd_dkdv_visits;
+  }
   if (dbias) {
     for (int i = 0; i < 3; ++i) p.db_s[i] = variant->dbias_strides[i];
     p.db_vec2 = ((reinterpret_cast<uintptr_t>(dbias) & 7u) == 0 && p.db_s[0] % 2 == 0 &&

@@ -61,9 +61,3 @@ cudaError_t launch_bwd(const BwdParams& p, int rk, cudaStream_t stream) {
 
 }  // namespace afx
 
-#ifdef ATTNFUSE_TRACE_DQ
-// Copy the dQ pipeline trace (65 rows x 8 events of clock64) to host memory.
-extern "C" int attnfuse_dq_trace_read(unsigned long long* dst) {
-  return (int)cudaMemcpyFromSymbol(dst, afx::g_dq_trace, sizeof(unsigned long long) * 65 * 8);
-}
-#endif

@@ -38,19 +38,6 @@
 
 namespace afx {
 
-// Optional pipeline tracing of the dQ kernel (compile with -DATTNFUSE_TRACE_DQ=<block>; off by
-// default): that CTA records clock64() at pipeline events of its first 64 key tiles.
-#ifdef ATTNFUSE_TRACE_DQ
-static __device__ unsigned long long g_dq_trace[65 * 8];
-#define AF_QTRACE(i, e)                                                                   \
-  do {                                                                                    \
-    if (blockIdx.x == (ATTNFUSE_TRACE_DQ) && (i) <= 64) g_dq_trace[(i) * 8 + (e)] = clock64(); \
-  } while (0)
-#else
-#define AF_QTRACE(i, e) \
-  do {                  \
-  } while (0)
-#endif
 
 namespace {
 
@@ -480,6 +467,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1) dkdv_kernel(const __grid_const
       const int s = it % QST, bs = it & 1;
       const int h = kvh * g + it / nq, qi = qtile(it % nq);
       const int m0 = qi * kBq;
+      if (p.visits_kv && r == 0) p.visits_kv[((static_cast<int64_t>(b) * Hq + h) * TQ64 + qi) * TK + j] = 1;
       float slope2 = 0.f;
       if constexpr (BIAS == 1) slope2 = var.slopes[h] * kLog2e;
       float* vec = reinterpret_cast<float*>(smem + C::OFF_VEC + s * 512);
@@ -706,7 +694,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       for (int jt = next_k(k_lo); jt < k_hi; jt = next_k(jt + 1), ++it) {
         const int sk = it % C::KST, sv = it % C::VST;
         if (it >= C::KST && !mbar_wait(&ctl->k_free[sk], ((it / C::KST) - 1) & 1, status, abort_flag)) break;
-        AF_QTRACE(it, 6);
         mbar_arrive_expect_tx(&ctl->k_full[sk], C::TILE);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d(smem + C::OFF_K + sk * C::TILE + pn * (kT * 128), &p.tmK, &ctl->k_full[sk],
@@ -733,7 +720,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       const uint32_t sQ = smem_u32(smem + C::OFF_Q), sDO = smem_u32(smem + C::OFF_DO);
       const uint32_t sK = smem_u32(smem + C::OFF_K), sV = smem_u32(smem + C::OFF_V);
       auto issue_dq = [&](int jq) {  // dQ' += dS(jq) K'(jq); dS(jq) is in TMEM
-        AF_QTRACE(jq, 1);
         tc_fence_after();
         const int sk = jq % C::KST;
 #pragma unroll
@@ -746,7 +732,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       };
       auto issue_s = [&](int js) {  // S(js) = Q' K'(js)^T, dP(js) = dO V(js)^T
         const int sk = js % C::KST, sv = js % C::VST;
-        AF_QTRACE(js, 0);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -816,8 +801,11 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
     }
     mbar_arrive(&ctl->q_ready);
     int it = 0;
+    uint8_t* const visits = p.visits_dq;
+    const int TKv = (N + kT - 1) / kT;
     for (int jt = next_k(k_lo); jt < k_hi; jt = next_k(jt + 1), ++it) {
       const int s = it % C::KST;
+      if (visits && t == 0) visits[((static_cast<int64_t>(b) * p.Hq + h) * TQ + i) * TKv + jt] = 1;
       if (!mbar_wait(&ctl->k_full[s], (it / C::KST) & 1, status, abort_flag)) break;
       if (ROPE) {
         rotate_tile_bf16<D, kT>(smem + C::OFF_K + s * C::TILE, jt * kT, N, p.rope_cs, t);
@@ -859,7 +847,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
         ok = false;
         break;
       }
-      if (lane == 0 && wq == 0) AF_QTRACE(jt, 2 + hh);
       tc_fence_after();
       uint32_t sr[64], dr[64];
       tmem_ld32<0>(tmem + lane_off + T_S + 64 * hh, sr);
@@ -947,7 +934,6 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0 && wq == 0) AF_QTRACE(jt, 4 + hh);
       if (lane == 0) mbar_arrive(&ctl->p_full[jt & 1]);
     }
     const int nk = jt;

@@ -180,6 +180,7 @@ struct VariantDev {
   const void* add_bias;
   int64_t ab_s[4];
   uint8_t* visits;
+  int norm;    // 0 softmax, 1 ReLU (relu_attention)
 };
 
 constexpr int kBsMaxN = 65536;                       // block-sparse sequence limit

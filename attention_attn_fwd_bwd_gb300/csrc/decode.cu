@@ -26,22 +26,6 @@
 
 namespace afx {
 
-// Optional pipeline tracing (compile with -DATTNFUSE_TRACE_DEC=<split>; off by default): the CTA
-// (split, kv head 0, batch 0) records clock64() at pipeline events of its first 32 tiles; row 32
-// holds the start, q-ready and end events.
-#ifdef ATTNFUSE_TRACE_DEC
-__device__ unsigned long long g_dec_trace[33 * 8];
-#define AF_DTRACE(i, e)                                                                        \
-  do {                                                                                         \
-    if (blockIdx.x == (ATTNFUSE_TRACE_DEC) && blockIdx.y == 0 && blockIdx.z == 0 && (i) <= 32) \
-      g_dec_trace[(i) * 8 + (e)] = clock64();                                                  \
-  } while (0)
-#else
-#define AF_DTRACE(i, e) \
-  do {                  \
-  } while (0)
-#endif
-
 namespace {
 
 constexpr int kDecThreads = 128;
@@ -108,13 +92,11 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   // zero the query tile (rows >= g stay zero)
   for (int i = tid; i < (int)(C::TILE / 16); i += kDecThreads)
     reinterpret_cast<uint4*>(smem + C::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
-  if (tid == 0) AF_DTRACE(32, 0);
   if (warp == 2) tmem_alloc(&ctl->tmem_base, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
-  if (tid == 0) AF_DTRACE(32, 1);
 
   if (warp == 3) {
     // ---- query tile: row h = R_{q_pos} q[b, kvh*g + h], bf16, 128B-swizzled ----
@@ -167,7 +149,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       }
     }
     fence_proxy_async_smem();
-    if (lane == 0) AF_DTRACE(32, 2);
     mbar_arrive(&ctl->q_ready);
   } else if (warp == 1) {
     // ---- TMA producer: K then V of every tile of the chunk, through kDecST-deep rings ----
@@ -181,7 +162,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         const int st = i % kDecST;
         const uint32_t ph = ((i / kDecST) - 1) & 1;
         if (i >= kDecST && !mbar_wait(&ctl->k_empty[st], ph, status, abort_flag)) break;
-        AF_DTRACE(i, 0);
         mbar_arrive_expect_tx(&ctl->k_full[st], C::TILE);
         for (int pn = 0; pn < C::PANELS; ++pn)
           tma_load_4d_hint(smem + C::OFF_K + st * C::TILE + pn * (kDecBN * 128), &p.tmK,
@@ -213,7 +193,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       auto issue_s = [&](int i) {
         const int st = i % kDecST;
         const uint32_t d_tmem = tmem + (i & 1) * 128;
-        AF_DTRACE(i, 1);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t koff = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
@@ -236,7 +215,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         const int st = i % kDecST;
         if (!mbar_wait(&ctl->p_full, i & 1, status, abort_flag)) break;
         if (!mbar_wait(&ctl->v_full[st], (i / kDecST) & 1, status, abort_flag)) break;
-        AF_DTRACE(i, 2);
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kDecBN / 16; ++kk)
@@ -269,7 +247,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
         ok = false;
         break;
       }
-      if (lane == 0) AF_DTRACE(i, 3);
       tc_fence_after();
       uint32_t xr[kDecBN];
       tmem_ld32<0>(tS, xr);
@@ -341,7 +318,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       l_run += f2_lo(acc) + f2_hi(acc);
       m_run = m_use;
       tc_fence_before();
-      if (lane == 0) AF_DTRACE(i, 4);
       mbar_arrive(&ctl->p_full);
     }
     if (ok && ntiles > 0) {
@@ -372,7 +348,6 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
       p.part_m[part] = (ok && l_run > 0.f) ? m_run : kNegInf;
       p.part_l[part] = ok ? l_run : 0.f;
     }
-    if (lane == 0) AF_DTRACE(32, 3);
   }
   // Let the combine kernel launch while this grid drains (its reads wait for our completion).
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -505,9 +480,3 @@ extern "C" attnfuse_status attnfuse_decode_noalloc(
                          scratch, afx::kNoAllocScratchBytes, stream);
 }
 
-#ifdef ATTNFUSE_TRACE_DEC
-// Copy the decode pipeline trace (33 rows x 8 events of clock64) to host memory.
-extern "C" int attnfuse_dec_trace_read(unsigned long long* dst) {
-  return (int)cudaMemcpyFromSymbol(dst, afx::g_dec_trace, sizeof(unsigned long long) * 33 * 8);
-}
-#endif

@@ -1,6 +1,6 @@
 // Forward attention kernel for head dim 64 on sm_103a (AttnFuse paper §4.1 fused RoPE, §2
 // online softmax, §3.1 combinators, §4.3 block skipping), plus the RoPE table and pre-rotation
-// kernels. Head dim 128 runs on CTA pairs (fwd_pair.cu).
+// kernels. Head dim 128 runs on the persistent CTA-pair kernel (fwd_pp.cuh).
 //
 // One CTA computes two 128-row query sub-tiles that read the same key/value head: either two
 // query heads of one GQA group at the same positions (they then share every rotated K tile),
@@ -25,19 +25,6 @@
 
 namespace afx {
 
-// Optional pipeline tracing (compile with -DATTNFUSE_TRACE=<block index>; off by default):
-// one CTA records clock64() at each pipeline event of its first 64 kv tiles.
-#ifdef ATTNFUSE_TRACE
-__device__ unsigned long long g_fwd_trace[64 * 16];
-#define AF_TRACE(i, e)                                                   \
-  do {                                                                   \
-    if (blockIdx.x == (ATTNFUSE_TRACE) && (i) < 64) g_fwd_trace[(i) * 16 + (e)] = clock64(); \
-  } while (0)
-#else
-#define AF_TRACE(i, e) \
-  do {                 \
-  } while (0)
-#endif
 
 namespace {
 
@@ -243,7 +230,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             go = false;
             break;
           }
-          AF_TRACE(ik, 0);
           mbar_arrive_expect_tx(&ctl->k_full[s], C::TILE);
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d_hint(smem + C::OFF_K + s * C::TILE + pn * (BN * 128), &p.tmK,
@@ -257,7 +243,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             go = false;
             break;
           }
-          AF_TRACE(iv, 12);
           mbar_arrive_expect_tx(&ctl->v_full[s], C::TILE);
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d_hint(smem + C::OFF_V + s * C::TILE + pn * (BN * 128), &p.tmV,
@@ -271,17 +256,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         mbar_wait(&ctl->k_full[k % KST], (k / KST) & 1, status, nullptr);
       for (int k = max(0, iv - VST); k < iv; ++k)
         mbar_wait(&ctl->v_full[k % VST], (k / VST) & 1, status, nullptr);
-#ifdef ATTNFUSE_TRACE
-    } else if (warp == 3 && lane == 0) {
-      // trace builds only: record when each K and V copy lands
-      int i = 0;
-      for (int j = next_tile(ctl, p, jb, je); j < je; j = next_tile(ctl, p, j + 1, je), ++i) {
-        if (!mbar_wait(&ctl->k_full[i % KST], (i / KST) & 1, status, abort_flag)) break;
-        AF_TRACE(i, 14);
-        if (!mbar_wait(&ctl->v_full[i % VST], (i / VST) & 1, status, abort_flag)) break;
-        AF_TRACE(i, 15);
-      }
-#endif
     } else if (warp == 1 && lane == 0) {
       // ======================= MMA issuer =======================
       constexpr uint32_t idesc_s = idesc_f32acc(128, BN, 0, 0, RK != kRopeNone);
@@ -322,7 +296,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         if (ok) {
           for (int s = 0; s < 2; ++s)
             if (tile_active(ctl, p, s, j)) {
-              AF_TRACE(0, 3 + s);
               issue_s(s, 0);
             }
           mma_commit(&ctl->k_empty[0]);
@@ -334,12 +307,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         const int kn = (i + 1) % KST;
         bool kready = false;
         if (!mbar_wait(&ctl->v_full[vs], (i / VST) & 1, status, abort_flag)) break;
-        AF_TRACE(i, 13);
         for (int s = 0; s < 2 && ok; ++s) {
           if (tile_active(ctl, p, s, j)) {
             if (!mbar_wait(&ctl->p_full[s], cnt_pv[s] & 1, status, abort_flag)) { ok = false; break; }
             tc_fence_after();
-            AF_TRACE(i, 9 + s);
             issue_pv(s, vs, cnt_pv[s] > 0);
             ++cnt_pv[s];
             pv_pend[s] = true;
@@ -353,11 +324,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             }
             if (pv_pend[s]) {
               if (!mbar_wait(&ctl->pv_done[s], (cnt_pv[s] - 1) & 1, status, abort_flag)) { ok = false; break; }
-              if (s == 0) AF_TRACE(i, 11);
               pv_pend[s] = false;
             }
             tc_fence_after();
-            AF_TRACE(i + 1, 3 + s);
             issue_s(s, kn);
           }
         }
@@ -403,7 +372,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           }
         }
         if (!mbar_wait(&ctl->k_full[st], (i / KST) & 1, status, abort_flag)) break;
-        if (rt == 0) AF_TRACE(i, 1);
         uint8_t* tile = smem + C::OFF_K + st * C::TILE;
 #pragma unroll
         for (int k = 0; k < CP; ++k) {
@@ -426,7 +394,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           if (k + 1 < CP) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
         }
         fence_proxy_async_smem();
-        if (rt == 0) AF_TRACE(i, 2);
         mbar_arrive(&ctl->k_ready[st]);
       }
     }
@@ -504,7 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         ok = false;
         break;
       }
-      if (r == 0) AF_TRACE(n_done, 5 + 2 * s);
       tc_fence_after();
       uint32_t xr[BN];
       tmem_ld32<0>(tS, xr);
@@ -628,7 +594,6 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       l_run += sum;
       m_run = m_use;
       tc_fence_before();
-      if (r == 0) AF_TRACE(n_done, 6 + 2 * s);
       mbar_arrive(&ctl->p_full[s]);
       if (var.visits && r == 0) {
         const int TQ = (p.N + BM - 1) / BM;
@@ -735,7 +700,7 @@ __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb
 size_t fwd_smem_size(int d) { return fwd_smem_bytes(d); }
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream) {
-  if (d != 64) return cudaErrorInvalidValue;  // head dim 128 runs on CTA pairs (fwd_pair.cu)
+  if (d != 64) return cudaErrorInvalidValue;  // head dim 128 runs on the CTA-pair kernel (fwd_pp.cuh)
   const size_t smem = fwd_smem_bytes(d);
   void (*fn)(FwdParams) = rope_kind == kRopeFused        ? fwd_kernel<64, kRopeFused>
                           : rope_kind == kRopePrerotated ? fwd_kernel<64, kRopePrerotated>
@@ -780,9 +745,3 @@ cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, i
 
 }  // namespace afx
 
-#ifdef ATTNFUSE_TRACE
-// Copy the forward pipeline trace (64 tiles x 16 events of clock64) to host memory.
-extern "C" int attnfuse_trace_read(unsigned long long* dst) {
-  return (int)cudaMemcpyFromSymbol(dst, afx::g_fwd_trace, sizeof(unsigned long long) * 64 * 16);
-}
-#endif

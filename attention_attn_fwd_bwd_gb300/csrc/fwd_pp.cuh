@@ -20,7 +20,7 @@
 // Warp roles (16 warps):
 //   warp 0      TMA producer (Q per unit and slot, this CTA's halves of K and V tiles); also
 //               forwards "K / V half landed" to the even CTA (K only without fused RoPE)
-//   warps 1, 2  MMA issuer of slot 0 / slot 1 (even CTA only)
+//   warps 1, 2  MMA issuers of slot 0 / slot 1, taking turns per kv tile (even CTA only)
 //   warp 3      scheduler: per-unit metadata (tiles, ranges, block-sparse bitmaps) into a ring
 //   warps 4-7   softmax of slot 0, warps 8-11 softmax of slot 1: one query row per thread;
 //               also rotate their Q tile (fused RoPE) and write O and LSE at the end of a unit
@@ -28,6 +28,7 @@
 // Every wait is bounded (see ptx.cuh).
 #pragma once
 #include <cuda.h>
+#include <type_traits>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -80,6 +81,7 @@ struct Ctl {
   uint64_t s_full[2], o_full[2];                       // MMA commits (multicast)
   uint64_t q_ready[2], k_ready[kKSt], v_ready[kVSt], p_full[2];  // even CTA: both CTAs arrive
   uint64_t meta_full[kRing], meta_empty[kRing];
+  uint64_t tok[2];                                     // issuers' turns (even CTA)
   uint64_t mma_final;
   uint32_t tmem_base;
   int abort_flag;
@@ -298,7 +300,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->meta_full[e], 32);
       mbar_init(&ctl->meta_empty[e], consumers);
     }
-    mbar_init(&ctl->mma_final, 2);
+    mbar_init(&ctl->mma_final, 2);   // one commit per issuer
+    mbar_init(&ctl->tok[0], 1);
+    mbar_init(&ctl->tok[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -438,14 +442,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (dq && dk && dv && rv == iv && (ROPE || rk == ik)) break;
         if (moved) {
           idle = 0;
-        } else if ((++idle & 255u) == 1u) {
-          const uint64_t now = globaltimer_ns();
-          if (idle == 1u) t0 = now;
-          if (*abort_flag) break;
-          if (now - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-            atomicExch(status, kDevTimeout);
-            *abort_flag = 1;
-            break;
+        } else {
+          // nothing to do: back off briefly so the polling does not compete with the MMAs'
+          // operand reads for shared memory
+          __nanosleep(32);
+          if ((++idle & 255u) == 1u) {
+            const uint64_t now = globaltimer_ns();
+            if (idle == 1u) t0 = now;
+            if (*abort_flag) break;
+            if (now - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
+              atomicExch(status, kDevTimeout);
+              *abort_flag = 1;
+              break;
+            }
           }
         }
       }
@@ -459,36 +468,58 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(&ctl->q_full[k & 1], (k >> 1) & 1, status, nullptr);
     } else if ((warp == 1 || warp == 2) && lane == 0 && rank == 0) {
       // ======================= pair-MMA issuer of slot s =======================
-      // Per kv tile: the PV of this slot's previous tile (possibly of the previous unit),
-      // then S of this tile. Every tile of the unit is waited on (K and, when the slot skips
-      // the tile, V) and released by both issuers, so neither can run a stage ahead.
+      // Per kv tile i the issuer of slot s issues one burst: O_s += P_s V(i-1), then
+      // S_s = Q_s K(i) (that S overwrites the P the PV reads; one thread's MMAs complete in
+      // order). The two issuers take turns through the tok barriers (slot 0's burst of tile i,
+      // slot 1's of tile i, slot 0's of tile i+1, ...), so the tensor pipe sees
+      //     PV_0(i-1) S_0(i) PV_1(i-1) S_1(i) PV_0(i) S_0(i+1) ...
+      // and each slot's softmax runs while the tensor cores work on the other slot. Two
+      // threads (on different SM sub-partitions) share the MMA issue work; every barrier wait of
+      // a burst comes before its MMAs, because a shared-memory access right after an MMA stalls
+      // the issuing thread for about two MMAs.
       const int s = warp - 1;
       constexpr uint32_t idesc_s = idesc_f32acc(256, kBN, 0, 0, RK != kRopeNone);
       constexpr uint32_t idesc_o = idesc_bf16_f32(256, kD, 0, 1);
-      const uint32_t sQ = smem_u32(smem + kOffQ + s * kQTile);
-      const uint32_t sK = smem_u32(smem + kOffK);
-      const uint32_t sV = smem_u32(smem + kOffV);
+      // Descriptors as a 32-bit low word (start address >> 4, plus the leading byte offset)
+      // and one shared high word; a tile's k-steps add compile-time offsets to the low word.
+      // Every operand lies below 256 KB of shared memory, so the address field never carries.
+      static_assert(kSmem < (1u << 18), "descriptor address field");
+      constexpr uint32_t dhi = desc_sw128_hi(1024);
+      const uint32_t dQ = desc_sw128_lo(smem_u32(smem + kOffQ + s * kQTile), 16);
+      const uint32_t dK0 = desc_sw128_lo(smem_u32(smem + kOffK), 16);
+      const uint32_t dV0 = desc_sw128_lo(smem_u32(smem + kOffV), kVHalf);
       const uint32_t tS = tmem + kTmS + 128 * s, tO = tmem + kTmO + 128 * s;
       int ik = 0;          // kv tiles walked (K and V copy index)
-      int pc = 0;          // S of this slot issued (phase of s_full / p_full)
-      bool pend = false;   // a PV of this slot waits for its P
+      int pc = 0;          // S issued (phase of s_full / p_full)
+      int nb = 0;          // bursts issued (phase of the turn barrier)
+      bool pend = false;   // a PV waits for its P
       int pend_v = 0;      // its V copy index
       bool pend_acc = false, pend_last = false;
       bool ok = true;
+      // wait for this slot's turn (slot 0's first burst goes first)
+      auto take_turn = [&]() {
+        if (s == 0 && nb == 0) return;
+        ok = mbar_wait_cluster(&ctl->tok[s], (s == 0 ? nb - 1 : nb) & 1, status, abort_flag);
+      };
+      auto pass_turn = [&]() {
+        mbar_arrive(&ctl->tok[s ^ 1]);
+        ++nb;
+      };
+      // the PV of the pending tile (its P and V waited on by the caller)
       auto issue_pv = [&]() {
-        ok = mbar_wait_cluster(&ctl->p_full[s], (pc - 1) & 1, status, abort_flag) &&
-             mbar_wait_cluster(&ctl->v_ready[pend_v % kVSt], (pend_v / kVSt) & 1, status, abort_flag);
-        if (!ok) return;
-        tc_fence_after();
         const int vs = pend_v % kVSt;
+        const uint32_t bv = dV0 + vs * (kVHalf >> 4);
+        mma_ts_pair_w(tO, tS, bv, dhi, idesc_o, pend_acc ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint64_t bd = smem_desc_sw128(sV + vs * kVHalf + kk * 2048, kVHalf, 1024);
-          mma_ts_pair(tO, tS + kk * 8, bd, idesc_o, (pend_acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 1; kk < kBN / 16; ++kk)
+          mma_ts_pair_w(tO, tS + kk * 8, bv + kk * (2048 >> 4), dhi, idesc_o, 1u);
         mma_commit_pair(&ctl->v_empty[vs], 3);
         if (pend_last) mma_commit_pair(&ctl->o_full[s], 3);
         pend = false;
+      };
+      auto wait_pv_inputs = [&]() {
+        ok = mbar_wait_cluster(&ctl->p_full[s], (pc - 1) & 1, status, abort_flag) &&
+             mbar_wait_cluster(&ctl->v_ready[pend_v % kVSt], (pend_v / kVSt) & 1, status, abort_flag);
       };
       for (int u = 0; ok; ++u) {
         const int e = u % kRing;
@@ -496,35 +527,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const UnitMeta& M = ctl->ring[e];
         if (!M.live) break;
-        // the previous unit's last PV first: its softmax waits for it before this unit's Q
-        if (pend) {
-          issue_pv();
-          if (!ok) break;
-        }
-        ok = mbar_wait_cluster(&ctl->q_ready[s], u & 1, status, abort_flag);
-        if (!ok) break;
-        const int ns = M.ns[s];
+        const int jb = M.jb, je = M.je, ns = M.ns[s], slo = M.slo[s], shi = M.shi[s];
         int cnt = 0;
-        if (ns == 0) {
-          mma_commit_pair(&ctl->q_empty[s], 3);
-          mma_commit_pair(&ctl->o_full[s], 3);
-        }
-        for (int j = M.jb; ok && j < M.je; j = next_tile(M, bs, j), ++ik) {
+        bool opened = false;
+        // First use of the slot in this unit: the previous unit's last PV (its softmax waits
+        // for that O before this unit's epilogue), then this unit's rotated Q.
+        auto open_slot = [&]() {
           if (pend) {
-            issue_pv();
-            if (!ok) break;
-          }
-          const int st = ik % kKSt;
-          ok = mbar_wait_cluster(&ctl->k_ready[st], (ik / kKSt) & 1, status, abort_flag);
-          if (!ok) break;
-          if (slot_act(M, bs, s, j)) {
+            wait_pv_inputs();
+            if (!ok) return;
             tc_fence_after();
+            issue_pv();
+          }
+          ok = mbar_wait_cluster(&ctl->q_ready[s], u & 1, status, abort_flag);
+          if (ok && ns == 0) {
+            mma_commit_pair(&ctl->q_empty[s], 3);
+            mma_commit_pair(&ctl->o_full[s], 3);
+          }
+          opened = true;
+        };
+        for (int j = jb; ok && j < je; j = next_tile(M, bs, j), ++ik) {
+          const bool a = bs ? pbit(M.sbits[s], j) : (j >= slo && j < shi);
+          const int st = ik % kKSt;
+          // ---- all waits of the burst ----
+          take_turn();
+          if (ok && !opened) open_slot();
+          if (ok && pend) wait_pv_inputs();
+          if (ok) ok = mbar_wait_cluster(&ctl->k_ready[st], (ik / kKSt) & 1, status, abort_flag);
+          if (ok && !a) ok = mbar_wait_cluster(&ctl->v_ready[ik % kVSt], (ik / kVSt) & 1, status, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          // ---- MMAs ----
+          if (pend) issue_pv();
+          if (a) {
+            const uint32_t bk = dK0 + st * (kKHalf >> 4);
+            mma_ss_pair_w<0>(tS, dQ, bk, dhi, idesc_s);
 #pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(sQ + (kk >> 2) * (kBM * 128) + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(sK + st * kKHalf + (kk >> 2) * (64 * 128) + (kk & 3) * 32, 16, 1024);
-              mma_ss_pair(tS, ad, bd, idesc_s, kk > 0);
-            }
+            for (int kk = 1; kk < kD / 16; ++kk)
+              mma_ss_pair_w<1>(tS, dQ + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4),
+                               bk + (((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4), dhi, idesc_s);
             mma_commit_pair(&ctl->s_full[s], 3);
             ++pc;
             ++cnt;
@@ -534,17 +575,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pend_acc = cnt > 1;
             pend_last = cnt == ns;
           } else {
-            // no PV of this slot reads V(ik): release it once it has landed
-            ok = mbar_wait_cluster(&ctl->v_ready[ik % kVSt], (ik / kVSt) & 1, status, abort_flag);
-            if (!ok) break;
+            // no PV of this slot reads V(ik)
             mma_commit_pair(&ctl->v_empty[ik % kVSt], 3);
           }
           mma_commit_pair(&ctl->k_empty[st], 3);
+          pass_turn();
         }
+        if (ok && !opened) open_slot();
         if (ok) mbar_arrive(&ctl->meta_empty[e]);
       }
-      if (ok && pend) issue_pv();
-      // All MMAs of both issuers must finish before TMEM is released.
+      if (ok && pend) {
+        wait_pv_inputs();
+        if (ok) {
+          tc_fence_after();
+          issue_pv();
+        }
+      }
+      // All MMAs must finish before TMEM is released.
       mma_commit_pair(&ctl->mma_final, 3);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
     }
@@ -658,10 +705,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* const visits = var.visits;
     int sc = 0;  // S of this slot consumed (phase of s_full)
     bool ok = true;
+    // Q' = R_m Q of unit un in place (fp16 with fused RoPE), then the slot's MMAs may read it.
+    auto prep_q = [&](const UnitMeta& Mq, int un) {
+      const int qq0 = Mq.q0[s][rank];
+      const bool qvalid = Mq.qv[s][rank] != 0;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full[s], un & 1, status, abort_flag));
+      if (!ok) return;
+      if (ROPE && qvalid) {
+        // Warp wq rotates the rows of two query-tile recurrence chains (query_cs8): rows
+        // wq + 8k and wq + 4 + 8k, each starting from its table entry and stepping 8 positions.
+        // Lane f takes dims 2f, 2f+1 and their partners 64+2f, 64+2f+1 (one 16-byte table read
+        // per row start).
+        const uint64_t pol_tab = l2_policy_evict_last();
+        const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
+        const float4 wstep = ldg_f4_hint(tab + (size_t)8 * (kD / 4) + lane, pol_tab);
+        uint8_t* tile = smem + kOffQ + s * kQTile;
+        const uint32_t within = static_cast<uint32_t>(lane & 3) * 4u;
+#pragma unroll
+        for (int ch = 0; ch < 2; ++ch) {
+          const int c0 = wq + 4 * ch;
+          float4 cs = ldg_f4_hint(tab + (size_t)min(qq0 + c0, N - 1) * (kD / 4) + lane, pol_tab);
+#pragma unroll 4
+          for (int k = 0; k < kBM / 8; ++k) {
+            const int rr = c0 + 8 * k;
+            if (qq0 + rr < N) {
+              const uint32_t off = sw128_offset(rr, lane >> 2) + within;
+              const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + off);
+              const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + kBM * 128 + off);
+              float yl0, yh0, yl1, yh1;
+              rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
+              rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
+              *reinterpret_cast<uint32_t*>(tile + off) = pack_f16x2_sat(yl0, yl1);
+              *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = pack_f16x2_sat(yh0, yh1);
+            }
+            float c0f, s0f, c1f, s1f;
+            rot_pair(cs.x, cs.y, wstep.x, wstep.y, c0f, s0f);
+            rot_pair(cs.z, cs.w, wstep.z, wstep.w, c1f, s1f);
+            cs = make_float4(c0f, s0f, c1f, s1f);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) arrive_leader(&ctl->q_ready[s], rank);
+    };
+    {
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->meta_full[0], 0, status, abort_flag));
+      if (ok && ctl->ring[0].live) prep_q(ctl->ring[0], 0);
+    }
     for (int u = 0; ok; ++u) {
       const int e = u % kRing;
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->meta_full[e], (u / kRing) & 1, status, abort_flag));
-      if (!ok) break;
       const UnitMeta& M = ctl->ring[e];
       if (!M.live) break;
       const int b = M.b;
@@ -685,47 +778,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       const bool bs64 = bs && var.bs_block == 64;
       const int blk_row = bs64 ? (r >> 6) : 0;
-
-      // ---- Q' = R_m Q in place (fp16), then the slot's MMAs may read it ----
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full[s], u & 1, status, abort_flag));
-      if (!ok) break;
-      if (ROPE && valid) {
-        // Warp wq rotates the rows of two query-tile recurrence chains (query_cs8): rows
-        // wq + 8k and wq + 4 + 8k, each starting from its table entry and stepping 8 positions.
-        // Lane f takes dims 2f, 2f+1 and their partners 64+2f, 64+2f+1 (one 16-byte table read
-        // per row start).
-        const uint64_t pol_tab = l2_policy_evict_last();
-        const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
-        const float4 wstep = ldg_f4_hint(tab + (size_t)8 * (kD / 4) + lane, pol_tab);
-        uint8_t* tile = smem + kOffQ + s * kQTile;
-        const uint32_t within = static_cast<uint32_t>(lane & 3) * 4u;
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          const int c0 = wq + 4 * ch;
-          float4 cs = ldg_f4_hint(tab + (size_t)min(q0 + c0, N - 1) * (kD / 4) + lane, pol_tab);
-#pragma unroll 4
-          for (int k = 0; k < kBM / 8; ++k) {
-            const int rr = c0 + 8 * k;
-            if (q0 + rr < N) {
-              const uint32_t off = sw128_offset(rr, lane >> 2) + within;
-              const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + off);
-              const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + kBM * 128 + off);
-              float yl0, yh0, yl1, yh1;
-              rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
-              rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
-              *reinterpret_cast<uint32_t*>(tile + off) = pack_f16x2_sat(yl0, yl1);
-              *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = pack_f16x2_sat(yh0, yh1);
-            }
-            float c0f, s0f, c1f, s1f;
-            rot_pair(cs.x, cs.y, wstep.x, wstep.y, c0f, s0f);
-            rot_pair(cs.z, cs.w, wstep.z, wstep.w, c1f, s1f);
-            cs = make_float4(c0f, s0f, c1f, s1f);
-          }
-        }
-        fence_proxy_async_smem();
-      }
-      __syncwarp();
-      if (lane == 0) arrive_leader(&ctl->q_ready[s], rank);
 
       // ---- kv tiles of the slot ----
       const float alibi = (BIAS == 1 && valid) ? var.slopes[head] * bias_u : 0.f;
@@ -843,7 +895,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t a = fma2(f2_pack(x[2 * c], x[2 * c + 1]), mul2v, nb2);
             const float p0 = ex2_approx(f2_lo(a)), p1 = ex2_approx(f2_hi(a));
             acc2[c & 3] = add2(acc2[c & 3], f2_pack(p0, p1));
-            pk[c] = pack_bf16x2(p0, p1);
+            pk[c] = pack_bf16x2_alu(p0, p1);
           }
           const uint64_t acc = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
           l_run += f2_lo(acc) + f2_hi(acc);
@@ -861,6 +913,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
+      // ---- the next unit's Q first: its copy and rotation overlap this unit's last PV, and
+      // the issuer can start the next unit's S while this unit's O is written out ----
+      const int en = (u + 1) % kRing;
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->meta_full[en], ((u + 1) / kRing) & 1, status, abort_flag));
+      if (!ok) break;
+      const bool more = ctl->ring[en].live != 0;
+      if (more) {
+        prep_q(ctl->ring[en], u + 1);
+        if (!ok) break;
+      }
       // ---- epilogue: O / l and LSE once the slot's last PV has completed ----
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[s], u & 1, status, abort_flag));
       if (!ok) break;
@@ -899,6 +961,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->meta_empty[e]);
+      if (!more) break;
     }
   }
 

@@ -16,7 +16,7 @@ struct FwdParams {
   int64_t o_sb, o_sh, o_sn;
   float* lse;                 // [B, Hq, N] or null
   int B, Hq, Hkv, N, g;
-  int pair_heads;             // 1: sub-tiles are heads (2p, 2p+1) at one q tile; 0: tiles (2t, 2t+1)
+  int pair_heads;             // head dim 64: 1: sub-tiles are heads (2p, 2p+1) at one q tile; 0: tiles (2t, 2t+1)
   int num_t;                  // q tiles (pair_heads) or q-tile pairs
   int pairs;                  // head pairs (Hq/2) or heads (Hq)
   float scale_log2;           // scale * log2(e)
@@ -63,6 +63,8 @@ struct BwdParams {
   float* dbias;                     // additive bias only: dBias [B, Hq, N, N] fp32, or null
   int64_t db_s[3];                  // its (b, h, m) element strides; the key stride is 1
   int db_vec2;                      // 1: pointer and strides allow 8-byte pair stores
+  uint8_t* visits_dq;               // debug record of the dQ kernel's (q tile, key tile) pairs
+  uint8_t* visits_kv;               // and of the dK/dV kernel's (64-row query item, key tile)
   int* status;
 };
 // rope_kind: kRopeNone, kRopeFused (Q / K tiles rotated on chip) or kRopePrerotated (tmQ /
@@ -79,9 +81,6 @@ constexpr int kRopeFused = 1;       // rotated in shared memory by the kernel, r
 constexpr int kRopePrerotated = 2;  // rotated by the pre-rotation kernel into fp16 buffers
 // One CTA per 256 query rows (two 128-row sub-tiles); head dim 64.
 cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream);
-// Head dim 128: clusters of two CTAs, one per 256 query rows (tmK box of 64 rows).
-size_t fwd_pair_smem_size();
-cudaError_t launch_fwd_pair(const FwdParams& p, int rope_kind, int clusters, cudaStream_t stream);
 // Head dim 128, persistent: clusters of two CTAs walk units of four 128-row query tiles of
 // one KV head (two independent softmax slots per CTA). norm: 0 softmax, 1 ReLU (P = relu(s)/N).
 size_t fwd_pp_smem_size();

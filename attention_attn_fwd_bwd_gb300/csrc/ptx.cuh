@@ -119,15 +119,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if ((++spins & 255u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-#ifdef ATTNFUSE_WAIT_DIAG
-        // diagnostic builds: the first timeout records where it happened (CTA, warp,
-        // barrier word, parity) instead of the plain code
-        if (status)
-          atomicCAS(status, 0, (int)(0x40000000u | ((a >> 3) & 0x3fffu) | ((threadIdx.x >> 5) << 14) |
-                                     (parity << 18) | (min(blockIdx.x, 2047u) << 19)));
-#else
         if (status) atomicExch(status, kDevTimeout);
-#endif
         if (abort_flag) *abort_flag = 1;
         return false;
       }
@@ -397,6 +389,42 @@ __device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// Shared-memory descriptors split into their two 32-bit words: the low word holds the start
+// address (bits 0-13, address >> 4) and the leading byte offset (bits 16-29); the high word the
+// stride byte offset, the descriptor version and the swizzle mode. Operands of one kind share
+// the high word, and stepping through a tile only adds to the low word, so an issuing thread
+// keeps one 32-bit base per operand and adds a compile-time offset per MMA.
+__host__ __device__ constexpr uint32_t desc_sw128_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
+__device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+
+// Pair MMAs taking split descriptors (see above); ACC: accumulate into D (1) or overwrite (0).
+template <int ACC>
+__device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 a, {%1, %3};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
+                                              uint32_t hi, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(hi), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // D[tmem] (+)= A[tmem] * B[smem desc], both CTAs of the pair.
 __device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
@@ -420,6 +448,19 @@ __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask
 
 __device__ __forceinline__ void tmem_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+// tcgen05.wait::ld that also names the 32 registers a preceding tcgen05.ld wrote, so the
+// compiler cannot move their uses above the wait.
+__device__ __forceinline__ void tmem_wait_ld_dep(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]),
+                 "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]),
+                 "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]),
+                 "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]),
+                 "+r"(r[31])
+               :
+               : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -527,6 +568,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
+}
+
+// Two finite, non-negative floats to bf16 (nearest, ties away from zero) with integer
+// operations only: add half a bf16 unit to the bit pattern and keep the top 16 bits. Runs on
+// the integer pipe, leaving the conversion pipe (shared with ex2) to the exponentials.
+__device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
 }
 
 // Round two floats to fp16, saturating to the largest finite value instead of overflowing.

@@ -54,6 +54,8 @@ def parse():
     ap.add_argument("--decode", action="store_true",
                     help="split-KV decode at the Llama-3-70B head shape (B=1, 8; splits sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the nested records of the other workloads and the steady-state run")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
     ap.add_argument("--profile-target", default="fwd",
@@ -147,7 +149,7 @@ class ClockSampler:
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "attention_attn_fwd_bwd_gb300", "csrc")
-    for name in ("fwd_pair.cu", "ptx.cuh", "common.cuh", "launch.h"):
+    for name in ("fwd_pp.cuh", "fwd_pp.cu", "ptx.cuh", "common.cuh", "launch.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -202,6 +204,66 @@ class OracleSampler:
         return flops / secs / 1e12, rows, secs
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu model")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def steady_state(step, stream, local, flops, ms_per_step):
+    """The headline step repeated for at least ~1.2 s (clocks sampled throughout): a steadier
+    number than the driver's short timed region, reported beside it."""
+    import torch
+
+    n = max(1000, int(1.2e3 / max(ms_per_step, 1e-3)))
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"steps": n, "ms_per_step": ms, "value": flops / (ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+            "clocks": clocks.stop()}
+
+
+def secondary_configs(args, local):
+    """The other workloads of the target, each with its own clock record: the mask variants
+    (B=2, H=16, N=4096, d=64: window 1024 + causal, ALiBi + causal, BigBird, causal), the
+    training step (B=8, Hq=32, Hkv=8, d=128, N=2048 and 4096: forward, backward fused and
+    pre-rotated), the Llama-3-70B-shaped split-KV decode (B=1 and 8, splits auto/1/8/32/128,
+    cold and warm L2) and the fused / pre-rotated crossover sweep of the head-dim-128 forward
+    (B*N = 16384, N = 256 .. 16384)."""
+    out = {}
+    for key, fn in (("mask_variants_d64", lambda: run_variants_bench(args, emit=False)),
+                    ("training_fwd_bwd", lambda: run_train_bench(args, emit=False)),
+                    ("decode_llama70b_head_shape", lambda: run_decode_bench(args, emit=False)),
+                    ("rotation_calculus_d128", lambda: run_sweep(args, quick=True, emit=False))):
+        clk = ClockSampler(local)
+        clk.start()
+        time.sleep(0.2)
+        t0 = time.perf_counter()
+        rows = fn()
+        out[key] = {"rows": rows, "clocks": clk.stop(), "wall_s": round(time.perf_counter() - t0, 1)}
+    return out
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return
@@ -222,7 +284,7 @@ def run_reference(args, rank, world):
         "data": "synthetic",
         "config": workload_config(args.workload),
         "cpu_baseline": {"value": tflops, "unit": "TFLOP/s", "cores": os.cpu_count(),
-                         "kind": "oracle",
+                         "cpu_model": cpu_model(), "kind": "oracle",
                          "sample": f"{batch} full query rows of the workload per step (fp64 "
                                    f"oracle, rows drawn uniformly over (b, h, m))"},
         "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -340,6 +402,10 @@ def run_ours(args, rank, world):
 
     if rank != 0:
         return
+    steady = configs = None
+    if world == 1 and not args.no_configs:
+        steady = steady_state(step, stream, local, flops, ms_per_step)
+        configs = secondary_configs(args, local)
     peaks, src = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     roof = None
@@ -347,14 +413,15 @@ def run_ours(args, rank, world):
         ach = flops / (kern_ms * 1e-3) / 1e12
         roof = {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s",
                 "frac": ach / peak, "traffic": committed_traffic(args.workload),
-                "kernel": "fwd_pair_kernel<fused RoPE, no bias> (2-CTA cluster)", "kernel_ms": kern_ms,
+                "kernel": "fwd_pp_kernel<fused RoPE, no bias, softmax> (persistent 2-CTA clusters)", "kernel_ms": kern_ms,
                 "peak_source": f"{src} bf16 burst (MEASURED_PEAKS.json)" if src == "measured" else "fallback",
                 "frac_of_sustained": ach / float(peaks.get("bf16_tflops_sustained", peak))}
     cpu = None
     if not args.no_cpu_baseline:
         smp = OracleSampler(B, Hq, Hkv, N, d, theta, mode != "none", seed=2000)
         tf, rows, secs = smp.timed(budget_s=12.0, batch=os.cpu_count() or 8)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "kind": "oracle",
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": os.cpu_count(), "cpu_model": cpu_model(),
+               "kind": "oracle",
                "sample": f"{rows} full query rows of the workload (fp64 oracle, {secs:.1f} s), "
                          f"rows drawn uniformly over (b, h, m); value = their causal FLOPs / time"}
     line = {
@@ -365,6 +432,7 @@ def run_ours(args, rank, world):
         "pct_of_peak": 100.0 * value / world / peak,
         "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clk,
+        "steady_state": steady, "configs": configs,
     }
     print(json.dumps(line), flush=True)
 
@@ -396,9 +464,11 @@ def _crossover(res, key):
     return None
 
 
-def run_sweep(args):
+def run_sweep(args, quick=False, emit=True):
     """The Rotation Calculus on GB300: fused vs pre-rotated vs no RoPE over N at B*N = 16384
-    tokens, forward for head dims 128 (Hq=32, Hkv=8) and 64 (H=16), and the d=128 backward."""
+    tokens, forward for head dims 128 (Hq=32, Hkv=8) and 64 (H=16), and the d=128 backward.
+    quick: the head-dim-128 forward only (the default run's nested record). Returns the rows
+    and the crossover records."""
     import torch
 
     import attention_attn_fwd_bwd_gb300 as af
@@ -406,11 +476,12 @@ def run_sweep(args):
 
     dev = torch.device("cuda")
     theta = 5e5
-    for d, Hq, Hkv in ((128, 32, 8), (64, 16, 16)):
+    rows_all = []
+    for d, Hq, Hkv in ((128, 32, 8),) if quick else ((128, 32, 8), (64, 16, 16)):
         res = []
         for N in (256, 512, 1024, 2048, 4096, 8192, 16384):
             B = 16384 // N
-            x = inputs.prefill(B, Hq, Hkv, N, d, seed=N, with_dout=(N <= 4096))
+            x = inputs.prefill(B, Hq, Hkv, N, d, seed=N, with_dout=(N <= 4096 and not quick))
             q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
             out = torch.empty_like(q)
             lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
@@ -438,13 +509,18 @@ def run_sweep(args):
                 row.update({"bwd_fused_ms": bt["fused"], "bwd_prerotate_ms": bt["prerotate"],
                             "bwd_fused_over_prerotate": bt["prerotate"] / bt["fused"]})
             res.append(row)
-            print(json.dumps({"sweep": "rotation_calculus", **row}), flush=True)
+            if emit:
+                print(json.dumps({"sweep": "rotation_calculus", **row}), flush=True)
         bwd_rows = [r for r in res if "bwd_fused_over_prerotate" in r]
-        print(json.dumps({"sweep": "rotation_calculus_crossover", "d": d,
-                          "N_star_fwd": _crossover(res, "fused_over_prerotate"),
-                          "N_star_bwd": _crossover(bwd_rows, "bwd_fused_over_prerotate") if bwd_rows else None,
-                          "note": "speedup = t_prerotate / t_fused; >1 means fusion wins; "
-                                  "None: no crossing inside the measured N"}), flush=True)
+        cross = {"sweep": "rotation_calculus_crossover", "d": d,
+                 "N_star_fwd": _crossover(res, "fused_over_prerotate"),
+                 "N_star_bwd": _crossover(bwd_rows, "bwd_fused_over_prerotate") if bwd_rows else None,
+                 "note": "speedup = t_prerotate / t_fused; >1 means fusion wins; "
+                         "None: no crossing inside the measured N"}
+        if emit:
+            print(json.dumps(cross), flush=True)
+        rows_all += res + [cross]
+    return rows_all
 
 
 def run_profile(args):
@@ -504,7 +580,7 @@ def _time_ms(fn, reps=20, warm=3):
     return samples[len(samples) // 2], samples[0], samples[int(0.9 * len(samples))]
 
 
-def run_train_bench(args):
+def run_train_bench(args, emit=True):
     """Training-step attention: fused-RoPE causal forward (O, LSE) and the 3-kernel backward."""
     import torch
 
@@ -515,6 +591,7 @@ def run_train_bench(args):
     peaks, _ = measured_peaks()
     peak = float(peaks["bf16_tflops"])
     B, Hq, Hkv, d, theta = 8, 32, 8, 128, 5e5
+    rows = []
     for N in (2048, 4096):
         x = inputs.prefill(B, Hq, Hkv, N, d, seed=4000 + N, with_dout=True)
         q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
@@ -531,7 +608,7 @@ def run_train_bench(args):
         tb, tb_min, tb_p90 = _time_ms(bwd)
         tbp, _, _ = _time_ms(bwd_pre)
         fl = causal_flops(B, Hq, N, d)
-        print(json.dumps({"train": "fused_rope_causal", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
+        rows.append({"train": "fused_rope_causal", "B": B, "Hq": Hq, "Hkv": Hkv, "N": N, "d": d,
                           "fwd_ms": tf, "bwd_ms": tb, "fwd_tflops": fl / tf / 1e9,
                           "bwd_tflops": 2.5 * fl / tb / 1e9,
                           "total_tflops": 3.5 * fl / (tf + tb) / 1e9,
@@ -539,7 +616,10 @@ def run_train_bench(args):
                           "total_frac_of_peak": 3.5 * fl / (tf + tb) / 1e9 / peak,
                           "fwd_min_p90_ms": [tf_min, tf_p90], "bwd_min_p90_ms": [tb_min, tb_p90],
                           "bwd_prerotate_ms": tbp, "bwd_prerotate_tflops": 2.5 * fl / tbp / 1e9,
-                          "launches": {"fwd": 2, "bwd": 4, "bwd_prerotate": 6}}), flush=True)
+                          "launches": {"fwd": 2, "bwd": 4, "bwd_prerotate": 6}})
+        if emit:
+            print(json.dumps(rows[-1]), flush=True)
+    return rows
 
 
 def allowed_pairs(N, mask, causal=False, window=0, row_ptr=None, col_idx=None, blk=64):
@@ -571,7 +651,7 @@ def allowed_pairs(N, mask, causal=False, window=0, row_ptr=None, col_idx=None, b
     return total
 
 
-def run_variants_bench(args):
+def run_variants_bench(args, emit=True):
     """Mask-variant forwards at B=2, H=16, N=4096, d=64, theta=1e4, fused RoPE."""
     import torch
 
@@ -597,6 +677,7 @@ def run_variants_bench(args):
         "causal": (af.Variant(mask=af.MASK_CAUSAL), allowed_pairs(N, "causal")),
     }
     do = inputs.prefill(B, H, H, N, d, seed=3000, with_dout=True)["dout"].to(dev)
+    rows = []
     for name, (gvar, pairs) in cases.items():
         ws = torch.empty(af.fwd_workspace_size(B, H, H, N, d, af.ROPE_FUSED), dtype=torch.uint8, device=dev)
         out = torch.empty_like(q)
@@ -608,13 +689,16 @@ def run_variants_bench(args):
         tb, _, _ = _time_ms(lambda: af.bwd(q, k, v, out, lse, do, rope_theta=1e4, variant=gvar,
                                            dq=dq, dk=dk, dv=dv, workspace=wsb))
         fl = 4.0 * d * B * H * pairs
-        print(json.dumps({"variant": name, "B": B, "H": H, "N": N, "d": d, "ms": t, "min_ms": tmin,
+        rows.append({"variant": name, "B": B, "H": H, "N": N, "d": d, "ms": t, "min_ms": tmin,
                           "p90_ms": tp90, "allowed_pairs_per_head": pairs,
                           "algorithmic_tflops": fl / t / 1e9,
                           "frac_of_peak": fl / t / 1e9 / float(peaks["bf16_tflops"]),
                           "bwd_ms": tb, "bwd_algorithmic_tflops": 2.5 * fl / tb / 1e9,
                           **({"active_blocks": int(len(ci)), "active_fraction": len(ci) / (N // 64) ** 2}
-                             if name.startswith("bigbird") else {})}), flush=True)
+                             if name.startswith("bigbird") else {})})
+        if emit:
+            print(json.dumps(rows[-1]), flush=True)
+    return rows
 
 
 def _graph_of(fn):
@@ -714,7 +798,7 @@ def run_tables_bench(args):
                               "frac_of_hbm_graph": nbytes / (medg * 1e-6) / 1e9 / float(peaks["hbm_gbs"])}), flush=True)
 
 
-def run_decode_bench(args):
+def run_decode_bench(args, emit=True):
     """Split-KV decode: Hq=64, Hkv=8, d=128, L=32768, q at 32767; K+V bytes / time (cold L2)."""
     import torch
 
@@ -725,6 +809,7 @@ def run_decode_bench(args):
     peaks, src = measured_peaks()
     Hq, Hkv, d, L = 64, 8, 128, 32768
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x the L2
+    rows = []
     for B in (1, 8):
         x = inputs.decode(B, Hq, Hkv, L, d, seed=5000 + B)
         q, kc, vc = (x[n].to(dev) for n in ("q", "k_cache", "v_cache"))
@@ -755,14 +840,17 @@ def run_decode_bench(args):
             med = res["cold"][len(res["cold"]) // 2]
             gbs = nbytes / (med * 1e-6) / 1e9
             used = splits if splits else af.decode_auto_splits(B, Hkv, L)
-            print(json.dumps({"decode": "llama70b_head_shape", "B": B, "splits": splits,
+            rows.append({"decode": "llama70b_head_shape", "B": B, "splits": splits,
                               "splits_used": used, "us_median_cold_l2": med,
                               "us_min_cold_l2": res["cold"][0],
                               "us_p90_cold_l2": res["cold"][int(0.9 * len(res["cold"]))],
                               "us_median_warm_l2": res["warm"][len(res["warm"]) // 2],
                               "kv_bytes": nbytes, "gbs_cold": gbs,
                               "frac_of_hbm": gbs / float(peaks["hbm_gbs"]),
-                              "launches": 2}), flush=True)
+                              "launches": 2})
+            if emit:
+                print(json.dumps(rows[-1]), flush=True)
+    return rows
 
 
 def main():

@@ -90,7 +90,19 @@ typedef enum {
   ATTNFUSE_BIAS_ADDITIVE = 2
 } attnfuse_bias_kind;
 
-/* A variant: one mask combinator, an optional causal restriction and one bias combinator.
+/* Normaliser combinators (paper §3.1 softmax / relu_attention). The pages name relu_attention
+ * without defining it; this library reads it as ReLU attention divided by the sequence length:
+ *   O_m = (1/N) sum_{allowed n} max(s_mn, 0) v_n.
+ * It has no log-sum-exp (lse must be NULL) and no backward (attnfuse_bwd returns
+ * ATTNFUSE_ERR_UNSUPPORTED); the forward supports it for head dim 128 with every mask, bias
+ * and rope mode. */
+typedef enum {
+  ATTNFUSE_NORM_SOFTMAX = 0,
+  ATTNFUSE_NORM_RELU = 1
+} attnfuse_normalizer;
+
+/* A variant: one mask combinator, an optional causal restriction, one bias combinator and the
+ * row normaliser.
  * All pointers are device pointers owned by the caller; unused fields are ignored. */
 typedef struct {
   int32_t mask;                /* attnfuse_mask_kind */
@@ -114,6 +126,13 @@ typedef struct {
                                   bias broadcasts to obtain its own gradient). Every element is
                                   written, 0 where (m, n) is masked. 4-byte aligned. */
   int64_t dbias_strides[4];    /* element strides of dbias: (b, h, m) any, n == 1 */
+  int32_t normalizer;          /* attnfuse_normalizer: the row normaliser (0 = softmax) */
+  uint8_t* bwd_dq_visits;      /* debug, nullable: [B, Hq, ceil(N/128), ceil(N/128)] bytes; the
+                                  backward's dQ kernel writes 1 for every (query tile, key tile)
+                                  it computes. The caller zeroes it first. */
+  uint8_t* bwd_dkdv_visits;    /* debug, nullable: [B, Hq, ceil(N/64), ceil(N/128)] bytes; the
+                                  dK/dV kernel writes 1 for every (64-row query block of head h,
+                                  key tile) it computes. The caller zeroes it first. */
 } attnfuse_variant;
 
 /* Last error message of this thread (empty string if none). */

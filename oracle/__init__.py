@@ -29,6 +29,7 @@ _lib = None
 
 MASK_FULL, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK_SPARSE = 0, 1, 2, 3
 BIAS_NONE, BIAS_ALIBI, BIAS_ADDITIVE = 0, 1, 2
+NORM_SOFTMAX, NORM_RELU = 0, 1
 
 
 def build(force: bool = False) -> str:
@@ -53,7 +54,7 @@ class _Variant(ctypes.Structure):
         ("bs_row_ptr", ctypes.c_void_p),
         ("bs_col_idx", ctypes.c_void_p),
         ("bias", ctypes.c_int32),
-        ("pad_", ctypes.c_int32),
+        ("norm", ctypes.c_int32),
         ("slopes", ctypes.c_void_p),
         ("add_bias", ctypes.c_void_p),
         ("add_bias_strides", ctypes.c_int64 * 4),
@@ -90,11 +91,13 @@ class Variant:
     mask: MASK_FULL / MASK_CAUSAL / MASK_WINDOW / MASK_BLOCK_SPARSE; causal: extra n <= m;
     window: W; bs_row_ptr / bs_col_idx: CSR of active blocks (block edge bs_block);
     bias: BIAS_NONE / BIAS_ALIBI (slopes, one per query head) / BIAS_ADDITIVE (add_bias,
-    any array broadcastable to [B, Hq, N, N]).
+    any array broadcastable to [B, Hq, N, N]); norm: NORM_SOFTMAX or NORM_RELU (relu_attention,
+    O_m = (1/N) sum_n max(s_mn, 0) v_n over the allowed keys; forward only, LSE is NaN).
     """
 
     def __init__(self, mask=MASK_CAUSAL, causal=False, window=0, bs_block=64, bs_row_ptr=None,
-                 bs_col_idx=None, bias=BIAS_NONE, slopes=None, add_bias=None):
+                 bs_col_idx=None, bias=BIAS_NONE, slopes=None, add_bias=None, norm=0):
+        self.norm = norm
         self.mask, self.causal, self.window, self.bs_block = mask, bool(causal), window, bs_block
         self.bs_row_ptr = None if bs_row_ptr is None else np.ascontiguousarray(bs_row_ptr, np.int32)
         self.bs_col_idx = None if bs_col_idx is None else np.ascontiguousarray(bs_col_idx, np.int32)
@@ -110,6 +113,7 @@ class Variant:
             v.bs_row_ptr = self.bs_row_ptr.ctypes.data
             v.bs_col_idx = self.bs_col_idx.ctypes.data
         v.bias = self.bias
+        v.norm = self.norm
         if self.bias == BIAS_ALIBI:
             v.slopes = self.slopes.ctypes.data
         if self.bias == BIAS_ADDITIVE:

@@ -30,6 +30,10 @@
  *   - ALiBi bias = slope_h * (n - m), slopes supplied by the caller (one per query head).
  *   - GQA: query head h reads key/value head h / (Hq / Hkv).
  *   - a row with no allowed key: O = 0, LSE = -inf.
+ *   - relu_attention (§3.1 names this normaliser without defining it): the softmax is replaced
+ *     by O_m = (1/N) sum_{allowed n} max(s_mn, 0) v_n, N the number of keys (the sequence
+ *     length), as in ReLU attention divided by the sequence length; there is no LSE (NaN is
+ *     returned) and no backward.
  * All tensors are contiguous row-major [B, H, N, d] fp64 unless stated.
  */
 #include <math.h>
@@ -39,6 +43,7 @@
 
 enum { ORC_MASK_FULL = 0, ORC_MASK_CAUSAL = 1, ORC_MASK_WINDOW = 2, ORC_MASK_BLOCK_SPARSE = 3 };
 enum { ORC_BIAS_NONE = 0, ORC_BIAS_ALIBI = 1, ORC_BIAS_ADDITIVE = 2 };
+enum { ORC_NORM_SOFTMAX = 0, ORC_NORM_RELU = 1 };
 
 typedef struct {
   int32_t mask;       /* ORC_MASK_* */
@@ -48,7 +53,7 @@ typedef struct {
   const int32_t* bs_row_ptr; /* CSR over block rows: [ceil(N/bs_block) + 1] */
   const int32_t* bs_col_idx; /* active block columns of each block row */
   int32_t bias;       /* ORC_BIAS_* */
-  int32_t pad_;
+  int32_t norm;       /* ORC_NORM_*: the row normaliser */
   const double* slopes;      /* [Hq] for ORC_BIAS_ALIBI */
   const double* add_bias;    /* additive bias, element (b,h,m,n) at the strides below */
   int64_t add_bias_strides[4];
@@ -134,6 +139,15 @@ static double row_forward(const orc_variant* var, int64_t b, int64_t h, int64_t 
     if (s[n] > mx) mx = s[n];
   }
   for (int c = 0; c < d; ++c) o[c] = 0.0;
+  if (var->norm == ORC_NORM_RELU) {
+    /* relu_attention: weights max(s, 0) / N, no exponent and no row sum */
+    for (int64_t n = 0; n < N; ++n) {
+      p[n] = (s[n] == -INFINITY || s[n] <= 0.0) ? 0.0 : s[n] / (double)N;
+      if (p[n] != 0.0)
+        for (int c = 0; c < d; ++c) o[c] += p[n] * vh[n * d + c];
+    }
+    return NAN;
+  }
   if (mx == -INFINITY) {
     for (int64_t n = 0; n < N; ++n) p[n] = 0.0;
     return -INFINITY;
@@ -263,6 +277,7 @@ int orc_bwd(const double* q, const double* k, const double* v, const double* dou
             int Hkv, int64_t N, int d, double scale, double theta, int rope,
             const orc_variant* var, int64_t ngroups, const int64_t* groups, double* out,
             double* lse, double* dq, double* dk, double* dv, double* dbias) {
+  if (var->norm != ORC_NORM_SOFTMAX) return 1; /* relu_attention has no backward here */
   if (check_shape(B, Hq, Hkv, N, d)) return 1;
   const int g = Hq / Hkv;
   const int64_t G = groups ? ngroups : (int64_t)B * Hkv;
@@ -370,6 +385,7 @@ int orc_bwd(const double* q, const double* k, const double* v, const double* dou
 int orc_bwd_dq_rows(const double* q, const double* k, const double* v, const double* dout, int B,
                     int Hq, int Hkv, int64_t N, int d, double scale, double theta, int rope,
                     const orc_variant* var, int64_t nrows, const int64_t* rows, double* dq_rows) {
+  if (var->norm != ORC_NORM_SOFTMAX) return 1;
   if (check_shape(B, Hq, Hkv, N, d)) return 1;
   const int g = Hq / Hkv;
   int err = 0;

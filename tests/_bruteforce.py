@@ -16,12 +16,14 @@ What it computes (AttnFuse paper):
     scale dS K', dK' = scale dS^T Q', dV = P^T dO, then dQ = R^T dQ', dK = R^T dK', dK and
     dV summed over the query heads of a group, dBias = dS (§4.4);
   - the decode step: one query row at q_pos against a cache whose keys are already rotated
-    (§4.2).
+    (§4.2);
+  - relu_attention (§3.1 names it without a definition; this build's reading): weights
+    max(s, 0) / N over the allowed keys, N the number of keys, O = sum of weight * v, no LSE.
 
 A mask is described by a plain dict: {"mask": "full" | "causal" | "window" | "block_sparse",
 "causal": bool, "window": W, "block": blk, "row_ptr": [...], "col_idx": [...], "bias":
 "none" | "alibi" | "additive", "slopes": [...], "add_bias": array broadcastable to
-[B, Hq, N, N]}.
+[B, Hq, N, N], "norm": "softmax" | "relu"}.
 """
 import math
 
@@ -119,8 +121,12 @@ def forward(q, k, v, scale, theta, rope_on, spec):
     _, _, rows = _prepare(q, k, scale, theta, rope_on, spec)
     out = np.zeros((B, Hq, N, d))
     lse = np.zeros((B, Hq, N))
+    relu = spec.get("norm", "softmax") == "relu"
     for (b, h, m), (keys, s) in rows.items():
-        p, lse[b, h, m] = _softmax(s)
+        if relu:
+            p, lse[b, h, m] = [max(x, 0.0) / N for x in s], math.nan
+        else:
+            p, lse[b, h, m] = _softmax(s)
         for c in range(d):
             out[b, h, m, c] = math.fsum(pi * v[b, h // g, n, c] for pi, n in zip(p, keys))
     return out, lse

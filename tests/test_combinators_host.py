@@ -55,9 +55,13 @@ def test_rejected_compositions(combo):
         C.attention(*(f() for f in combo))
 
 
-def test_relu_attention_has_no_semantics():
-    with pytest.raises(NotImplementedError):
-        C.attention(C.causal(), C.relu_attention())
+def test_relu_attention_maps_to_the_relu_normaliser():
+    att = C.attention(C.rope(5e5), C.causal(), C.relu_attention())
+    v = att.variant(4, torch.device("cpu"))
+    assert v.norm == af.NORM_RELU and v.mask == af.MASK_CAUSAL
+    assert C.attention(C.causal()).variant(4, torch.device("cpu")).norm == af.NORM_SOFTMAX
+    with pytest.raises(ValueError, match="one normaliser"):
+        C.attention(C.softmax(), C.relu_attention())
 
 
 def test_rope_auto_rule():

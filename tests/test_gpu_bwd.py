@@ -198,3 +198,38 @@ def test_bwd_mask_variant_workload(vname):
     _, _, _, rk, rv = oracle.backward(q64, k64, v64, do64, d ** -0.5, 1e4, True, ovar, groups=[(1, 9)])
     check_grad(dk.cpu()[1, 9], rk[1, 9], "dk[1,9]")
     check_grad(dv.cpu()[1, 9], rv[1, 9], "dv[1,9]")
+
+
+@pytest.mark.parametrize("vname,N,d,B,Hq,Hkv", [
+    ("bigbird", 4096, 64, 1, 2, 2),          # the mask-variant workload's BigBird layout
+    ("window_1024_c", 4096, 64, 1, 2, 2),    # its sliding window + causal
+    ("causal", 2048, 128, 1, 8, 2),          # GQA 4:1, head dim 128
+    ("bs_128_c", 1000, 128, 2, 4, 2),        # ragged N, 128-blocks with the causal restriction
+    ("bs_64", 700, 64, 1, 3, 1),             # 64-blocks, GQA 3:1
+])
+def test_bwd_tile_visits_match_oracle(vname, N, d, B, Hq, Hkv):
+    """Both backward kernels visit exactly the active tiles (paper §4.3): the dQ kernel's
+    (query tile, key tile) record equals the oracle's tile-visit set for 128 x 128 tiles, and
+    the dK/dV kernel's (64-row query block, key tile) record the set for 64 x 128 tiles, bit
+    for bit and for every head. Extra visits (wasted work that still gives correct gradients)
+    fail here."""
+    import oracle
+
+    dev = torch.device("cuda")
+    x = inputs.prefill(B, Hq, Hkv, N, d, seed=N + 3, with_dout=True)
+    q, k, v, do = (x[n].to(dev) for n in ("q", "k", "v", "dout"))
+    gvar, ovar = variant_pair(vname, N, Hq, dev, seed=5, B=B)
+    out, lse = af.fwd(q, k, v, rope_theta=1e4, rope_mode=af.ROPE_FUSED, variant=gvar)
+    t128, t64 = -(-N // 128), -(-N // 64)
+    gvar.bwd_dq_visits = torch.zeros((B, Hq, t128, t128), dtype=torch.uint8, device=dev)
+    gvar.bwd_dkdv_visits = torch.zeros((B, Hq, t64, t128), dtype=torch.uint8, device=dev)
+    af.bwd(q, k, v, out, lse, do, rope_theta=1e4, rope_mode=af.ROPE_FUSED, variant=gvar)
+    torch.cuda.synchronize()
+    assert af.device_status() == 0
+    ref_q = oracle.tile_visits(N, 128, 128, ovar)
+    ref_kv = oracle.tile_visits(N, 64, 128, ovar)
+    got_q, got_kv = gvar.bwd_dq_visits.cpu().numpy(), gvar.bwd_dkdv_visits.cpu().numpy()
+    for b in range(B):
+        for h in range(Hq):
+            assert np.array_equal(got_q[b, h], ref_q), f"dQ visits differ at b={b} h={h}"
+            assert np.array_equal(got_kv[b, h], ref_kv), f"dK/dV visits differ at b={b} h={h}"

@@ -29,6 +29,8 @@ def _orc_variant(orc, spec):
         kw.update(bias=1, slopes=np.array(spec["slopes"]))
     elif spec.get("bias") == "additive":
         kw.update(bias=2, add_bias=spec["add_bias"])
+    if spec.get("norm") == "relu":
+        kw["norm"] = 1
     return orc.Variant(**kw)
 
 
@@ -109,3 +111,17 @@ def test_rope_matches_brute_force(orc):
         y = orc.rope(x, pos, 5e5, inverse=inverse)
         by = np.array([bf.rotate(list(x[r]), pos[r], 5e5, inverse) for r in range(6)])
         _close(y, by, "rope")
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_relu_forward_matches_brute_force(orc, case):
+    """The relu_attention normaliser over every mask and bias kind: O agrees with the brute
+    force to 1e-12 and no LSE is defined (NaN)."""
+    name, B, Hq, Hkv, N, d, rope_on, theta, scale, spec = case
+    spec = dict(spec, norm="relu")
+    rng = np.random.default_rng(zlib.crc32(name.encode()) + 1)
+    q, k, v = _rand(rng, B, Hq, N, d), _rand(rng, B, Hkv, N, d), _rand(rng, B, Hkv, N, d)
+    o, lse = orc.forward(q, k, v, scale, theta, rope_on, _orc_variant(orc, spec))
+    bo, _ = bf.forward(q, k, v, scale, theta, rope_on, spec)
+    _close(o, bo, "relu O")
+    assert np.all(np.isnan(lse))

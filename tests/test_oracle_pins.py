@@ -456,3 +456,31 @@ def test_bigbird_layout_structure():
         else:
             assert {0, 1, r}.issubset(set(cols.tolist()))
             assert len(cols) == len({0, 1} | {c for c in (r - 1, r, r + 1) if c < 64}) + 3
+
+
+def test_relu_attention_closed_forms(orc):
+    """relu_attention (this build's reading of the paper's §3.1 normaliser: weights
+    max(s, 0) / N, N the number of keys). Pins that separate it from nearby mistakes:
+    - every score positive and equal (q = k = u, no RoPE): causal row m is
+      (scale |u|^2 / N) * sum_{n<=m} v_n, divided by N, not by the m + 1 visible keys;
+    - every score negative (q = -u): O = 0 exactly (the relu is applied);
+    - positive homogeneity: O(a q) = a O(q) for a > 0, which no exponential satisfies."""
+    rng = np.random.default_rng(11)
+    B, H, N, d, scale = 1, 2, 12, 8, 0.3
+    u = rng.standard_normal(d)
+    k = np.broadcast_to(u, (B, H, N, d)).copy()
+    v = rng.standard_normal((B, H, N, d))
+    var = orc.Variant(mask=orc.MASK_CAUSAL, norm=orc.NORM_RELU)
+    o, lse = orc.forward(k.copy(), k, v, scale, 1e4, False, var)
+    c = scale * float(u @ u) / N
+    assert np.allclose(o, c * np.cumsum(v, axis=2), rtol=0, atol=1e-12)
+    assert np.all(np.isnan(lse))
+    o_neg, _ = orc.forward(-k, k, v, scale, 1e4, False, var)
+    assert np.array_equal(o_neg, np.zeros_like(o_neg))
+    q = rng.standard_normal((B, H, N, d))
+    kk = rng.standard_normal((B, H, N, d))
+    for rope_on in (False, True):
+        o1, _ = orc.forward(q, kk, v, scale, 1e4, rope_on, orc.Variant(mask=orc.MASK_FULL, norm=orc.NORM_RELU))
+        o3, _ = orc.forward(3.0 * q, kk, v, scale, 1e4, rope_on, orc.Variant(mask=orc.MASK_FULL, norm=orc.NORM_RELU))
+        assert np.allclose(o3, 3.0 * o1, rtol=0, atol=1e-12)
+        assert not np.allclose(o1, 0.0)
