@@ -8,19 +8,19 @@
 // two heads at two positions or four positions of one head.
 //
 // Each slot is an independent online softmax over its own rows, with its own score buffer S_s
-// and output accumulator O_s in tensor memory. The tensor cores run, per kv tile,
-//     O_0 += P_0 V(i-1);  S_0 = Q_0 K(i)^T;  O_1 += P_1 V(i-1);  S_1 = Q_1 K(i)^T
+// and output accumulator O_s in tensor memory. Per kv tile i, slot s runs
+//     O_s += P_s V(i-1);  S_s = Q_s K(i)^T
 // as M = 256 cta_group::2 MMAs (both CTAs' rows of a slot at once; each CTA supplies half of
-// every K and V tile). While slot 0's softmax turns S_0 into P_0, the tensor cores work on slot
-// 1, and the other way round. P_s is written over S_s: the MMA that overwrites S_s is issued
-// by the same thread after the one that reads P_s, and one thread's MMAs complete in order.
+// every K and V tile), issued by the slot's own thread. P_s is written over S_s: the MMA that
+// overwrites S_s is issued by the same thread after the one that reads P_s, and one thread's
+// MMAs complete in order.
 //
 // TMEM (512 columns, same addresses in both CTAs): S_0 [0,128), S_1 [128,256), O_0 [256,384),
 // O_1 [384,512); P_s occupies the first 64 columns of S_s (bf16 pairs).
 // Warp roles (16 warps):
 //   warp 0      TMA producer (Q per unit and slot, this CTA's halves of K and V tiles); also
 //               forwards "K / V half landed" to the even CTA (K only without fused RoPE)
-//   warps 1, 2  MMA issuers of slot 0 / slot 1, taking turns per kv tile (even CTA only)
+//   warps 1, 2  MMA issuers of slot 0 / slot 1 (even CTA only)
 //   warp 3      scheduler: per-unit metadata (tiles, ranges, block-sparse bitmaps) into a ring
 //   warps 4-7   softmax of slot 0, warps 8-11 softmax of slot 1: one query row per thread;
 //               also rotate their Q tile (fused RoPE) and write O and LSE at the end of a unit
@@ -81,7 +81,6 @@ struct Ctl {
   uint64_t s_full[2], o_full[2];                       // MMA commits (multicast)
   uint64_t q_ready[2], k_ready[kKSt], v_ready[kVSt], p_full[2];  // even CTA: both CTAs arrive
   uint64_t meta_full[kRing], meta_empty[kRing];
-  uint64_t tok[2];                                     // issuers' turns (even CTA)
   uint64_t mma_final;
   uint32_t tmem_base;
   int abort_flag;
@@ -301,8 +300,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->meta_empty[e], consumers);
     }
     mbar_init(&ctl->mma_final, 2);   // one commit per issuer
-    mbar_init(&ctl->tok[0], 1);
-    mbar_init(&ctl->tok[1], 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -470,13 +467,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ======================= pair-MMA issuer of slot s =======================
       // Per kv tile i the issuer of slot s issues one burst: O_s += P_s V(i-1), then
       // S_s = Q_s K(i) (that S overwrites the P the PV reads; one thread's MMAs complete in
-      // order). The two issuers take turns through the tok barriers (slot 0's burst of tile i,
-      // slot 1's of tile i, slot 0's of tile i+1, ...), so the tensor pipe sees
-      //     PV_0(i-1) S_0(i) PV_1(i-1) S_1(i) PV_0(i) S_0(i+1) ...
-      // and each slot's softmax runs while the tensor cores work on the other slot. Two
-      // threads (on different SM sub-partitions) share the MMA issue work; every barrier wait of
-      // a burst comes before its MMAs, because a shared-memory access right after an MMA stalls
-      // the issuing thread for about two MMAs.
+      // order). The two issuers run concurrently on different SM sub-partitions, so each
+      // one's barrier waits overlap the other's MMAs. Every wait of a burst comes before its
+      // MMAs: a shared-memory access while MMAs stream their operands from shared memory
+      // costs the issuing thread a couple of hundred cycles.
       const int s = warp - 1;
       constexpr uint32_t idesc_s = idesc_f32acc(256, kBN, 0, 0, RK != kRopeNone);
       constexpr uint32_t idesc_o = idesc_bf16_f32(256, kD, 0, 1);
@@ -491,20 +485,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t tS = tmem + kTmS + 128 * s, tO = tmem + kTmO + 128 * s;
       int ik = 0;          // kv tiles walked (K and V copy index)
       int pc = 0;          // S issued (phase of s_full / p_full)
-      int nb = 0;          // bursts issued (phase of the turn barrier)
       bool pend = false;   // a PV waits for its P
       int pend_v = 0;      // its V copy index
       bool pend_acc = false, pend_last = false;
       bool ok = true;
-      // wait for this slot's turn (slot 0's first burst goes first)
-      auto take_turn = [&]() {
-        if (s == 0 && nb == 0) return;
-        ok = mbar_wait_cluster(&ctl->tok[s], (s == 0 ? nb - 1 : nb) & 1, status, abort_flag);
-      };
-      auto pass_turn = [&]() {
-        mbar_arrive(&ctl->tok[s ^ 1]);
-        ++nb;
-      };
       // the PV of the pending tile (its P and V waited on by the caller)
       auto issue_pv = [&]() {
         const int vs = pend_v % kVSt;
@@ -550,8 +534,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const bool a = bs ? pbit(M.sbits[s], j) : (j >= slo && j < shi);
           const int st = ik % kKSt;
           // ---- all waits of the burst ----
-          take_turn();
-          if (ok && !opened) open_slot();
+          if (!opened) open_slot();
           if (ok && pend) wait_pv_inputs();
           if (ok) ok = mbar_wait_cluster(&ctl->k_ready[st], (ik / kKSt) & 1, status, abort_flag);
           if (ok && !a) ok = mbar_wait_cluster(&ctl->v_ready[ik % kVSt], (ik / kVSt) & 1, status, abort_flag);
@@ -579,7 +562,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_commit_pair(&ctl->v_empty[ik % kVSt], 3);
           }
           mma_commit_pair(&ctl->k_empty[st], 3);
-          pass_turn();
         }
         if (ok && !opened) open_slot();
         if (ok) mbar_arrive(&ctl->meta_empty[e]);
@@ -895,7 +877,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t a = fma2(f2_pack(x[2 * c], x[2 * c + 1]), mul2v, nb2);
             const float p0 = ex2_approx(f2_lo(a)), p1 = ex2_approx(f2_hi(a));
             acc2[c & 3] = add2(acc2[c & 3], f2_pack(p0, p1));
-            pk[c] = pack_bf16x2_alu(p0, p1);
+            pk[c] = pack_bf16x2(p0, p1);
           }
           const uint64_t acc = add2(add2(acc2[0], acc2[1]), add2(acc2[2], acc2[3]));
           l_run += f2_lo(acc) + f2_hi(acc);

@@ -570,13 +570,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return r;
 }
 
-// Two finite, non-negative floats to bf16 (nearest, ties away from zero) with integer
-// operations only: add half a bf16 unit to the bit pattern and keep the top 16 bits. Runs on
-// the integer pipe, leaving the conversion pipe (shared with ex2) to the exponentials.
-__device__ __forceinline__ uint32_t pack_bf16x2_alu(float lo, float hi) {
-  return __byte_perm(__float_as_uint(lo) + 0x8000u, __float_as_uint(hi) + 0x8000u, 0x7632);
-}
-
 // Round two floats to fp16, saturating to the largest finite value instead of overflowing.
 __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   uint32_t r;
