@@ -230,15 +230,18 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
 // ATTNFUSE_ROPE_AUTO: the faster of on-chip rotation and pre-rotation, by the crossover
 // N* measured on GB300 (the paper's Rotation Calculus, §5.3; B*N = 16384 tokens, causal).
 // Head dim 64: fusion wins below N* ~ 1.26k (forward; two sweeps gave 1240 and 1285) and
-// ~ 280 (backward, which re-reads each K tile once per query tile). Head dim 128: pre-rotation
-// was faster at every N from 256 to 16384, forward and backward.
+// ~ 280 (backward, which re-reads each K tile once per query tile). Head dim 128: the
+// persistent forward, whose K tiles serve four query tiles, wins below N* ~ 3.36k (t_prerotate
+// / t_fused = 1.33 at N = 256, 1.07 at 2048, 0.97 at 4096); the backward pre-rotates at every N.
 constexpr int kAutoFusedBelowN64Fwd = 1260;
 constexpr int kAutoFusedBelowN64Bwd = 284;
+constexpr int kAutoFusedBelowN128Fwd = 3360;
 
 static attnfuse_rope_mode resolve_rope(attnfuse_rope_mode m, int N, int d, bool backward) {
   if (m != ATTNFUSE_ROPE_AUTO) return m;
   if (d == 64 && N < (backward ? kAutoFusedBelowN64Bwd : kAutoFusedBelowN64Fwd))
     return ATTNFUSE_ROPE_FUSED;
+  if (d == 128 && !backward && N < kAutoFusedBelowN128Fwd) return ATTNFUSE_ROPE_FUSED;
   return ATTNFUSE_ROPE_PREROTATE;
 }
 
@@ -568,7 +571,7 @@ static attnfuse_status decode_plan(int B, int Hkv, int L, int num_splits, int* s
       }
     }
   }
-  s = std::max(1, std::min(s, tiles));
+  s = std::max(1, std::min(std::min(s, tiles), kDecMaxSplits));
   const int ch = ((tiles + s - 1) / s) * 128;
   *chunk = ch;
   *splits = s;

@@ -357,26 +357,51 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   if (warp == 2) tmem_dealloc(tmem, 512);
 }
 
-// Phase 2: one CTA per (b, query head); thread c handles output column c.
+// Phase 2: one CTA per (b, query head); thread c handles output column c. The splits are read
+// in parallel: thread s takes split s's (max, sum), a block reduction gives the overall max,
+// the per-split weights pass through shared memory, and each column then sums its splits
+// with independent loads (no chain of dependent global reads).
 template <int D>
 __global__ void __launch_bounds__(D) combine_kernel(const __grid_constant__ DecParams p) {
+  __shared__ float w_sh[kDecMaxSplits];
+  __shared__ float red[D / 32];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int bh = blockIdx.x;
   const int b = bh / p.Hq, h = bh % p.Hq;
-  const int c = threadIdx.x;
+  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  const int S = p.splits_used;
   const int64_t base = (int64_t)bh * p.splits;
-  float M = kNegInf;
-  for (int s = 0; s < p.splits_used; ++s) M = fmaxf(M, p.part_m[base + s]);
-  float L = 0.f, acc = 0.f;
-  if (M != kNegInf) {
-    for (int s = 0; s < p.splits_used; ++s) {
-      const float ms = p.part_m[base + s];
-      if (ms == kNegInf) continue;
-      const float w = ex2_approx(ms - M);
-      L += w * p.part_l[base + s];
-      acc += w * p.part_acc[(base + s) * D + c];
-    }
+  // overall max over the splits (log2 units)
+  float mloc = kNegInf;
+  for (int s = c; s < S; s += D) mloc = fmaxf(mloc, p.part_m[base + s]);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+  if (lane == 0) red[warp] = mloc;
+  __syncthreads();
+  float M = red[0];
+#pragma unroll
+  for (int k = 1; k < D / 32; ++k) M = fmaxf(M, red[k]);
+  __syncthreads();
+  // per-split weights and their sum of row sums
+  float lloc = 0.f;
+  for (int s = c; s < S; s += D) {
+    const float ms = p.part_m[base + s];
+    const float w = (M == kNegInf || ms == kNegInf) ? 0.f : ex2_approx(ms - M);
+    w_sh[s] = w;
+    lloc += w * p.part_l[base + s];
   }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+  if (lane == 0) red[warp] = lloc;
+  __syncthreads();
+  float L = 0.f;
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) L += red[k];
+  // column c: sum_s w_s acc_s[c]
+  float acc = 0.f;
+  const float* pa = p.part_acc + base * D + c;
+#pragma unroll 8
+  for (int s = 0; s < S; ++s) acc += w_sh[s] * pa[(int64_t)s * D];
   const float o = (L > 0.f) ? acc / L : 0.f;
   p.out[b * p.o_sb + h * p.o_sh + c] = __float2bfloat16_rn(o);
   if (p.lse && c == 0) p.lse[bh] = (L > 0.f) ? (M + log2f(L)) * kLn2 : kNegInf;

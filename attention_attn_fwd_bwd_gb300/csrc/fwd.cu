@@ -660,37 +660,49 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int N, int half, Rope
 }
 
 // ---------------------------------------------------------------------------------------------
-// Pre-rotation (paper Fig. 1a): out[b,h,n,:] = R_n x[b,h,n,:], out contiguous. One thread per
-// (row, chunk pair); HBM-bound elementwise pass.
+// Pre-rotation (paper Fig. 1a): out[b,h,n,:] = R_n x[b,h,n,:], out contiguous. HBM-bound
+// elementwise pass.
+//
+// The (cos, sin) of a row follow the recurrence the kernels use on chip: row r of a block of
+// BLK rows at n0 starts from the table entry of position n0 + r % RG and advances r / RG times
+// by the entry of position RG (queries of the forward: RG = 8, BLK = 128; keys: RG = 128 / (d/16)
+// in blocks of 64 or 128; RG = BLK = 1 reads every row's own entry). One thread walks one such
+// chain (rows n0 + q, n0 + q + RG, ...) for one chunk pair, taking one angle-addition step per
+// row, so the rotated values are bit-identical to the kernels' while the pass stays bound by
+// memory rather than by recomputing the chain for every row.
 // ---------------------------------------------------------------------------------------------
-template <bool OUT_F16, int KEY_D, int BLK, bool QUERY = false>
+template <bool OUT_F16>
 __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb, int64_t sh,
                                  int64_t sn, __nv_bfloat16* __restrict__ out, int H, int N, int d,
-                                 const float2* __restrict__ cs, int64_t rows) {
-  // KEY_D != 0: the (cos, sin) follow a kernel's in-block recurrence (key_cs8 with blocks of
-  // BLK rows, or query_cs8 for the forward's query tiles) so that on-chip and pre-rotated
-  // operands are bit-identical. KEY_D == 0: table.
+                                 const float2* __restrict__ cs, int RG, int BLK, int64_t chains) {
   const int cp = d / 16;
-  const int64_t total = rows * cp;
-  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+  const int nblk = (N + BLK - 1) / BLK;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < chains;
        idx += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = idx / cp;
     const int c = static_cast<int>(idx % cp);
-    const int n = static_cast<int>(row % N);
-    const int64_t bh = row / N;
+    int64_t t = idx / cp;
+    const int q = static_cast<int>(t % RG);
+    t /= RG;
+    const int blk = static_cast<int>(t % nblk);
+    const int64_t bh = t / nblk;
     const int h = static_cast<int>(bh % H);
     const int64_t bb = bh / H;
-    const __nv_bfloat16* src = x + bb * sb + h * sh + n * sn;
-    uint4 lo = *reinterpret_cast<const uint4*>(src + c * 8);
-    uint4 hi = *reinterpret_cast<const uint4*>(src + d / 2 + c * 8);
-    float cc[8], ss[8];
-    if (KEY_D != 0 && QUERY) query_cs8<KEY_D == 0 ? 64 : KEY_D>(cs, n, c, cc, ss);
-    else if (KEY_D != 0) key_cs8<KEY_D == 0 ? 64 : KEY_D, BLK>(cs, n, c, cc, ss);
-    else load_cs8(cs + (size_t)n * (d / 2) + c * 8, cc, ss);
-    rot_chunk_cs<OUT_F16>(lo, hi, cc, ss);
-    __nv_bfloat16* dst = out + row * d;
-    *reinterpret_cast<uint4*>(dst + c * 8) = lo;
-    *reinterpret_cast<uint4*>(dst + d / 2 + c * 8) = hi;
+    const int n0 = blk * BLK + q;
+    if (n0 >= N) continue;
+    float cc[8], ss[8], wc[8], ws[8];
+    load_cs8(cs + (size_t)n0 * (d / 2) + c * 8, cc, ss);
+    if (BLK > RG) load_cs8(cs + (size_t)RG * (d / 2) + c * 8, wc, ws);
+    const __nv_bfloat16* src = x + bb * sb + h * sh + c * 8;
+    __nv_bfloat16* dst = out + (bh * N) * d + c * 8;
+#pragma unroll 4
+    for (int n = n0; n < blk * BLK + BLK && n < N; n += RG) {
+      uint4 lo = *reinterpret_cast<const uint4*>(src + n * sn);
+      uint4 hi = *reinterpret_cast<const uint4*>(src + n * sn + d / 2);
+      rot_chunk_cs<OUT_F16>(lo, hi, cc, ss);
+      *reinterpret_cast<uint4*>(dst + (int64_t)n * d) = lo;
+      *reinterpret_cast<uint4*>(dst + (int64_t)n * d + d / 2) = hi;
+      if (n + RG < blk * BLK + BLK) advance_cs8(cc, ss, wc, ws);
+    }
   }
 }
 
@@ -723,23 +735,24 @@ cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
                              int N, int d, const float2* cs, bool out_f16, int block,
                              cudaStream_t stream) {
-  const int64_t rows = static_cast<int64_t>(B) * H * N;
-  const int64_t total = rows * (d / 16);
+  // the recurrence of the target kernel (see prerotate_kernel)
+  const int cp = d / 16;
+  int RG = 1, BLK = 1;                       // block == 0: each row's own table entry
+  if (block < 0) {                           // forward queries
+    RG = 8;
+    BLK = 128;
+  } else if (block > 0) {                    // forward keys (fp16) or backward operands (bf16)
+    RG = 128 / cp;
+    BLK = out_f16 ? (d == 128 ? 64 : 128) : 128;
+  }
+  const int64_t chains = static_cast<int64_t>(B) * H * ((N + BLK - 1) / BLK) * RG * cp;
   const int threads = 256;
-  const int blocks = static_cast<int>(std::min<int64_t>((total + threads - 1) / threads, 152 * 16));
+  const int blocks = static_cast<int>(std::min<int64_t>((chains + threads - 1) / threads, 152 * 16));
   void (*fn)(const __nv_bfloat16*, int64_t, int64_t, int64_t, __nv_bfloat16*, int, int, int,
-             const float2*, int64_t) = nullptr;
-  if (block == 0)
-    fn = out_f16 ? prerotate_kernel<true, 0, 128> : prerotate_kernel<false, 0, 128>;
-  else if (block < 0)  // forward queries: the 128-row query-tile recurrence
-    fn = d == 128 ? prerotate_kernel<true, 128, 128, true> : prerotate_kernel<true, 64, 128, true>;
-  else if (out_f16)  // forward keys: blocks of 64 (head dim 128) or 128 (head dim 64)
-    fn = d == 128 ? prerotate_kernel<true, 128, 64> : prerotate_kernel<true, 64, 128>;
-  else               // backward operands: blocks of 128
-    fn = d == 128 ? prerotate_kernel<false, 128, 128> : prerotate_kernel<false, 64, 128>;
+             const float2*, int, int, int64_t) = out_f16 ? prerotate_kernel<true> : prerotate_kernel<false>;
   fn<<<blocks, threads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(x), strides[0], strides[1], strides[2],
-      static_cast<__nv_bfloat16*>(out), H, N, d, cs, rows);
+      static_cast<__nv_bfloat16*>(out), H, N, d, cs, RG, BLK, chains);
   return cudaGetLastError();
 }
 

@@ -71,6 +71,7 @@ struct BwdParams {
 // tmK point at pre-rotated copies); dQ and dK are rotated back unless kRopeNone.
 cudaError_t launch_bwd(const BwdParams& p, int rope_kind, cudaStream_t stream);
 
+constexpr int kDecMaxSplits = 512;  // the combine kernel merges at most this many KV chunks
 size_t decode_smem_size(int d);
 cudaError_t launch_decode(const DecParams& p, int d, bool rope_q, cudaStream_t stream);
 

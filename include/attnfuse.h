@@ -194,7 +194,7 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
  * q: [B, Hq, d] (strides b, h, c); k_cache, v_cache: [B, Hkv, L, d]; out: [B, Hq, d];
  * lse: [B, Hq] or NULL. num_splits: number of KV chunks per (b, kv-head), 0 = automatic
  * (about two resident CTAs per SM); chunks are whole 128-key tiles, so fewer chunks than
- * requested are used when L / 128 < num_splits. Requires Hq / Hkv <= 32. The q rotation
+ * requested are used when L / 128 < num_splits, and at most 512 are used. Requires Hq / Hkv <= 32. The q rotation
  * (FUSED) is rounded to bf16, the element type of the cache.
  * ------------------------------------------------------------------------------------------ */
 attnfuse_status attnfuse_decode_workspace_size(int B, int Hq, int Hkv, int L, int d,
@@ -251,10 +251,10 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
 
 /* The mode ATTNFUSE_ROPE_AUTO resolves to for sequence length N and head dim d, for the
  * forward (backward = 0) or the backward (backward = 1). Measured on GB300 with B*N = 16384
- * tokens, causal: fusion wins only for head dim 64, below N ~ 1.26k (forward) and N ~ 280
- * (backward); for head dim 128 the pre-rotation pass is cheaper than rotating each K tile once
- * per query tile at every N from 256 up. The workspace size functions accept
- * ATTNFUSE_ROPE_AUTO and size for the resolved mode. */
+ * tokens, causal: fusion wins for head dim 64 below N ~ 1.26k (forward) and N ~ 280
+ * (backward), and for the head-dim-128 forward below N ~ 3.36k; above those, and for the
+ * head-dim-128 backward at every N, the pre-rotation pass is cheaper than rotating K tiles on
+ * chip. The workspace size functions accept ATTNFUSE_ROPE_AUTO and size for the resolved mode. */
 attnfuse_status attnfuse_rope_auto_mode(int N, int d, int backward, attnfuse_rope_mode* mode);
 
 /* Build the (cos, sin) table that the rotating modes keep at the start of their workspace:

@@ -65,8 +65,9 @@ def test_relu_attention_maps_to_the_relu_normaliser():
 
 
 def test_rope_auto_rule():
-    """The measured crossover (GB300, B*N = 16384): fusion wins only for head dim 64, below
-    N ~ 1.26k (forward) and ~ 280 (backward); pre-rotation everywhere else."""
+    """The measured crossover (GB300, B*N = 16384): fusion wins for head dim 64 below
+    N ~ 1.26k (forward) and ~ 280 (backward), for the head-dim-128 forward below N ~ 3.36k;
+    pre-rotation everywhere else."""
     from attention_attn_fwd_bwd_gb300 import _build
 
     _build.build()
@@ -79,8 +80,11 @@ def test_rope_auto_rule():
         assert af.rope_auto_mode(N, 64, backward=True) == af.ROPE_FUSED
     for N in (284, 1024, 4096):
         assert af.rope_auto_mode(N, 64, backward=True) == af.ROPE_PREROTATE
-    for N in (1, 256, 4096):
+    for N in (1, 256, 2048, 3359):
+        assert af.rope_auto_mode(N, 128) == af.ROPE_FUSED
+    for N in (3360, 4096, 16384):
         assert af.rope_auto_mode(N, 128) == af.ROPE_PREROTATE
+    for N in (1, 256, 4096):
         assert af.rope_auto_mode(N, 128, backward=True) == af.ROPE_PREROTATE
     # workspace sizes follow the resolved mode
     for N, d in ((512, 64), (4096, 64), (512, 128)):
