@@ -229,13 +229,15 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
 
 // ATTNFUSE_ROPE_AUTO: the faster of on-chip rotation and pre-rotation, by the crossover
 // N* measured on GB300 (the paper's Rotation Calculus, §5.3; B*N = 16384 tokens, causal).
-// Head dim 64: fusion wins below N* ~ 1.26k (forward; two sweeps gave 1240 and 1285) and
-// ~ 280 (backward, which re-reads each K tile once per query tile). Head dim 128: the
-// persistent forward, whose K tiles serve four query tiles, wins below N* ~ 3.36k (t_prerotate
-// / t_fused = 1.33 at N = 256, 1.07 at 2048, 0.97 at 4096); the backward pre-rotates at every N.
-constexpr int kAutoFusedBelowN64Fwd = 1260;
-constexpr int kAutoFusedBelowN64Bwd = 284;
-constexpr int kAutoFusedBelowN128Fwd = 3360;
+// The pre-rotation pass streams at ~5 TB/s, so it costs ~70 us per 16k-token, 32-head call.
+// Head dim 64: fusion wins below N* ~ 1.9k (forward; t_prerotate / t_fused = 1.22 at N = 256,
+// 0.99 at 2048) and ~ 260 (backward, which re-reads each K tile once per query tile). Head
+// dim 128: the persistent forward, whose K tiles serve four query tiles, wins below
+// N* ~ 2.19k (1.16 at N = 256, 1.01 at 2048, 0.93 at 4096); the backward pre-rotates at
+// every N.
+constexpr int kAutoFusedBelowN64Fwd = 1900;
+constexpr int kAutoFusedBelowN64Bwd = 258;
+constexpr int kAutoFusedBelowN128Fwd = 2190;
 
 static attnfuse_rope_mode resolve_rope(attnfuse_rope_mode m, int N, int d, bool backward) {
   if (m != ATTNFUSE_ROPE_AUTO) return m;

@@ -149,13 +149,13 @@ def test_rope_auto_mode_rule(lib):
     m = ctypes.c_int()
     auto = lambda N, d, bwd: (lib.attnfuse_rope_auto_mode(N, d, bwd, ctypes.byref(m)), m.value)
     FUSED, PRE = af.ROPE_FUSED, af.ROPE_PREROTATE
-    # head dim 128: fusion wins for the forward below the measured crossover (3360); the
+    # head dim 128: fusion wins for the forward below the measured crossover (2190); the
     # backward pre-rotates at every N
-    assert auto(256, 128, 0) == (OK, FUSED) and auto(3359, 128, 0) == (OK, FUSED)
-    assert auto(3360, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
-    # head dim 64: fusion wins below the measured crossovers (forward 1260, backward 284)
-    assert auto(1259, 64, 0) == (OK, FUSED) and auto(1260, 64, 0) == (OK, PRE)
-    assert auto(283, 64, 1) == (OK, FUSED) and auto(284, 64, 1) == (OK, PRE)
+    assert auto(256, 128, 0) == (OK, FUSED) and auto(2189, 128, 0) == (OK, FUSED)
+    assert auto(2190, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
+    # head dim 64: fusion wins below the measured crossovers (forward 1900, backward 258)
+    assert auto(1899, 64, 0) == (OK, FUSED) and auto(1900, 64, 0) == (OK, PRE)
+    assert auto(257, 64, 1) == (OK, FUSED) and auto(258, 64, 1) == (OK, PRE)
     assert lib.attnfuse_rope_auto_mode(0, 64, 0, ctypes.byref(m)) == INVALID
     assert lib.attnfuse_rope_auto_mode(512, 80, 0, ctypes.byref(m)) == UNSUPPORTED
     assert lib.attnfuse_rope_auto_mode(512, 64, 0, None) == INVALID

@@ -91,8 +91,8 @@ def test_bwd_deterministic():
 
 @pytest.mark.parametrize("N", [2048, 4096])
 def test_bwd_training_workload(N):
-    """B=8, Hq=32, Hkv=8, d=128, theta=5e5, causal, fused RoPE; dq on sampled rows, dk/dv on
-    two whole GQA groups (every row of those groups' key/value heads)."""
+    """B=8, Hq=32, Hkv=8, d=128, theta=5e5, causal, fused RoPE; dq on one whole (b, h) slice
+    plus sampled rows, dk/dv on whole GQA groups (every row of those groups' key/value heads)."""
     import oracle
 
     B, Hq, Hkv, d = 8, 32, 8, 128
@@ -101,6 +101,8 @@ def test_bwd_training_workload(N):
     q64, k64, v64, do64 = (f64(x[n]) for n in ("q", "k", "v", "dout"))
     var = oracle.Variant(mask=1)
     rows = inputs.sample_rows(B, Hq, N, 48, seed=N, always=[(0, 0, 0), (7, 31, N - 1), (3, 9, 128)])
+    m = np.arange(N, dtype=np.int64)
+    rows = np.concatenate([rows, np.stack([np.full_like(m, 6), np.full_like(m, 13), m], axis=1)])
     rdq = oracle.backward_dq_rows(q64, k64, v64, do64, d ** -0.5, 5e5, True, var, rows)
     dqc = dq.cpu()
     check_grad(torch.stack([dqc[b, h, m] for b, h, m in rows]), rdq, "dq rows")

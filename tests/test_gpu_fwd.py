@@ -196,16 +196,25 @@ def test_strided_inputs():
 
 @pytest.mark.parametrize("rope_mode", [af.ROPE_FUSED, af.ROPE_PREROTATE])
 def test_full_size_llama8b_sampled(rope_mode):
-    """B=4, Hq=32, Hkv=8, N=4096, d=128, theta=5e5, causal; sampled rows vs the oracle."""
+    """B=4, Hq=32, Hkv=8, N=4096, d=128, theta=5e5, causal: every row of one whole (b, h)
+    slice, plus sampled rows of the others, vs the oracle."""
     rows = inputs.sample_rows(4, 32, 4096, 40, seed=2,
                               always=[(0, 0, 0), (3, 31, 4095), (1, 5, 4095), (2, 17, 128),
                                       (3, 30, 127), (0, 1, 2047)])
+    rows = np.concatenate([rows, _slice_rows(1, 22, 4096)])
     _run(4, 32, 8, 4096, 128, rope_mode, "causal", seed=2000, theta=5e5, rows=rows)
+
+
+def _slice_rows(b, h, N):
+    """(b, h, m) for every query row m of one (b, h) slice."""
+    m = np.arange(N, dtype=np.int64)
+    return np.stack([np.full_like(m, b), np.full_like(m, h), m], axis=1)
 
 
 @pytest.mark.parametrize("vname", ["window_1024_c", "alibi", "bigbird"])
 def test_full_size_mask_variants_sampled(vname):
-    """B=2, H=16, N=4096, d=64, theta=1e4, fused: window 1024 + causal, ALiBi, BigBird."""
+    """B=2, H=16, N=4096, d=64, theta=1e4, fused: window 1024 + causal, ALiBi, BigBird; one
+    whole (b, h) slice plus sampled rows vs the oracle, tile-visit sets bit-exact."""
     import oracle
 
     dev = torch.device("cuda")
@@ -228,6 +237,7 @@ def test_full_size_mask_variants_sampled(vname):
     assert af.device_status() == 0
     rows = inputs.sample_rows(B, H, N, 40, seed=seed, always=[(0, 0, 0), (1, 15, 4095),
                                                               (0, 3, 1024), (1, 8, 63)])
+    rows = np.concatenate([rows, _slice_rows(1, 9, N)])
     o_ref, l_ref = oracle.forward_rows(f64(x["q"]), f64(x["k"]), f64(x["v"]), 0.125, 1e4, True,
                                        ovar, rows)
     oc, lc = out.cpu(), lse.cpu()
