@@ -125,6 +125,13 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // The table always covers at least 128 positions: the fused key rotation reads the entry of
 // position 128 / (d / 16) as its per-row step.
 int rope_table_rows(int N) { return N < 128 ? 128 : N; }
+// Head-dim-128 forward with fused RoPE: the rotated keys (fp16) and one flag per 64-key block.
+size_t fused_k_bytes(int B, int Hkv, int N, int d) {
+  return align_up((size_t)B * Hkv * N * d * 2, 256);
+}
+size_t fused_sync_bytes(int B, int Hkv, int N) {
+  return align_up((size_t)B * Hkv * ((N + 63) / 64) * sizeof(uint32_t), 256);
+}
 size_t rope_table_bytes(int N, int d) {
   return align_up((size_t)rope_table_rows(N) * (d / 2) * sizeof(float2), 256);
 }
@@ -232,12 +239,12 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
 // The pre-rotation pass streams at ~5 TB/s, so it costs ~70 us per 16k-token, 32-head call.
 // Head dim 64: fusion wins below N* ~ 1.9k (forward; t_prerotate / t_fused = 1.22 at N = 256,
 // 0.99 at 2048) and ~ 260 (backward, which re-reads each K tile once per query tile). Head
-// dim 128: the persistent forward, whose K tiles serve four query tiles, wins below
-// N* ~ 2.19k (1.16 at N = 256, 1.01 at 2048, 0.93 at 4096); the backward pre-rotates at
-// every N.
+// dim 128: the persistent forward rotates each K block once per call (shared through L2) and
+// each Q tile in shared memory, and wins below N* ~ 14k (1.13 at N = 256, 1.06 at 2048, 1.02
+// at 4096, 1.00 at 16384); the backward pre-rotates at every N.
 constexpr int kAutoFusedBelowN64Fwd = 1900;
 constexpr int kAutoFusedBelowN64Bwd = 258;
-constexpr int kAutoFusedBelowN128Fwd = 2190;
+constexpr int kAutoFusedBelowN128Fwd = 14000;
 
 static attnfuse_rope_mode resolve_rope(attnfuse_rope_mode m, int N, int d, bool backward) {
   if (m != ATTNFUSE_ROPE_AUTO) return m;
@@ -269,6 +276,7 @@ attnfuse_status attnfuse_fwd_workspace_size(int B, int Hq, int Hkv, int N, int d
     n += align_up((size_t)B * Hq * N * d * 2, 256);
     n += align_up((size_t)B * Hkv * N * d * 2, 256);
   }
+  if (rope_mode == ATTNFUSE_ROPE_FUSED && d == 128) n += fused_k_bytes(B, Hkv, N, d) + fused_sync_bytes(B, Hkv, N);
   if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
   *bytes = n;
   return ok();
@@ -359,6 +367,19 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
     qa = qr; ka = kr; qs = qs_c; ks = ks_c;
+  }
+  if (rope_mode == ATTNFUSE_ROPE_FUSED && d == 128) {
+    // K is rotated once per 64-key block inside the forward (by whichever CTA needs the block
+    // first) into a workspace copy that every CTA then loads with TMA
+    uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
+    p.k_raw = static_cast<const __nv_bfloat16*>(k);
+    p.k_sb = k_strides[0]; p.k_sh = k_strides[1]; p.k_sn = k_strides[2];
+    p.k_rot = reinterpret_cast<uint16_t*>(base);
+    p.k_sync = reinterpret_cast<uint32_t*>(base + fused_k_bytes(B, Hkv, N, d));
+    cudaError_t e = cudaMemsetAsync(p.k_sync, 0, fused_sync_bytes(B, Hkv, N), stream);
+    if (e != cudaSuccess) return cuda_fail(e, "k_sync reset");
+    ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
+    ka = p.k_rot; ks = ks_c;
   }
   if ((rc = encode_bhnd(&p.tmQ, qa, qs, B, Hq, N, d, "q"))) return rc;
   // head dim 128 runs on CTA pairs, each loading 64-key halves of K

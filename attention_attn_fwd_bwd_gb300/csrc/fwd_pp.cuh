@@ -24,7 +24,8 @@
 //   warp 3      scheduler: per-unit metadata (tiles, ranges, block-sparse bitmaps) into a ring
 //   warps 4-7   softmax of slot 0, warps 8-11 softmax of slot 1: one query row per thread;
 //               also rotate their Q tile (fused RoPE) and write O and LSE at the end of a unit
-//   warps 12-15 K rotators (fused RoPE): rotate this CTA's 64 keys of each K tile in place
+//   warps 12-15 K rotators (fused RoPE): rotate each 64-key block of K once per call into a
+//               workspace copy K' (fp16) that every CTA loads with TMA
 // Every wait is bounded (see ptx.cuh).
 #pragma once
 #include <cuda.h>
@@ -285,7 +286,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int s = 0; s < kKSt; ++s) {
       mbar_init(&ctl->k_full[s], 1);
       mbar_init(&ctl->k_empty[s], 2);   // one commit per issuer
-      mbar_init(&ctl->k_ready[s], ROPE ? 8 : 2);
+      mbar_init(&ctl->k_ready[s], 2);
     }
     for (int s = 0; s < kVSt; ++s) {
       mbar_init(&ctl->v_full[s], 1);
@@ -349,6 +350,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto meta_ready = [&](int u) {
         return mbar_test(&ctl->meta_full[u % kRing], (u / kRing) & 1);
       };
+      // Fused RoPE: this CTA's 64-key block of kv tile j has been rotated into K' (by any CTA).
+      const int nkb = (p.N + 63) / 64;
+      auto k_block_rotated = [&](const UnitMeta& M, int j) {
+        const int kb = 2 * j + rank;
+        if (kb >= nkb) return true;  // past the end: the copy reads zeros
+        if (ld_acquire_gpu(p.k_sync + (M.b * p.Hkv + M.kvh) * nkb + kb) != 2u) return false;
+        fence_proxy_async_global();
+        return true;
+      };
       while (true) {
         bool moved = false;
         // ---- Q ----
@@ -381,7 +391,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               moved = true;
             } else {
               const int st = ik % kKSt;
-              if (ik < kKSt || mbar_test(&ctl->k_empty[st], ((ik / kKSt) - 1) & 1)) {
+              if ((ik < kKSt || mbar_test(&ctl->k_empty[st], ((ik / kKSt) - 1) & 1)) &&
+                  (!ROPE || k_block_rotated(M, jk))) {
                 mbar_arrive_expect_tx(&ctl->k_full[st], kKHalf);
                 for (int pn = 0; pn < 2; ++pn)
                   tma_load_4d_hint(smem + kOffK + st * kKHalf + pn * (64 * 128), &p.tmK, &ctl->k_full[st],
@@ -418,7 +429,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         // ---- relay ----
-        if (!ROPE && rk < ik && mbar_test(&ctl->k_full[rk % kKSt], (rk / kKSt) & 1)) {
+        if (rk < ik && mbar_test(&ctl->k_full[rk % kKSt], (rk / kKSt) & 1)) {
           arrive_leader(&ctl->k_ready[rk % kKSt], rank);
           ++rk;
           moved = true;
@@ -436,7 +447,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++urel;
           }
         }
-        if (dq && dk && dv && rv == iv && (ROPE || rk == ik)) break;
+        if (dq && dk && dv && rv == iv && rk == ik) break;
         if (moved) {
           idle = 0;
         } else {
@@ -581,13 +592,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ======================= K rotators (fused RoPE) =======================
     setmaxnreg_dec<kRegsRot>();
     if (ROPE) {
-      // Thread (c, rg) rotates chunk pair c of rows rg, rg+16, rg+32, rg+48 of this CTA's
-      // 64-key half; the (cos, sin) of successive rows advance by the angle of 16 positions.
-      const int rt = tid - 384;
-      const int c = rt & 7, rg = rt >> 3;
-      const int kN = p.N;
+      // K' = R_n K is made once per 64-key block and call. The rotator warps walk the blocks
+      // their units load (this CTA's half of every kv tile), warp w taking every fourth; the
+      // first warp of any CTA to claim a block rotates it from global memory into the fp16 K'
+      // buffer and flags it, and the producers of every CTA copy K' with TMA (mostly from L2).
+      // Lane (c, rl) rotates 16-byte chunk c of both halves of rows rg + 16k (k < 4) of the
+      // four chains rg = rl + 4i; a chain starts from its table entry and steps the (cos, sin)
+      // of 16 positions per row (the pre-rotation pass uses the same chains, so K' is
+      // bit-identical to its output).
+      const int wr = warp - 12;
+      const int c = lane & 7, rl = lane >> 3;
+      const int kN = p.N, nkb = (kN + 63) / 64;
       const float2* const cs_tab = p.rope_cs;
-      uint64_t wc2[4], ws2[4];  // (cos, sin) of 16 positions, pairs of dims
+      constexpr uint64_t kSign2 = 0x8000000080000000ull;
+      uint64_t wc2[4], ws2[4], nws2[4];  // (cos, sin) of 16 positions, pairs of dims
       {
         float wc[8], ws[8];
         load_cs8(cs_tab + (size_t)16 * (kD / 2) + c * 8, wc, ws);
@@ -595,16 +613,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int w = 0; w < 4; ++w) {
           wc2[w] = f2_pack(wc[2 * w], wc[2 * w + 1]);
           ws2[w] = f2_pack(ws[2 * w], ws[2 * w + 1]);
+          nws2[w] = ws2[w] ^ kSign2;
         }
       }
       const uint64_t pol_tab = l2_policy_evict_last();  // the table stays in L2
-      float4 pre[4];
-      auto fetch = [&](int jj) {
-        const int pos = min(jj * kBN + rank * 64 + rg, kN - 1);
-        const float4* src = reinterpret_cast<const float4*>(cs_tab + (size_t)pos * (kD / 2) + c * 8);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) pre[w] = ldg_f4_hint(src + w, pol_tab);
-      };
+      const uint64_t pol_in = l2_policy_evict_first();  // K is read once here
+      const uint64_t pol_out = l2_policy_evict_last();  // K' is re-read by every unit
       int ik = 0;
       bool ok = true;
       for (int u = 0; ok; ++u) {
@@ -613,59 +627,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const UnitMeta& M = ctl->ring[e];
         if (!M.live) break;
-        if (M.jb < M.je) fetch(M.jb);
+        const int bh = M.b * p.Hkv + M.kvh;
+        const __nv_bfloat16* src = p.k_raw + M.b * p.k_sb + M.kvh * p.k_sh;
+        uint16_t* dst = p.k_rot + (int64_t)bh * kN * kD;
         for (int j = M.jb; j < M.je; j = next_tile(M, bs, j), ++ik) {
-          const int st = ik % kKSt;
-          const int n0 = j * kBN + rank * 64;
-          uint64_t c2[4], s2[4];
+          const int kb = 2 * j + rank;
+          if ((ik & 3) != wr || kb >= nkb) continue;
+          uint32_t* flag = p.k_sync + bh * nkb + kb;
+          uint32_t mine = 0;
+          if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(flag) == 0u)
+            mine = atomicCAS(flag, 0u, 1u) == 0u ? 1u : 0u;
+          if (!__shfl_sync(0xffffffffu, mine, 0)) continue;
+          const int n0 = kb * 64;
+#pragma unroll 1
+          for (int i = 0; i < 4; ++i) {
+            const int rg = rl + 4 * i;
+            float4 pre[4];
+            {
+              const float4* t = reinterpret_cast<const float4*>(
+                  cs_tab + (size_t)min(n0 + rg, kN - 1) * (kD / 2) + c * 8);
 #pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            c2[w] = f2_pack(pre[w].x, pre[w].z);
-            s2[w] = f2_pack(pre[w].y, pre[w].w);
-          }
-          {
-            const int jn = next_tile(M, bs, j);
-            fetch(jn < M.je ? jn : j);
-          }
-          if (!__all_sync(0xffffffffu, mbar_wait(&ctl->k_full[st], (ik / kKSt) & 1, status, abort_flag))) {
-            ok = false;
-            break;
-          }
-          uint8_t* tile = smem + kOffK + st * kKHalf;
+              for (int w = 0; w < 4; ++w) pre[w] = ldg_f4_hint(t + w, pol_tab);
+            }
+            uint4 lo[4], hi[4];
 #pragma unroll
-          for (int k2 = 0; k2 < 4; k2 += 2) {
-            uint4 lo[2], hi[2];
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat16* row = src + (int64_t)min(n0 + rg + 16 * k, kN - 1) * p.k_sn + c * 8;
+              lo[k] = ldg_u4_hint(row, pol_in);
+              hi[k] = ldg_u4_hint(row + 64, pol_in);
+            }
+            uint64_t c2[4], s2[4], ns2[4];
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              const uint32_t offl = sw128_offset(rg + 16 * (k2 + k), c);
-              lo[k] = *reinterpret_cast<const uint4*>(tile + offl);
-              hi[k] = *reinterpret_cast<const uint4*>(tile + offl + 64 * 128);
+            for (int w = 0; w < 4; ++w) {
+              c2[w] = f2_pack(pre[w].x, pre[w].z);
+              s2[w] = f2_pack(pre[w].y, pre[w].w);
+              ns2[w] = s2[w] ^ kSign2;
             }
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              uint64_t ns2[4];
-#pragma unroll
-              for (int w = 0; w < 4; ++w) ns2[w] = s2[w] ^ 0x8000000080000000ull;
+            for (int k = 0; k < 4; ++k) {
               rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
-              if (k2 + k + 1 < 4) {
-                uint64_t nws2[4];
-#pragma unroll
-                for (int w = 0; w < 4; ++w) nws2[w] = ws2[w] ^ 0x8000000080000000ull;
-                advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
-              }
+              if (k < 3) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
             }
 #pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              if (n0 + rg + 16 * (k2 + k) < kN) {
-                const uint32_t offl = sw128_offset(rg + 16 * (k2 + k), c);
-                *reinterpret_cast<uint4*>(tile + offl) = lo[k];
-                *reinterpret_cast<uint4*>(tile + offl + 64 * 128) = hi[k];
+            for (int k = 0; k < 4; ++k) {
+              const int n = n0 + rg + 16 * k;
+              if (n < kN) {
+                uint16_t* out = dst + (int64_t)n * kD + c * 8;
+                stg_u4_hint(out, lo[k], pol_out);
+                stg_u4_hint(out + 64, hi[k], pol_out);
               }
             }
           }
-          fence_proxy_async_smem();
+          // K' visible to other CTAs' TMA copies before the flag says so
+          fence_proxy_async_global();
+          __threadfence();
           __syncwarp();
-          if (lane == 0) arrive_leader(&ctl->k_ready[st], rank);
+          if (lane == 0) st_release_gpu(flag, 2u);
         }
         if (ok && lane == 0) mbar_arrive(&ctl->meta_empty[e]);
       }

@@ -23,6 +23,13 @@ struct FwdParams {
   float scale;
   int pp_hp;                  // persistent head-dim-128 forward: query heads per unit (1, 2, 4)
   int pp_clusters;            // and the number of 2-CTA clusters launched
+  // persistent head-dim-128 forward with fused RoPE: K is rotated once per 64-key block into
+  // k_rot (fp16 [B, Hkv, N, d], contiguous; tmK maps it), k_sync[block] = 0 untouched,
+  // 1 claimed, 2 rotated (zeroed before every launch)
+  const __nv_bfloat16* k_raw;
+  int64_t k_sb, k_sh, k_sn;
+  uint16_t* k_rot;
+  uint32_t* k_sync;
   VariantDev var;
   int* status;
 };

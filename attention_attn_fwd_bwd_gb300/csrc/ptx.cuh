@@ -292,6 +292,36 @@ __device__ __forceinline__ float4 ldg_f4_hint(const float4* ptr, uint64_t pol) {
   return v;
 }
 
+// 16-byte global load / store with an L2 eviction-priority hint (data one kernel writes and
+// other CTAs of the same kernel then read with TMA).
+__device__ __forceinline__ uint4 ldg_u4_hint(const void* ptr, uint64_t pol) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(ptr), "l"(pol));
+  return v;
+}
+__device__ __forceinline__ void stg_u4_hint(void* ptr, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(ptr), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
+// Flags that CTAs of one kernel exchange through global memory: a release store after the
+// data, an acquire load before reading it.
+__device__ __forceinline__ void st_release_gpu(uint32_t* ptr, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(ptr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
+  return v;
+}
+// Order this thread's generic-proxy global accesses with its later async-proxy ones (TMA).
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void tma_load_4d_hint(void* dst, const void* tmap, uint64_t* bar,
                                                  int c0, int c1, int c2, int c3,
                                                  uint64_t policy) {

@@ -81,7 +81,9 @@ def test_workspace_sizes(lib):
     assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 0, ctypes.byref(n)) == OK
     assert n.value == 0
     assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 1, ctypes.byref(n)) == OK
-    assert n.value == 4096 * 64 * 8  # (cos, sin) fp32 table
+    # (cos, sin) fp32 table, then (head dim 128) the rotated keys K' in fp16 and one flag per
+    # 64-key block
+    assert n.value == 4096 * 64 * 8 + 4 * 8 * 4096 * 128 * 2 + 4 * 8 * 64 * 4
     assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 2, ctypes.byref(n)) == OK
     assert n.value == 4096 * 64 * 8 + 4 * 32 * 4096 * 128 * 2 + 4 * 8 * 4096 * 128 * 2
     assert lib.attnfuse_fwd_workspace_size(1, 2, 2, 10, 64, 1, ctypes.byref(n)) == OK
@@ -149,10 +151,10 @@ def test_rope_auto_mode_rule(lib):
     m = ctypes.c_int()
     auto = lambda N, d, bwd: (lib.attnfuse_rope_auto_mode(N, d, bwd, ctypes.byref(m)), m.value)
     FUSED, PRE = af.ROPE_FUSED, af.ROPE_PREROTATE
-    # head dim 128: fusion wins for the forward below the measured crossover (2190); the
+    # head dim 128: fusion wins for the forward below the measured crossover (14000); the
     # backward pre-rotates at every N
-    assert auto(256, 128, 0) == (OK, FUSED) and auto(2189, 128, 0) == (OK, FUSED)
-    assert auto(2190, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
+    assert auto(256, 128, 0) == (OK, FUSED) and auto(13999, 128, 0) == (OK, FUSED)
+    assert auto(14000, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
     # head dim 64: fusion wins below the measured crossovers (forward 1900, backward 258)
     assert auto(1899, 64, 0) == (OK, FUSED) and auto(1900, 64, 0) == (OK, PRE)
     assert auto(257, 64, 1) == (OK, FUSED) and auto(258, 64, 1) == (OK, PRE)
