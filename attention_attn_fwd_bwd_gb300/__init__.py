@@ -101,6 +101,9 @@ def load():
             "attnfuse_debug_wait_timeout": ([ctypes.c_uint64, P], I),
             "attnfuse_rope_table": ([P, S, I, I, F, P], I),
             "attnfuse_rope_auto_mode": ([I, I, I, ctypes.POINTER(I)], I),
+            "attnfuse_fwd_fp8_workspace_size": ([I, I, I, I, I, ctypes.POINTER(S)], I),
+            "attnfuse_fwd_fp8": ([P, ST, P, ST, P, ST, P, ST, P, I, I, I, I, I, F, F, F, F, VP,
+                                  P, S, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -283,6 +286,12 @@ def fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode):
     return n.value
 
 
+def fwd_fp8_workspace_size(B, Hq, Hkv, N, d):
+    n = ctypes.c_size_t()
+    _check(load().attnfuse_fwd_fp8_workspace_size(B, Hq, Hkv, N, d, ctypes.byref(n)))
+    return n.value
+
+
 def bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode):
     n = ctypes.c_size_t()
     _check(load().attnfuse_bwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, ctypes.byref(n)))
@@ -350,6 +359,48 @@ def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=N
             _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
             _ptr(out), _strides(out, 4), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
             float(rope_theta), rope_mode, ctypes.byref(cv), _ptr(ws), ws_n, st))
+    return out, lse
+
+
+def fwd_fp8(q, k, v, q_scale, k_scale, v_scale, scale=None, variant=None, out=None, lse=None,
+            with_lse=True, workspace=None, stream=None):
+    """e4m3 forward (head dim 128): q [B,Hq,N,128], k/v [B,Hkv,N,128] as torch.uint8 (raw
+    e4m3 bytes) or torch.float8_e4m3fn CUDA tensors; attends over q_scale*q, k_scale*k and
+    v_scale*v; returns (out bf16, lse fp32). No RoPE: q and k are used as given."""
+    import torch
+
+    f8 = tuple(t for t in (torch.uint8, getattr(torch, "float8_e4m3fn", None)) if t is not None)
+    bf16, f32 = (torch.bfloat16,), (torch.float32,)
+    _need(q, "q", f8, ndim=4, dims="[B, Hq, N, d]")
+    B, Hq, N, d = q.shape
+    dev = q.device
+    _need(k, "k", f8, ndim=4, dims="[B, Hkv, N, d]")
+    Hkv = k.shape[1]
+    _need(k, "k", f8, (B, Hkv, N, d), dev)
+    _need(v, "v", f8, (B, Hkv, N, d), dev)
+    if scale is None:
+        scale = d ** -0.5
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", bf16, (B, Hq, N, d), dev)
+    relu = variant is not None and variant.norm == NORM_RELU
+    if relu and lse is not None:
+        raise ValueError("relu_attention has no LSE: pass lse=None")
+    if with_lse and lse is None and not relu:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", f32, (B, Hq, N), dev, contiguous=True)
+    if variant is not None:
+        variant.check(dev, B, Hq, N)
+    ws_n = fwd_fp8_workspace_size(B, Hq, Hkv, N, d)
+    ws = _workspace(ws_n, dev, workspace)
+    cv = (variant or Variant()).c_struct()
+    ctx, st = _launch_context(dev, stream)
+    with ctx:
+        _check(load().attnfuse_fwd_fp8(
+            _ptr(q), _strides(q, 4), _ptr(k), _strides(k, 4), _ptr(v), _strides(v, 4),
+            _ptr(out), _strides(out, 4), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+            float(q_scale), float(k_scale), float(v_scale), ctypes.byref(cv), _ptr(ws), ws_n, st))
     return out, lse
 
 

@@ -93,6 +93,24 @@ attnfuse_status encode_bhnd(CUtensorMap* m, const void* ptr, const int64_t st[4]
   return ATTNFUSE_OK;
 }
 
+// e4m3 [B, H, N, d] view with element (= byte) strides; box (128, box_rows, 1, 1): one
+// 128-byte swizzle row holds a whole head-dim-128 row.
+attnfuse_status encode_bhnd8(CUtensorMap* m, const void* ptr, const int64_t st[4], int B, int H,
+                             int N, int d, const char* name, int box_rows) {
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)st[2], (cuuint64_t)st[1], (cuuint64_t)st[0]};
+  cuuint32_t box[4] = {128, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(ptr), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "%s: tensor map encode failed (CUresult %d)", name,
+                (int)r);
+  return ATTNFUSE_OK;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Validation
 // ---------------------------------------------------------------------------------------------
@@ -404,6 +422,96 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   cudaError_t e = d == 128 ? launch_fwd_pp(p, rk, p.var.norm, stream)
                            : launch_fwd(p, d, rk, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+  return ok();
+}
+
+// ---------------------------------------------------------------------------------------------
+// e4m3 forward
+// ---------------------------------------------------------------------------------------------
+namespace {
+size_t fp8_v_bytes(int B, int Hkv, int N, int d) { return align_up((size_t)B * Hkv * N * d * 2, 256); }
+size_t fp8_sync_bytes(int B, int Hkv, int N) {
+  return align_up((size_t)B * Hkv * 2 * ((N + 127) / 128) * sizeof(uint32_t), 256);
+}
+attnfuse_status check_tensor8(const void* p, const int64_t st[4], const char* name) {
+  if (!p) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  if (!st) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s strides are NULL", name);
+  if (st[3] != 1) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s: innermost stride must be 1", name);
+  for (int i = 0; i < 3; ++i)
+    if (st[i] <= 0 || (st[i] % 16) != 0)
+      return fail(ATTNFUSE_ERR_INVALID_ARG,
+                  "%s: stride[%d] = %lld must be a positive multiple of 16 elements", name, i,
+                  (long long)st[i]);
+  return ATTNFUSE_OK;
+}
+bool positive_finite(float x) { return x > 0.f && std::isfinite(x); }
+}  // namespace
+
+attnfuse_status attnfuse_fwd_fp8_workspace_size(int B, int Hq, int Hkv, int N, int d, size_t* bytes) {
+  if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  if (d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "e4m3 forward needs head dim 128 (got %d)", d);
+  *bytes = fp8_v_bytes(B, Hkv, N, d) + fp8_sync_bytes(B, Hkv, N);
+  return ok();
+}
+
+attnfuse_status attnfuse_fwd_fp8(const void* q, const int64_t q_strides[4], const void* k,
+                                 const int64_t k_strides[4], const void* v,
+                                 const int64_t v_strides[4], void* out, const int64_t o_strides[4],
+                                 float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                                 float q_scale, float k_scale, float v_scale,
+                                 const attnfuse_variant* variant, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream) {
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  if (d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "e4m3 forward needs head dim 128 (got %d)", d);
+  if ((rc = check_tensor8(q, q_strides, "q"))) return rc;
+  if ((rc = check_tensor8(k, k_strides, "k"))) return rc;
+  if ((rc = check_tensor8(v, v_strides, "v"))) return rc;
+  if ((rc = check_tensor(out, o_strides, "out"))) return rc;
+  if (lse && (reinterpret_cast<uintptr_t>(lse) & 3u))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "lse is not 4-byte aligned");
+  if (!positive_finite(scale)) return fail(ATTNFUSE_ERR_INVALID_ARG, "scale must be positive and finite");
+  if (!positive_finite(q_scale) || !positive_finite(k_scale) || !positive_finite(v_scale))
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "q_scale, k_scale and v_scale must be positive and finite");
+  FwdParams p;
+  memset(&p, 0, sizeof(p));
+  if ((rc = to_dev_variant(variant, N, Hq, &p.var))) return rc;
+  if (p.var.norm == ATTNFUSE_NORM_RELU && lse)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "relu_attention has no LSE: pass lse = NULL");
+  size_t need = 0;
+  if ((rc = attnfuse_fwd_fp8_workspace_size(B, Hq, Hkv, N, d, &need))) return rc;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need,
+                workspace_bytes);
+  int* st = nullptr;
+  if ((rc = device_state(&st))) return rc;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  p.v_raw = static_cast<const uint8_t*>(v);
+  p.v_sb = v_strides[0]; p.v_sh = v_strides[1]; p.v_sn = v_strides[2];
+  p.v_wide = reinterpret_cast<uint16_t*>(base);
+  p.v_sync = reinterpret_cast<uint32_t*>(base + fp8_v_bytes(B, Hkv, N, d));
+  cudaError_t e = cudaMemsetAsync(p.v_sync, 0, fp8_sync_bytes(B, Hkv, N), stream);
+  if (e != cudaSuccess) return cuda_fail(e, "v_sync reset");
+  int64_t vs_c[4] = {(int64_t)Hkv * N * d, (int64_t)N * d, d, 1};
+  if ((rc = encode_bhnd8(&p.tmQ, q, q_strides, B, Hq, N, d, "q", 128))) return rc;
+  if ((rc = encode_bhnd8(&p.tmK, k, k_strides, B, Hkv, N, d, "k", 64))) return rc;
+  if ((rc = encode_bhnd(&p.tmV, p.v_wide, vs_c, B, Hkv, N, d, "v (widened)"))) return rc;
+  p.out = static_cast<__nv_bfloat16*>(out);
+  p.o_sb = o_strides[0]; p.o_sh = o_strides[1]; p.o_sn = o_strides[2];
+  p.lse = lse;
+  p.B = B; p.Hq = Hq; p.Hkv = Hkv; p.N = N; p.g = Hq / Hkv;
+  // the dequantisation scales of q and k fold into the score scale, v's into O
+  const float s_qk = scale * q_scale * k_scale;
+  if (!positive_finite(s_qk)) return fail(ATTNFUSE_ERR_INVALID_ARG, "scale * q_scale * k_scale is not finite");
+  p.scale_log2 = s_qk * 1.4426950408889634f;
+  p.scale = s_qk;
+  p.o_scale = v_scale;
+  p.status = st;
+  e = launch_fwd_pp(p, kFp8, p.var.norm, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "e4m3 forward launch");
   return ok();
 }
 

@@ -1,5 +1,6 @@
 // Launcher of the persistent head-dim-128 forward (kernel in fwd_pp.cuh; the instances are
-// compiled per RoPE kind in fwd_pp_none.cu, fwd_pp_fused.cu and fwd_pp_pre.cu).
+// compiled per operand kind in fwd_pp_none.cu, fwd_pp_fused.cu, fwd_pp_pre.cu and
+// fwd_pp_fp8.cu).
 #include <algorithm>
 #include <mutex>
 
@@ -10,6 +11,7 @@ namespace afx {
 FwdFn fwd_pp_pick_none(int bias, int norm);
 FwdFn fwd_pp_pick_fused(int bias, int norm);
 FwdFn fwd_pp_pick_pre(int bias, int norm);
+FwdFn fwd_pp_pick_fp8(int bias, int norm);
 
 size_t fwd_pp_smem_size() { return kSmem; }
 
@@ -50,6 +52,7 @@ cudaError_t launch_fwd_pp(FwdParams p, int rope_kind, int norm, cudaStream_t str
   const int bias = p.var.bias;
   FwdFn fn = rope_kind == kRopeFused        ? fwd_pp_pick_fused(bias, norm)
              : rope_kind == kRopePrerotated ? fwd_pp_pick_pre(bias, norm)
+             : rope_kind == kFp8            ? fwd_pp_pick_fp8(bias, norm)
                                             : fwd_pp_pick_none(bias, norm);
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem);
   if (e != cudaSuccess) return e;

@@ -25,7 +25,8 @@
 //   warps 4-7   softmax of slot 0, warps 8-11 softmax of slot 1: one query row per thread;
 //               also rotate their Q tile (fused RoPE) and write O and LSE at the end of a unit
 //   warps 12-15 K rotators (fused RoPE): rotate each 64-key block of K once per call into a
-//               workspace copy K' (fp16) that every CTA loads with TMA
+//               workspace copy K' (fp16) that every CTA loads with TMA; with e4m3 inputs they
+//               widen V to bf16 the same way (the scores then run on kind::f8f6f4 MMAs)
 // Every wait is bounded (see ptx.cuh).
 #pragma once
 #include <cuda.h>
@@ -255,7 +256,8 @@ __device__ void fill_meta(UnitMeta& M, const FwdParams& p, const Sched& S, int c
 
 }  // namespace
 
-// RK: how the score operands are produced (kRopeNone / kRopeFused / kRopePrerotated).
+// RK: how the score operands are produced (kRopeNone / kRopeFused / kRopePrerotated, or
+// kFp8: e4m3 Q and K used as they are, e4m3 V widened to bf16).
 // BIAS: score bias compiled in (0 none, 1 ALiBi, 2 additive). NORM: 0 softmax, 1 ReLU
 // normaliser (P = relu(s) / N, no row sum).
 template <int RK, int BIAS, int NORM>
@@ -268,6 +270,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const VariantDev& var = p.var;
   constexpr bool ROPE = (RK == kRopeFused);
+  constexpr bool FP8 = (RK == kFp8);
   const int rank = static_cast<int>(cluster_ctarank());
   const int cid = static_cast<int>(blockIdx.x) >> 1;
   const Sched S = make_sched(p);
@@ -293,9 +296,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->v_empty[s], 2);
       mbar_init(&ctl->v_ready[s], 2);
     }
-    // ring consumers: producer, (even CTA) two issuers, (fused RoPE) four rotator warps,
+    // ring consumers: producer, (even CTA) two issuers, (fused RoPE, e4m3) four rotator warps,
     // eight softmax warps
-    const int consumers = 1 + (rank == 0 ? 2 : 0) + (ROPE ? 4 : 0) + 8;
+    const int consumers = 1 + (rank == 0 ? 2 : 0) + ((ROPE || FP8) ? 4 : 0) + 8;
     for (int e = 0; e < kRing; ++e) {
       mbar_init(&ctl->meta_full[e], 32);
       mbar_init(&ctl->meta_empty[e], consumers);
@@ -350,14 +353,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto meta_ready = [&](int u) {
         return mbar_test(&ctl->meta_full[u % kRing], (u / kRing) & 1);
       };
-      // Fused RoPE: this CTA's 64-key block of kv tile j has been rotated into K' (by any CTA).
-      const int nkb = (p.N + 63) / 64;
+      // A block another CTA's warps write for this kernel (fused RoPE: K'; e4m3: widened V)
+      // is ready once its flag reads 2; TMA may then copy it.
+      auto flag_done = [&](const uint32_t* f) {
+        if (ld_acquire_gpu(f) != 2u) return false;
+        fence_proxy_async_global();
+        return true;
+      };
+      const int nkb = (p.N + 63) / 64, nvb = 2 * ((p.N + kBN - 1) / kBN);
+      // this CTA's 64-key block of kv tile j, rotated
       auto k_block_rotated = [&](const UnitMeta& M, int j) {
         const int kb = 2 * j + rank;
         if (kb >= nkb) return true;  // past the end: the copy reads zeros
-        if (ld_acquire_gpu(p.k_sync + (M.b * p.Hkv + M.kvh) * nkb + kb) != 2u) return false;
-        fence_proxy_async_global();
-        return true;
+        return flag_done(p.k_sync + (M.b * p.Hkv + M.kvh) * nkb + kb);
+      };
+      // this CTA's 64 dims of the 128 keys of kv tile j, widened
+      auto v_block_widened = [&](const UnitMeta& M, int j) {
+        return flag_done(p.v_sync + (M.b * p.Hkv + M.kvh) * nvb + 2 * j + rank);
       };
       while (true) {
         bool moved = false;
@@ -367,8 +379,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!M.live) {
             dq = true;
           } else if (uq == 0 || mbar_test(&ctl->q_empty[sq], (uq - 1) & 1)) {
-            mbar_arrive_expect_tx(&ctl->q_full[sq], kQTile);
-            for (int pn = 0; pn < 2; ++pn)
+            mbar_arrive_expect_tx(&ctl->q_full[sq], FP8 ? kQTile / 2 : kQTile);
+            for (int pn = 0; pn < (FP8 ? 1 : 2); ++pn)
               tma_load_4d_hint(smem + kOffQ + sq * kQTile + pn * (kBM * 128), &p.tmQ, &ctl->q_full[sq],
                                pn * 64, M.q0[sq][rank], M.head[sq][rank], M.b, pol_stream);
             if (++sq == 2) {
@@ -393,8 +405,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int st = ik % kKSt;
               if ((ik < kKSt || mbar_test(&ctl->k_empty[st], ((ik / kKSt) - 1) & 1)) &&
                   (!ROPE || k_block_rotated(M, jk))) {
-                mbar_arrive_expect_tx(&ctl->k_full[st], kKHalf);
-                for (int pn = 0; pn < 2; ++pn)
+                mbar_arrive_expect_tx(&ctl->k_full[st], FP8 ? kKHalf / 2 : kKHalf);
+                for (int pn = 0; pn < (FP8 ? 1 : 2); ++pn)
                   tma_load_4d_hint(smem + kOffK + st * kKHalf + pn * (64 * 128), &p.tmK, &ctl->k_full[st],
                                    pn * 64, jk * kBN + rank * 64, M.kvh, M.b, pol_keep);
                 ++ik;
@@ -417,7 +429,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               moved = true;
             } else if (iv < ik) {
               const int st = iv % kVSt;
-              if (iv < kVSt || mbar_test(&ctl->v_empty[st], ((iv / kVSt) - 1) & 1)) {
+              if ((iv < kVSt || mbar_test(&ctl->v_empty[st], ((iv / kVSt) - 1) & 1)) &&
+                  (!FP8 || v_block_widened(M, jv))) {
                 mbar_arrive_expect_tx(&ctl->v_full[st], kVHalf);
                 tma_load_4d_hint(smem + kOffV + st * kVHalf, &p.tmV, &ctl->v_full[st], rank * 64,
                                  jv * kBN, M.kvh, M.b, pol_keep);
@@ -483,7 +496,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // MMAs: a shared-memory access while MMAs stream their operands from shared memory
       // costs the issuing thread a couple of hundred cycles.
       const int s = warp - 1;
-      constexpr uint32_t idesc_s = idesc_f32acc(256, kBN, 0, 0, RK != kRopeNone);
+      constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(256, kBN) : idesc_f32acc(256, kBN, 0, 0, RK != kRopeNone);
       constexpr uint32_t idesc_o = idesc_bf16_f32(256, kD, 0, 1);
       // Descriptors as a 32-bit low word (start address >> 4, plus the leading byte offset)
       // and one shared high word; a tile's k-steps add compile-time offsets to the low word.
@@ -555,11 +568,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (pend) issue_pv();
           if (a) {
             const uint32_t bk = dK0 + st * (kKHalf >> 4);
-            mma_ss_pair_w<0>(tS, dQ, bk, dhi, idesc_s);
+            if constexpr (FP8) {
+              // one 128-byte panel per row: four k-steps of 32 e4m3 values (32 bytes)
+              mma_ss_pair_f8_w<0>(tS, dQ, bk, dhi, idesc_s);
 #pragma unroll
-            for (int kk = 1; kk < kD / 16; ++kk)
-              mma_ss_pair_w<1>(tS, dQ + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4),
-                               bk + (((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4), dhi, idesc_s);
+              for (int kk = 1; kk < kD / 32; ++kk)
+                mma_ss_pair_f8_w<1>(tS, dQ + ((kk * 32) >> 4), bk + ((kk * 32) >> 4), dhi, idesc_s);
+            } else {
+              mma_ss_pair_w<0>(tS, dQ, bk, dhi, idesc_s);
+#pragma unroll
+              for (int kk = 1; kk < kD / 16; ++kk)
+                mma_ss_pair_w<1>(tS, dQ + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4),
+                                 bk + (((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4), dhi, idesc_s);
+            }
             mma_commit_pair(&ctl->s_full[s], 3);
             ++pc;
             ++cnt;
@@ -679,6 +700,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           // K' visible to other CTAs' TMA copies before the flag says so
+          fence_proxy_async_global();
+          __threadfence();
+          __syncwarp();
+          if (lane == 0) st_release_gpu(flag, 2u);
+        }
+        if (ok && lane == 0) mbar_arrive(&ctl->meta_empty[e]);
+      }
+    }
+    if (FP8) {
+      // V (e4m3) is widened to bf16 once per block of 128 keys x 64 dims (this CTA's half of a
+      // kv tile's PV operand) and call, claimed and flagged like K' above, into a workspace
+      // copy that the producers copy with TMA. Lane (row rr, quarter q4) widens 16 values of
+      // rows rr + 8i; four rows are loaded before any is converted.
+      const int wr = warp - 12;
+      const int rr = lane >> 2, q4 = lane & 3;
+      const int kN = p.N, nvb = 2 * ((kN + kBN - 1) / kBN);
+      const uint64_t pol_in = l2_policy_evict_first();  // V is read once here
+      const uint64_t pol_out = l2_policy_evict_last();  // and the widened copy by every unit
+      int ik = 0;
+      bool ok = true;
+      for (int u = 0; ok; ++u) {
+        const int e = u % kRing;
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->meta_full[e], (u / kRing) & 1, status, abort_flag));
+        if (!ok) break;
+        const UnitMeta& M = ctl->ring[e];
+        if (!M.live) break;
+        const int bh = M.b * p.Hkv + M.kvh;
+        const int c0 = rank * 64 + q4 * 16;  // first dim of this lane's 16
+        const uint8_t* src = p.v_raw + M.b * p.v_sb + M.kvh * p.v_sh + c0;
+        uint16_t* dst = p.v_wide + (int64_t)bh * kN * kD + c0;
+        for (int j = M.jb; j < M.je; j = next_tile(M, bs, j), ++ik) {
+          if ((ik & 3) != wr) continue;
+          uint32_t* flag = p.v_sync + bh * nvb + 2 * j + rank;
+          uint32_t mine = 0;
+          if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(flag) == 0u)
+            mine = atomicCAS(flag, 0u, 1u) == 0u ? 1u : 0u;
+          if (!__shfl_sync(0xffffffffu, mine, 0)) continue;
+          const int n0 = j * kBN + rr;
+#pragma unroll 1
+          for (int i0 = 0; i0 < kBN / 8; i0 += 4) {
+            uint4 x[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              x[i] = ldg_u4_hint(src + (int64_t)min(n0 + 8 * (i0 + i), kN - 1) * p.v_sn, pol_in);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int n = n0 + 8 * (i0 + i);
+              uint4 lo, hi;
+              e4m3x16_to_bf16(x[i], lo, hi);
+              if (n < kN) {
+                stg_u4_hint(dst + (int64_t)n * kD, lo, pol_out);
+                stg_u4_hint(dst + (int64_t)n * kD + 8, hi, pol_out);
+              }
+            }
+          }
           fence_proxy_async_global();
           __threadfence();
           __syncwarp();
@@ -928,7 +1004,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const bool have = M.ns[s] > 0;
       if (valid) {
-        const float inv = NORM == 1 ? 1.f : ((l_run > 0.f) ? 1.f / l_run : 0.f);
+        float inv = NORM == 1 ? 1.f : ((l_run > 0.f) ? 1.f / l_run : 0.f);
+        if constexpr (FP8) inv *= p.o_scale;
         __nv_bfloat16* orow = p.out + b * p.o_sb + head * p.o_sh + (int64_t)m * p.o_sn;
 #pragma unroll 1
         for (int ch = 0; ch < 4; ++ch) {

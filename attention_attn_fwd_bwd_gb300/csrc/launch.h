@@ -30,6 +30,14 @@ struct FwdParams {
   int64_t k_sb, k_sh, k_sn;
   uint16_t* k_rot;
   uint32_t* k_sync;
+  // e4m3 forward: V (e4m3, byte strides) is widened once per 128-key x 64-dim block into
+  // v_wide (bf16 [B, Hkv, N, d], contiguous; tmV maps it), v_sync[block] as k_sync; O is
+  // multiplied by o_scale (V's dequantisation scale)
+  const uint8_t* v_raw;
+  int64_t v_sb, v_sh, v_sn;
+  uint16_t* v_wide;
+  uint32_t* v_sync;
+  float o_scale;
   VariantDev var;
   int* status;
 };
@@ -87,6 +95,8 @@ size_t fwd_smem_size(int d);
 constexpr int kRopeNone = 0;        // bf16 inputs used as they are
 constexpr int kRopeFused = 1;       // rotated in shared memory by the kernel, rounded to fp16
 constexpr int kRopePrerotated = 2;  // rotated by the pre-rotation kernel into fp16 buffers
+constexpr int kFp8 = 3;             // head-dim-128 forward: e4m3 Q and K (scores on
+                                    // kind::f8f6f4), V widened once per call to bf16
 // One CTA per 256 query rows (two 128-row sub-tiles); head dim 64.
 cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream);
 // Head dim 128, persistent: clusters of two CTAs walk units of four 128-row query tiles of

@@ -7,6 +7,7 @@
 #pragma once
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 namespace afx {
 
@@ -444,6 +445,19 @@ __device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint32_t a_lo, ui
       "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
       : "memory");
 }
+// The same with 8-bit operands (kind::f8f6f4; A and B of the same format, set in idesc).
+template <int ACC>
+__device__ __forceinline__ void mma_ss_pair_f8_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
+                                                 uint32_t hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %5, 0;\n\t"
+      "mov.b64 a, {%1, %3};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
 __device__ __forceinline__ void mma_ts_pair_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo,
                                               uint32_t hi, uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -579,6 +593,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N, ui
   return idesc_f32acc(M, N, a_mn, b_mn, 0);
 }
 
+// kind::f8f6f4 with E4M3 A and B (format code 0 for both), f32 accumulator, K-major operands.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
+  return (1u << 4) | ((N >> 3) << 17) | ((M >> 4) << 24);
+}
+
 // Byte offset of 16-byte chunk `chunk` (0..7) of row `row` inside a 128B-swizzled tile whose
 // base is 1024-byte aligned and whose rows are 128 bytes apart.
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t chunk) {
@@ -639,6 +658,27 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
 // bf16x2 word -> packed fp32 pair (exact)
 __device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
   return f2_pack(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+// 16 e4m3 values (one 16-byte word) widened to bf16, exactly: e4m3 -> f16 pairs, f16 -> f32,
+// and every e4m3 value is representable in bf16.
+__device__ __forceinline__ void e4m3x16_to_bf16(uint4 x, uint4& lo, uint4& hi) {
+  const uint32_t in[4] = {x.x, x.y, x.z, x.w};
+  uint32_t out[8];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const unsigned short pair = static_cast<unsigned short>(in[w] >> (16 * h));
+      uint32_t f16x2;
+      asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(f16x2) : "h"(pair));
+      const float a = __half2float(__ushort_as_half(static_cast<unsigned short>(f16x2 & 0xFFFFu)));
+      const float b = __half2float(__ushort_as_half(static_cast<unsigned short>(f16x2 >> 16)));
+      out[2 * w + h] = pack_bf16x2(a, b);
+    }
+  }
+  lo = make_uint4(out[0], out[1], out[2], out[3]);
+  hi = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
 __device__ __forceinline__ float bf16lo_to_f32(uint32_t w) { return __uint_as_float(w << 16); }

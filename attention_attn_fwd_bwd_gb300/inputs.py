@@ -35,6 +35,24 @@ def prefill(B, Hq, Hkv, N, d, seed, with_dout=False):
     return out
 
 
+def prefill_e4m3(B, Hq, Hkv, N, d, seed):
+    """e4m3 inputs for the fp8 forward: q, k, v are drawn exactly as in ``prefill`` (fp32
+    N(0, 1), same generator order), each scaled so that its largest magnitude maps to 448 (the
+    largest finite e4m3 value) and rounded to e4m3 by torch's float8_e4m3fn conversion.
+    Returns raw bytes as torch.uint8 CPU tensors under "q", "k", "v" and the per-tensor
+    dequantisation scales (python floats) under "q_scale", "k_scale", "v_scale": the intended
+    value of a byte x is scale * e4m3(x)."""
+    g = torch.Generator("cpu").manual_seed(int(seed))
+    out = {}
+    for name, shape in (("q", (B, Hq, N, d)), ("k", (B, Hkv, N, d)), ("v", (B, Hkv, N, d))):
+        x = torch.randn(*shape, generator=g, dtype=torch.float32)
+        amax = float(x.abs().max()) if x.numel() else 1.0
+        sc = float(np.float32(max(amax, 1e-6) / 448.0))
+        out[name] = (x / sc).clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+        out[name + "_scale"] = sc
+    return out
+
+
 def decode(B, Hq, Hkv, L, d, seed):
     """bf16 CPU tensors q [B,Hq,d], k_cache, v_cache [B,Hkv,L,d]."""
     g = torch.Generator("cpu").manual_seed(int(seed))

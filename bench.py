@@ -53,13 +53,16 @@ def parse():
                     help="the paper's GPT-2-small forwards and Llama-3-8B / Mistral-7B decodes")
     ap.add_argument("--decode", action="store_true",
                     help="split-KV decode at the Llama-3-70B head shape (B=1, 8; splits sweep)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="e4m3 forward at the Llama-3-8B shape (causal, no RoPE) vs the bf16 one")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the nested records of the other workloads and the steady-state run")
     ap.add_argument("--profile", action="store_true",
                     help="one warm-up call and one call of the workload, then exit (for ncu)")
     ap.add_argument("--profile-target", default="fwd",
-                    choices=["fwd", "decode", "decode-b1", "train", "train-prerotate", "d64-causal"],
+                    choices=["fwd", "decode", "decode-b1", "train", "train-prerotate", "d64-causal",
+                             "fp8"],
                     help="--profile: forward workload, Llama-3-70B decode (B=8), fwd+bwd (N=2048) "
                          "or the head-dim-64 causal forward (B=2, H=16, N=4096, fused RoPE)")
     return ap.parse_args()
@@ -248,12 +251,13 @@ def secondary_configs(args, local):
     (B=2, H=16, N=4096, d=64: window 1024 + causal, ALiBi + causal, BigBird, causal), the
     training step (B=8, Hq=32, Hkv=8, d=128, N=2048 and 4096: forward, backward fused and
     pre-rotated), the Llama-3-70B-shaped split-KV decode (B=1 and 8, splits auto/1/8/32/128,
-    cold and warm L2) and the fused / pre-rotated crossover sweep of the head-dim-128 forward
-    (B*N = 16384, N = 256 .. 16384)."""
+    cold and warm L2), the e4m3 forward at the Llama-3-8B shape and the fused / pre-rotated
+    crossover sweep of the head-dim-128 forward (B*N = 16384, N = 256 .. 16384)."""
     out = {}
     for key, fn in (("mask_variants_d64", lambda: run_variants_bench(args, emit=False)),
                     ("training_fwd_bwd", lambda: run_train_bench(args, emit=False)),
                     ("decode_llama70b_head_shape", lambda: run_decode_bench(args, emit=False)),
+                    ("fp8_e4m3_forward_d128", lambda: run_fp8_bench(args, emit=False)),
                     ("rotation_calculus_d128", lambda: run_sweep(args, quick=True, emit=False))):
         clk = ClockSampler(local)
         clk.start()
@@ -542,6 +546,11 @@ def run_profile(args):
         for _ in range(2):
             out, lse = af.fwd(q, k, v, rope_theta=5e5)
             af.bwd(q, k, v, out, lse, do, rope_theta=5e5, rope_mode=mode)
+    elif args.profile_target == "fp8":
+        x = inputs.prefill_e4m3(4, 32, 8, 4096, 128, seed=8000)
+        q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
+        for _ in range(2):
+            af.fwd_fp8(q, k, v, x["q_scale"], x["k_scale"], x["v_scale"])
     elif args.profile_target == "d64-causal":
         x = inputs.prefill(2, 16, 16, 4096, 64, seed=3000)
         q, k, v = (x[n].cuda() for n in ("q", "k", "v"))
@@ -699,6 +708,64 @@ def run_variants_bench(args, emit=True):
         if emit:
             print(json.dumps(rows[-1]), flush=True)
     return rows
+
+
+def run_fp8_bench(args, emit=True):
+    """e4m3 forward (per-tensor scales, no RoPE, causal) at B=4, Hq=32, Hkv=8, N=4096, d=128,
+    beside the bf16 forward without RoPE on the same values; three input sets rotate so no call
+    finds its operands in L2 from the call before. The fp8 peak is the measured bf16 GEMM peak
+    times the nominal fp8/bf16 ratio (2); only the score half of the FLOPs runs at the fp8
+    rate (P V is a bf16 MMA), so the mixed peak, 1 / (0.5 / fp8 + 0.5 / bf16), is reported
+    too."""
+    import torch
+
+    import attention_attn_fwd_bwd_gb300 as af
+    from attention_attn_fwd_bwd_gb300 import inputs
+
+    dev = torch.device("cuda")
+    peaks, _ = measured_peaks()
+    bf16_peak = float(peaks["bf16_tflops"])
+    fp8_peak = 2.0 * bf16_peak
+    mixed_peak = 1.0 / (0.5 / fp8_peak + 0.5 / bf16_peak)
+    B, Hq, Hkv, N, d = 4, 32, 8, 4096, 128
+    sets = []
+    for i in range(3):
+        x = inputs.prefill_e4m3(B, Hq, Hkv, N, d, seed=8000 + i)
+        sets.append(((x["q"].to(dev), x["k"].to(dev), x["v"].to(dev)),
+                     (x["q_scale"], x["k_scale"], x["v_scale"])))
+    ws = torch.empty(af.fwd_fp8_workspace_size(B, Hq, Hkv, N, d), dtype=torch.uint8, device=dev)
+    out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    it = [0]
+
+    def call_fp8():
+        (q, k, v), sc = sets[it[0] % 3]
+        it[0] += 1
+        af.fwd_fp8(q, k, v, *sc, out=out, lse=lse, workspace=ws)
+
+    t, tmin, tp90 = _time_ms(call_fp8, reps=60, warm=5)
+    # the bf16 forward (no RoPE) on bf16 copies of the same decoded values
+    bsets = []
+    for (q, k, v), (sq, sk, sv) in sets:
+        bsets.append(tuple((t8.view(torch.float8_e4m3fn).float() * s).to(torch.bfloat16)
+                           for t8, s in ((q, sq), (k, sk), (v, sv))))
+
+    def call_bf16():
+        q, k, v = bsets[it[0] % 3]
+        it[0] += 1
+        af.fwd(q, k, v, rope_mode=af.ROPE_NONE, out=out, lse=lse)
+
+    tb, _, _ = _time_ms(call_bf16, reps=60, warm=5)
+    fl = causal_flops(B, Hq, N, d)
+    row = {"workload": "e4m3 forward, causal, no RoPE (B=4, Hq=32, Hkv=8, N=4096, d=128)",
+           "ms": t, "min_ms": tmin, "p90_ms": tp90, "tflops": fl / t / 1e9,
+           "fp8_peak_tflops": fp8_peak, "frac_of_fp8_peak": fl / t / 1e9 / fp8_peak,
+           "mixed_peak_tflops": mixed_peak, "frac_of_mixed_peak": fl / t / 1e9 / mixed_peak,
+           "bf16_none_ms": tb, "bf16_none_tflops": fl / tb / 1e9,
+           "peak_source": "measured bf16 burst (MEASURED_PEAKS.json) x nominal fp8/bf16 ratio 2"}
+    if emit:
+        print(json.dumps(row), flush=True)
+    return [row]
 
 
 def _graph_of(fn):
@@ -884,6 +951,10 @@ def main():
     if args.variants:
         if rank == 0:
             run_variants_bench(args)
+        return
+    if args.fp8:
+        if rank == 0:
+            run_fp8_bench(args)
         return
     if args.tables:
         if rank == 0:

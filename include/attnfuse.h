@@ -169,6 +169,34 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
                              size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
+ * e4m3 (fp8) forward (paper §9.1 future work: low-precision attention), head dim 128.
+ * q: [B, Hq, N, 128], k, v: [B, Hkv, N, 128], all e4m3 (OCP FP8 E4M3: 1 sign, 4 exponent bits
+ * with bias 7, 3 mantissa bits, no infinities; S.1111.111 is NaN), one byte per element,
+ * element strides multiples of 16, innermost stride 1, 16-byte aligned. The values the call
+ * attends over are q_scale * q, k_scale * k and v_scale * v (per-tensor dequantisation scales,
+ * positive and finite); out (bf16) and lse (fp32, or NULL) are as in attnfuse_fwd.
+ * The scores S = Q K^T run on tcgen05 kind::f8f6f4 MMAs (exact products, fp32 accumulation);
+ * q_scale * k_scale * scale is applied with the softmax scale. V is widened to bf16 (exact)
+ * once per call into the workspace and P V runs as in the bf16 forward; v_scale multiplies O.
+ * No RoPE: q and k are used as given (a caller with rotary positions quantises the rotated
+ * tensors). variant: as attnfuse_fwd (all masks, ALiBi, additive bias, both normalisers).
+ * Workspace: attnfuse_fwd_fp8_workspace_size bytes (the widened V, B*Hkv*N*256 bytes, and one
+ * 32-bit flag per 128-key x 64-dim block, zeroed by every call with cudaMemsetAsync).
+ * Errors: ATTNFUSE_ERR_UNSUPPORTED for d != 128; ATTNFUSE_ERR_INVALID_ARG for bad pointers,
+ * strides or scales; ATTNFUSE_ERR_WORKSPACE_TOO_SMALL.
+ * ------------------------------------------------------------------------------------------ */
+attnfuse_status attnfuse_fwd_fp8_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                                size_t* bytes);
+
+attnfuse_status attnfuse_fwd_fp8(const void* q, const int64_t q_strides[4], const void* k,
+                                 const int64_t k_strides[4], const void* v,
+                                 const int64_t v_strides[4], void* out, const int64_t o_strides[4],
+                                 float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                                 float q_scale, float k_scale, float v_scale,
+                                 const attnfuse_variant* variant, void* workspace,
+                                 size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
  * Backward (paper §4.4): preprocess D = rowsum(dO * O), a dK/dV kernel and a dQ kernel, no
  * atomics. Gradients are with respect to the un-rotated q and k (the inverse rotation is
  * applied in the epilogues) and dk, dv are summed over each GQA group.

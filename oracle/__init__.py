@@ -246,6 +246,22 @@ def decode(q, kc, vc, q_pos, scale, theta, rope_q=True):
     return out, lse
 
 
+def decode_e4m3(x):
+    """Values of e4m3 bytes (the fp8 forward's operand format) as float64, from the OCP 8-bit
+    floating-point definition of E4M3: byte s eeee mmm encodes (-1)^s 2^(e-7) (1 + m/8) for
+    e > 0 and (-1)^s 2^(-6) (m/8) for e = 0 (subnormals); eeee mmm = 1111 111 is NaN and there
+    are no infinities. The pages name fp8 attention as future work without fixing a format;
+    E4M3 is the plainest reading (the tensor cores' fp8 operand format with the wider range
+    of mantissa). x: any integer array of bytes (0..255)."""
+    b = np.asarray(x).astype(np.int64) & 0xFF
+    sign = np.where(b & 0x80, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    mag = np.where(e > 0, np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64)), np.ldexp(m / 8.0, -6))
+    out = sign * mag
+    return np.where((b & 0x7F) == 0x7F, np.nan, out)
+
+
 def tile_visits(N, BM, BN, variant: Variant):
     """uint8 [ceil(N/BM), ceil(N/BN)]: 1 where the tile holds at least one allowed pair."""
     TQ, TK = -(-N // BM), -(-N // BN)

@@ -88,6 +88,10 @@ def test_workspace_sizes(lib):
     assert n.value == 4096 * 64 * 8 + 4 * 32 * 4096 * 128 * 2 + 4 * 8 * 4096 * 128 * 2
     assert lib.attnfuse_fwd_workspace_size(1, 2, 2, 10, 64, 1, ctypes.byref(n)) == OK
     assert n.value == 128 * 32 * 8  # the table always covers 128 positions
+    # e4m3 forward: the widened V (bf16) and one flag per 128-key x 64-dim block
+    assert lib.attnfuse_fwd_fp8_workspace_size(4, 32, 8, 4096, 128, ctypes.byref(n)) == OK
+    assert n.value == 4 * 8 * 4096 * 128 * 2 + 4 * 8 * 2 * 32 * 4
+    assert lib.attnfuse_fwd_fp8_workspace_size(4, 32, 8, 4096, 64, ctypes.byref(n)) == UNSUPPORTED
     assert lib.attnfuse_bwd_workspace_size(8, 32, 8, 2048, 128, 1, ctypes.byref(n)) == OK
     assert n.value == 2048 * 64 * 8 + 8 * 32 * 2048 * 4
     assert lib.attnfuse_decode_workspace_size(1, 64, 8, 32768, 128, 8, ctypes.byref(n)) == OK

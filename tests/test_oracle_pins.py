@@ -484,3 +484,25 @@ def test_relu_attention_closed_forms(orc):
         o3, _ = orc.forward(3.0 * q, kk, v, scale, 1e4, rope_on, orc.Variant(mask=orc.MASK_FULL, norm=orc.NORM_RELU))
         assert np.allclose(o3, 3.0 * o1, rtol=0, atol=1e-12)
         assert not np.allclose(o1, 0.0)
+
+
+def test_decode_e4m3_closed_forms_and_library():
+    """E4M3 (OCP 8-bit floating point): 1.0 = 0 0111 000, the largest finite value 448 =
+    0 1111 110, the smallest subnormal 2^-9 = 0 0000 001, the smallest normal 2^-6, sign bit,
+    NaN at x 1111 111; and all 256 codes against torch's float8_e4m3fn widening (an
+    independent library routine)."""
+    import oracle
+
+    d = oracle.decode_e4m3
+    assert d(0x38) == 1.0 and d(0xB8) == -1.0
+    assert d(0x7E) == 448.0 and d(0xFE) == -448.0
+    assert d(0x01) == 2.0 ** -9 and d(0x07) == 7 * 2.0 ** -9
+    assert d(0x08) == 2.0 ** -6 and d(0x0F) == 2.0 ** -6 * 1.875
+    assert d(0x00) == 0.0 and np.signbit(d(0x80))
+    assert np.isnan(d(0x7F)) and np.isnan(d(0xFF))
+    b = np.arange(256)
+    ref = torch.tensor(b, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    got = d(b)
+    assert np.array_equal(np.isnan(ref), np.isnan(got))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ref[fin], got[fin])
