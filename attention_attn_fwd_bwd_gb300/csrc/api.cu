@@ -143,9 +143,21 @@ size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // The table always covers at least 128 positions: the fused key rotation reads the entry of
 // position 128 / (d / 16) as its per-row step.
 int rope_table_rows(int N) { return N < 128 ? 128 : N; }
-// Head-dim-128 forward with fused RoPE: the rotated keys (fp16) and one flag per 64-key block.
+// Forward with fused RoPE: the rotated keys (fp16) and one flag per 64-key block (head dim 128;
+// head dim 64 uses one per 128-key tile, fewer).
 size_t fused_k_bytes(int B, int Hkv, int N, int d) {
   return align_up((size_t)B * Hkv * N * d * 2, 256);
+}
+// Head dim 64 (one CTA per 256 query rows, not persistent): rotating each K tile once and
+// sharing it through L2 pays when many query tiles re-read it; with few readers the copy's
+// latency on the first reader's path costs more than rotating K stages in place per CTA.
+// Measured on GB300 (B*N = 16384, H=16, causal): in place 0.166 / 0.241 ms at N = 1024 /
+// 2048, shared 0.187 / 0.239; at N = 4096 shared wins for causal, ALiBi and BigBird and
+// loses for a 1024-key window (0.161 vs 0.151 ms).
+bool share_rotated_k_d64(int N, const VariantDev& v) {
+  if (N < 2048) return false;
+  if (v.mask == 2 && v.window < 2048) return false;
+  return true;
 }
 size_t fused_sync_bytes(int B, int Hkv, int N) {
   return align_up((size_t)B * Hkv * ((N + 63) / 64) * sizeof(uint32_t), 256);
@@ -255,12 +267,13 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
 // ATTNFUSE_ROPE_AUTO: the faster of on-chip rotation and pre-rotation, by the crossover
 // N* measured on GB300 (the paper's Rotation Calculus, §5.3; B*N = 16384 tokens, causal).
 // The pre-rotation pass streams at ~5 TB/s, so it costs ~70 us per 16k-token, 32-head call.
-// Head dim 64: fusion wins below N* ~ 1.9k (forward; t_prerotate / t_fused = 1.22 at N = 256,
-// 0.99 at 2048) and ~ 260 (backward, which re-reads each K tile once per query tile). Head
+// Head dim 64: fusion wins below N* ~ 3.2k (forward; t_prerotate / t_fused = 1.23 at N = 256,
+// 1.08 at 1024, 1.00 at 2048 and 4096, 0.99 at 8192) and ~ 260 (backward, which re-reads each
+// K tile once per query tile). Head
 // dim 128: the persistent forward rotates each K block once per call (shared through L2) and
 // each Q tile in shared memory, and wins below N* ~ 14k (1.13 at N = 256, 1.06 at 2048, 1.02
 // at 4096, 1.00 at 16384); the backward pre-rotates at every N.
-constexpr int kAutoFusedBelowN64Fwd = 1900;
+constexpr int kAutoFusedBelowN64Fwd = 3160;
 constexpr int kAutoFusedBelowN64Bwd = 258;
 constexpr int kAutoFusedBelowN128Fwd = 14000;
 
@@ -294,7 +307,7 @@ attnfuse_status attnfuse_fwd_workspace_size(int B, int Hq, int Hkv, int N, int d
     n += align_up((size_t)B * Hq * N * d * 2, 256);
     n += align_up((size_t)B * Hkv * N * d * 2, 256);
   }
-  if (rope_mode == ATTNFUSE_ROPE_FUSED && d == 128) n += fused_k_bytes(B, Hkv, N, d) + fused_sync_bytes(B, Hkv, N);
+  if (rope_mode == ATTNFUSE_ROPE_FUSED) n += fused_k_bytes(B, Hkv, N, d) + fused_sync_bytes(B, Hkv, N);
   if (rope_mode < 0 || rope_mode > 2) return fail(ATTNFUSE_ERR_INVALID_ARG, "rope mode %d", rope_mode);
   *bytes = n;
   return ok();
@@ -386,9 +399,10 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
     qa = qr; ka = kr; qs = qs_c; ks = ks_c;
   }
-  if (rope_mode == ATTNFUSE_ROPE_FUSED && d == 128) {
-    // K is rotated once per 64-key block inside the forward (by whichever CTA needs the block
-    // first) into a workspace copy that every CTA then loads with TMA
+  if (rope_mode == ATTNFUSE_ROPE_FUSED && (d == 128 || share_rotated_k_d64(N, p.var))) {
+    // K is rotated once per call inside the forward, per 64-key block (head dim 128) or
+    // 128-key tile (head dim 64), by whichever CTA needs it first, into a workspace copy that
+    // every CTA then loads with TMA
     uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
     p.k_raw = static_cast<const __nv_bfloat16*>(k);
     p.k_sb = k_strides[0]; p.k_sh = k_strides[1]; p.k_sn = k_strides[2];

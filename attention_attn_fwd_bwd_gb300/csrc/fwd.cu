@@ -9,8 +9,10 @@
 //   warp 1      MMA issuer: S_s = Q_s K^T and O_s += P_s V with tcgen05.mma, TMEM accumulators
 //   warps 4-7   softmax for sub-tile 0 (one thread per query row)
 //   warps 8-11  softmax for sub-tile 1
-//   warps 12-15 K rotators (fused RoPE): rotate each K stage in shared memory in place, one
-//               warp per SM sub-partition; (cos, sin) advance down the rows by angle addition
+//   warps 12-15 K rotators (fused RoPE): rotate each 128-key tile of K once per call (by
+//               whichever CTA claims it first) into an fp16 workspace copy K' that the
+//               producers load with TMA, or (short or windowed sequences) each CTA's K stages
+//               in shared memory in place; (cos, sin) advance down the rows by angle addition
 // Registers are re-balanced with setmaxnreg: 64 (producers), 80 (rotators), 184 (softmax).
 // TMEM columns: S0 [0,128), S1 [128,256), O0 [256,256+D), O1 [256+D, 256+2D); P_s (bf16)
 // overwrites the first 64 columns of S_s. Every wait is bounded (see ptx.cuh).
@@ -115,6 +117,9 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const VariantDev& var = p.var;
   constexpr bool ROPE = (RK == kRopeFused);
+  // fused RoPE, K rotated once per call into the workspace copy K' (the host picks this when
+  // K tiles are re-read by enough query tiles), else each CTA rotates its K stages in place
+  const bool kshare = ROPE && p.k_rot != nullptr;
 
   // ---------------- work unit ----------------
   const int per_t = p.B * p.pairs;
@@ -230,6 +235,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             go = false;
             break;
           }
+          // fused RoPE: K' of tile jk, rotated once per call by whichever CTA claimed it
+          if (kshare && !flag_wait(p.k_sync + (b * p.Hkv + kvh) * TK + jk, 2u, status, abort_flag)) {
+            go = false;
+            break;
+          }
           mbar_arrive_expect_tx(&ctl->k_full[s], C::TILE);
           for (int pn = 0; pn < C::PANELS; ++pn)
             tma_load_4d_hint(smem + C::OFF_K + s * C::TILE + pn * (BN * 128), &p.tmK,
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       bool pv_pend[2] = {false, false};
       int j = next_tile(ctl, p, jb, je);
       if (ok && j < je) {
-        ok = mbar_wait(ROPE ? &ctl->k_ready[0] : &ctl->k_full[0], 0, status, abort_flag);
+        ok = mbar_wait((ROPE && !kshare) ? &ctl->k_ready[0] : &ctl->k_full[0], 0, status, abort_flag);
         tc_fence_after();
         if (ok) {
           for (int s = 0; s < 2; ++s)
@@ -318,8 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           if (s == 1) mma_commit(&ctl->v_empty[vs]);
           if (jn < je && tile_active(ctl, p, s, jn)) {
             if (!kready) {
-              if (!mbar_wait(ROPE ? &ctl->k_ready[kn] : &ctl->k_full[kn], ((i + 1) / KST) & 1,
-                             status, abort_flag)) { ok = false; break; }
+              if (!mbar_wait((ROPE && !kshare) ? &ctl->k_ready[kn] : &ctl->k_full[kn],
+                             ((i + 1) / KST) & 1, status, abort_flag)) {
+                ok = false;
+                break;
+              }
               kready = true;
             }
             if (pv_pend[s]) {
@@ -340,7 +353,96 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
   } else if (warp >= 12) {
     // ======================= K rotators (fused RoPE) =======================
     setmaxnreg_dec<kRegsRotator>();
-    if (ROPE) {
+    if (ROPE && kshare) {
+      // K' = R_n K is made once per 128-key tile and call: the four rotator warps walk this
+      // CTA's tiles, warp w taking every fourth; the first warp of any CTA to claim a tile (a
+      // compare-and-swap on its flag: 0 untouched, 1 claimed, 2 done) rotates it from global
+      // memory into the fp16 copy in the workspace and releases the flag, and the producer
+      // copies K' with TMA once the flag reads 2. A claimed tile is finished by a warp that
+      // waits on nothing, and an unclaimed one by this CTA's own rotators, so no wait is
+      // endless. Lane (c, rl) rotates chunk pair c (dims 8c.., D/2+8c..) of rows rg + RG k
+      // of the chains rg = rl + 8i, each starting from its table entry and stepping the
+      // (cos, sin) of RG positions per row (the chains of the pre-rotation pass, so K' is
+      // bit-identical to its output).
+      constexpr int CP = D / 16;    // chunk pairs per row
+      constexpr int RG = 128 / CP;  // chains per tile; a chain holds rows rg, rg + RG, ...
+      static_assert(CP == 4, "the rotator lane map assumes head dim 64");
+      constexpr uint64_t kSign2 = 0x8000000080000000ull;
+      const int wr = warp - 12;
+      const int c = lane & 3, rl = lane >> 2;
+      const int kN = p.N;
+      uint64_t wc2[4], ws2[4], nws2[4];
+      {
+        float wc[8], ws[8];
+        load_cs8(p.rope_cs + (size_t)RG * (D / 2) + c * 8, wc, ws);
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          wc2[w] = f2_pack(wc[2 * w], wc[2 * w + 1]);
+          ws2[w] = f2_pack(ws[2 * w], ws[2 * w + 1]);
+          nws2[w] = ws2[w] ^ kSign2;
+        }
+      }
+      const uint64_t pol_tab = l2_policy_evict_last();
+      const uint64_t pol_in = l2_policy_evict_first();
+      const uint64_t pol_out = l2_policy_evict_last();
+      const int bh = b * p.Hkv + kvh;
+      const __nv_bfloat16* src = p.k_raw + b * p.k_sb + kvh * p.k_sh;
+      uint16_t* dst = p.k_rot + (int64_t)bh * kN * D;
+      int i = 0;
+      for (int j = next_tile(ctl, p, jb, je); j < je; j = next_tile(ctl, p, j + 1, je), ++i) {
+        if ((i & 3) != wr) continue;
+        uint32_t* flag = p.k_sync + bh * TK + j;
+        uint32_t mine = 0;
+        if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(flag) == 0u)
+          mine = atomicCAS(flag, 0u, 1u) == 0u ? 1u : 0u;
+        if (!__shfl_sync(0xffffffffu, mine, 0)) continue;
+        const int n0 = j * BN;
+#pragma unroll 1
+        for (int ci = 0; ci < RG / 8; ++ci) {
+          const int rg = rl + 8 * ci;
+          float4 pre[4];
+          {
+            const float4* t = reinterpret_cast<const float4*>(
+                p.rope_cs + (size_t)min(n0 + rg, kN - 1) * (D / 2) + c * 8);
+#pragma unroll
+            for (int w = 0; w < 4; ++w) pre[w] = ldg_f4_hint(t + w, pol_tab);
+          }
+          uint4 lo[CP], hi[CP];
+#pragma unroll
+          for (int k = 0; k < CP; ++k) {
+            const __nv_bfloat16* row = src + (int64_t)min(n0 + rg + RG * k, kN - 1) * p.k_sn + c * 8;
+            lo[k] = ldg_u4_hint(row, pol_in);
+            hi[k] = ldg_u4_hint(row + D / 2, pol_in);
+          }
+          uint64_t c2[4], s2[4], ns2[4];
+#pragma unroll
+          for (int w = 0; w < 4; ++w) {
+            c2[w] = f2_pack(pre[w].x, pre[w].z);
+            s2[w] = f2_pack(pre[w].y, pre[w].w);
+            ns2[w] = s2[w] ^ kSign2;
+          }
+#pragma unroll
+          for (int k = 0; k < CP; ++k) {
+            rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
+            if (k + 1 < CP) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
+          }
+#pragma unroll
+          for (int k = 0; k < CP; ++k) {
+            const int n = n0 + rg + RG * k;
+            if (n < kN) {
+              uint16_t* out = dst + (int64_t)n * D + c * 8;
+              stg_u4_hint(out, lo[k], pol_out);
+              stg_u4_hint(out + D / 2, hi[k], pol_out);
+            }
+          }
+        }
+        fence_proxy_async_global();
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) st_release_gpu(flag, 2u);
+      }
+    } else if (ROPE) {
+      // each CTA rotates its own K stages in place after they land
       constexpr int CP = D / 16;    // chunk pairs per row
       constexpr int RG = 128 / CP;  // row groups; a thread owns rows rg, rg + RG, ...
       const int rt = tid - 384;

@@ -128,6 +128,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
   }
 }
 
+// Bounded wait until a global flag that another CTA releases reads `want`; then this thread's
+// later TMA copies see what was written before the release. Same failure contract as mbar_wait.
+__device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t want, int* status,
+                                          volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t spins = 0;
+  while (true) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == want) {
+      asm volatile("fence.proxy.async.global;" ::: "memory");
+      return true;
+    }
+    __nanosleep(64);
+    if ((++spins & 63u) == 0) {
+      if (abort_flag && *abort_flag) return false;
+      if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
+        if (status) atomicExch(status, kDevTimeout);
+        if (abort_flag) *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // Thread-block clusters: rank, cluster-wide barrier, mbarriers of another CTA of the cluster
 // ---------------------------------------------------------------------------------------------

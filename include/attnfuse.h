@@ -61,10 +61,10 @@ typedef int attnfuse_status;
 typedef enum {
   ATTNFUSE_ROPE_NONE = 0,      /* no rotation: plain scaled_dot_product */
   ATTNFUSE_ROPE_FUSED = 1,     /* rotate inside the attention kernel: each Q tile once in
-                                  shared memory; K per tile in shared memory (head dim 64) or,
-                                  for head dim 128, each 64-key block once per call by the
-                                  first CTA that needs it, into a workspace copy K' that every
-                                  CTA reads from L2 (no separate pass, no Q' round trip) */
+                                  shared memory; each block of K (64 keys at head dim 128, 128
+                                  at 64) once per call by the first CTA that needs it, into a
+                                  workspace copy K' that every CTA reads from L2 (no separate
+                                  pass, no Q' round trip) */
   ATTNFUSE_ROPE_PREROTATE = 2, /* separate rotate kernel writes Q', K' to the workspace, then
                                   attention runs without rotation (the paper's baseline) */
   ATTNFUSE_ROPE_AUTO = 3       /* the faster of FUSED and PREROTATE for this call's N, head dim
@@ -154,9 +154,9 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
  * q: [B, Hq, N, d]; k, v: [B, Hkv, N, d]; out: [B, Hq, N, d]; lse: [B, Hq, N] or NULL.
  * variant: NULL means causal with no bias. Fully masked (q-tile, kv-tile) pairs are skipped.
  * ------------------------------------------------------------------------------------------ */
-/* Workspace: NONE none; FUSED the (cos, sin) table, plus for head dim 128 the rotated keys
- * (fp16, B*Hkv*N*d*2 bytes) and one 32-bit flag per 64-key block (zeroed by every call with
- * cudaMemsetAsync on `stream`); PREROTATE the table, Q' and K'. */
+/* Workspace: NONE none; FUSED the (cos, sin) table, the rotated keys (fp16, B*Hkv*N*d*2
+ * bytes) and one 32-bit flag per 64 keys (zeroed by every call with cudaMemsetAsync on
+ * `stream`); PREROTATE the table, Q' and K'. */
 attnfuse_status attnfuse_fwd_workspace_size(int B, int Hq, int Hkv, int N, int d,
                                             attnfuse_rope_mode rope_mode, size_t* bytes);
 
@@ -286,7 +286,7 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
 
 /* The mode ATTNFUSE_ROPE_AUTO resolves to for sequence length N and head dim d, for the
  * forward (backward = 0) or the backward (backward = 1). Measured on GB300 with B*N = 16384
- * tokens, causal: fusion wins for head dim 64 below N ~ 1.9k (forward) and N ~ 260
+ * tokens, causal: fusion wins for head dim 64 below N ~ 3.2k (forward) and N ~ 260
  * (backward), and for the head-dim-128 forward below N ~ 14k; above those, and for the
  * head-dim-128 backward at every N, the pre-rotation pass is cheaper than rotating K tiles on
  * chip. The workspace size functions accept ATTNFUSE_ROPE_AUTO and size for the resolved mode. */

@@ -87,7 +87,9 @@ def test_workspace_sizes(lib):
     assert lib.attnfuse_fwd_workspace_size(4, 32, 8, 4096, 128, 2, ctypes.byref(n)) == OK
     assert n.value == 4096 * 64 * 8 + 4 * 32 * 4096 * 128 * 2 + 4 * 8 * 4096 * 128 * 2
     assert lib.attnfuse_fwd_workspace_size(1, 2, 2, 10, 64, 1, ctypes.byref(n)) == OK
-    assert n.value == 128 * 32 * 8  # the table always covers 128 positions
+    # the table always covers 128 positions; K' (10 x 64 fp16 per head, 256-byte aligned) and
+    # one flag per 64 keys (256-byte aligned)
+    assert n.value == 128 * 32 * 8 + 2 * 10 * 64 * 2 + 256
     # e4m3 forward: the widened V (bf16) and one flag per 128-key x 64-dim block
     assert lib.attnfuse_fwd_fp8_workspace_size(4, 32, 8, 4096, 128, ctypes.byref(n)) == OK
     assert n.value == 4 * 8 * 4096 * 128 * 2 + 4 * 8 * 2 * 32 * 4
@@ -159,8 +161,8 @@ def test_rope_auto_mode_rule(lib):
     # backward pre-rotates at every N
     assert auto(256, 128, 0) == (OK, FUSED) and auto(13999, 128, 0) == (OK, FUSED)
     assert auto(14000, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
-    # head dim 64: fusion wins below the measured crossovers (forward 1900, backward 258)
-    assert auto(1899, 64, 0) == (OK, FUSED) and auto(1900, 64, 0) == (OK, PRE)
+    # head dim 64: fusion wins below the measured crossovers (forward 3160, backward 258)
+    assert auto(3159, 64, 0) == (OK, FUSED) and auto(3160, 64, 0) == (OK, PRE)
     assert auto(257, 64, 1) == (OK, FUSED) and auto(258, 64, 1) == (OK, PRE)
     assert lib.attnfuse_rope_auto_mode(0, 64, 0, ctypes.byref(m)) == INVALID
     assert lib.attnfuse_rope_auto_mode(512, 80, 0, ctypes.byref(m)) == UNSUPPORTED

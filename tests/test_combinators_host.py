@@ -66,15 +66,15 @@ def test_relu_attention_maps_to_the_relu_normaliser():
 
 def test_rope_auto_rule():
     """The measured crossover (GB300, B*N = 16384): fusion wins for head dim 64 below
-    N ~ 1.9k (forward) and ~ 260 (backward), for the head-dim-128 forward below N ~ 14k;
+    N ~ 3.2k (forward) and ~ 260 (backward), for the head-dim-128 forward below N ~ 14k;
     pre-rotation everywhere else."""
     from attention_attn_fwd_bwd_gb300 import _build
 
     _build.build()
     af.load()
-    for N in (1, 128, 1024, 1899):
+    for N in (1, 128, 1024, 3159):
         assert af.rope_auto_mode(N, 64) == af.ROPE_FUSED
-    for N in (1900, 2048, 65536):
+    for N in (3160, 4096, 65536):
         assert af.rope_auto_mode(N, 64) == af.ROPE_PREROTATE
     for N in (1, 128, 257):
         assert af.rope_auto_mode(N, 64, backward=True) == af.ROPE_FUSED
