@@ -28,7 +28,7 @@ MASK_FULL, MASK_CAUSAL, MASK_WINDOW, MASK_BLOCK_SPARSE = 0, 1, 2, 3
 BIAS_NONE, BIAS_ALIBI, BIAS_ADDITIVE = 0, 1, 2
 NORM_SOFTMAX, NORM_RELU = 0, 1
 _STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE_TOO_SMALL",
-           4: "CUDA_ERROR", 5: "TIMEOUT"}
+           4: "CUDA_ERROR", 5: "TIMEOUT", 6: "FP16_RANGE"}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_lib", "libattnfuse.so")
@@ -102,6 +102,8 @@ def load():
             "attnfuse_rope_table": ([P, S, I, I, F, P], I),
             "attnfuse_rope_auto_mode": ([I, I, I, ctypes.POINTER(I)], I),
             "attnfuse_fwd_fp8_workspace_size": ([I, I, I, I, I, ctypes.POINTER(S)], I),
+            "attnfuse_fwd_host_workspace_size": ([I, I, I, I, I, I, I, ctypes.POINTER(S)], I),
+            "attnfuse_fwd_host": ([P, P, P, P, P, I, I, I, I, I, F, F, I, VP, I, P, S, P], I),
             "attnfuse_fwd_fp8": ([P, ST, P, ST, P, ST, P, ST, P, I, I, I, I, I, F, F, F, F, VP,
                                   P, S, P], I),
         }
@@ -362,6 +364,63 @@ def fwd(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=N
     return out, lse
 
 
+def fwd_host_workspace_size(B, Hq, Hkv, N, d, rope_mode, chunk_b):
+    n = ctypes.c_size_t()
+    _check(load().attnfuse_fwd_host_workspace_size(B, Hq, Hkv, N, d, rope_mode, chunk_b,
+                                                   ctypes.byref(n)))
+    return n.value
+
+
+def fwd_host(q, k, v, scale=None, rope_theta=10000.0, rope_mode=ROPE_FUSED, variant=None,
+             out=None, lse=None, with_lse=True, chunk_b=1, workspace=None, device=None,
+             stream=None, sync=True):
+    """Forward on CPU tensors (contiguous bf16; pinned memory lets the copies overlap): the
+    batch is copied in, attended and copied out in chunks of chunk_b elements, the copies of
+    one chunk overlapping the forward of the next. Returns CPU (out, lse); with sync=False the
+    results are valid once the device stream has reached this point."""
+    import torch
+
+    bf16, f32 = (torch.bfloat16,), (torch.float32,)
+    for t, name in ((q, "q"), (k, "k"), (v, "v")):
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+            raise ValueError(f"{name}: expected a CPU tensor")
+        if t.dtype not in bf16:
+            raise TypeError(f"{name}: dtype {t.dtype}, expected torch.bfloat16")
+        if t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous [B, H, N, d] tensor")
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if tuple(k.shape) != (B, Hkv, N, d) or tuple(v.shape) != (B, Hkv, N, d):
+        raise ValueError("k, v: expected [B, Hkv, N, d] matching q")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if scale is None:
+        scale = d ** -0.5
+    pin = q.is_pinned()
+    if out is None:
+        out = torch.empty((B, Hq, N, d), dtype=torch.bfloat16, pin_memory=pin)
+    relu = variant is not None and variant.norm == NORM_RELU
+    if with_lse and lse is None and not relu:
+        lse = torch.empty((B, Hq, N), dtype=torch.float32, pin_memory=pin)
+    for t, name, dt, shape in ((out, "out", bf16, (B, Hq, N, d)), (lse, "lse", f32, (B, Hq, N))):
+        if t is None:
+            continue
+        if t.device.type != "cpu" or t.dtype not in dt or tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{name}: expected a contiguous CPU {dt[0]} tensor of shape {shape}")
+    if variant is not None:
+        variant.check(dev, B, Hq, N)
+    ws_n = fwd_host_workspace_size(B, Hq, Hkv, N, d, rope_mode, chunk_b)
+    ws = _workspace(ws_n, dev, workspace)
+    cv = (variant or Variant()).c_struct()
+    ctx, st = _launch_context(dev, stream)
+    with ctx:
+        _check(load().attnfuse_fwd_host(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, Hq, Hkv, N, d, float(scale),
+            float(rope_theta), rope_mode, ctypes.byref(cv), int(chunk_b), _ptr(ws), ws_n, st))
+        if sync:
+            torch.cuda.current_stream(dev).synchronize() if stream is None else stream.synchronize()
+    return out, lse
+
+
 def fwd_fp8(q, k, v, q_scale, k_scale, v_scale, scale=None, variant=None, out=None, lse=None,
             with_lse=True, workspace=None, stream=None):
     """e4m3 forward (head dim 128): q [B,Hq,N,128], k/v [B,Hkv,N,128] as torch.uint8 (raw
@@ -502,8 +561,9 @@ def rope_prerotate(x, rope_theta, out=None, workspace=None, stream=None):
 
 
 def device_status(clear=True, stream=None, device=None):
-    """Synchronise and return the device status word (0 OK, 5 TIMEOUT) of `device` (default:
-    the stream's device, else the current device)."""
+    """Synchronise and return the device status of `device` (default: the stream's device,
+    else the current device): 0 OK, 5 TIMEOUT (a kernel gave up waiting), 6 FP16_RANGE (a
+    rotating-mode forward saturated an fp16 Q' / K' element or met a non-finite input)."""
     import torch
 
     if device is None:

@@ -260,7 +260,7 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
     e = cudaMemcpy(st, &zero, sizeof(int), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return cuda_fail(e, "clear status word");
   }
-  *code = v ? ATTNFUSE_ERR_TIMEOUT : ATTNFUSE_OK;
+  *code = (v & kDevTimeout) ? ATTNFUSE_ERR_TIMEOUT : (v & kDevF16Range) ? ATTNFUSE_ERR_FP16_RANGE : ATTNFUSE_OK;
   return ok();
 }
 
@@ -331,7 +331,7 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
   float2* cs = static_cast<float2*>(workspace);
   cudaError_t e = launch_rope_table(cs, rope_table_rows(N), d / 2, make_freqs(d, rope_theta), stream);
   if (e != cudaSuccess) return cuda_fail(e, "rope table launch");
-  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, 0, stream);
+  e = launch_prerotate(x, x_strides, out, B, H, N, d, cs, false, 0, stream, nullptr);
   if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
   return ok();
 }
@@ -392,8 +392,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     uint8_t* base = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
     void* qr = base;
     void* kr = base + align_up((size_t)B * Hq * N * d * 2, 256);
-    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, -1, stream);
-    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, 1, stream);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, cs, true, -1, stream, st);
+    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, 1, stream, st);
     if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
     qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
@@ -529,6 +529,151 @@ attnfuse_status attnfuse_fwd_fp8(const void* q, const int64_t q_strides[4], cons
   return ok();
 }
 
+// ---------------------------------------------------------------------------------------------
+// Forward on host buffers: copy-in, forward and copy-out pipelined over batch chunks
+// ---------------------------------------------------------------------------------------------
+namespace {
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr;  // copy streams (the forward runs on the caller's)
+  cudaEvent_t start = nullptr, in_done[2] = {}, fwd_done[2] = {}, out_done[2] = {};
+};
+std::mutex g_pipe_mu;
+HostPipe g_pipe[64];
+
+cudaError_t host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.in) {
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess) return e;
+    for (int i = 0; i < 2; ++i) {
+      if ((e = cudaEventCreateWithFlags(&hp.in_done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&hp.fwd_done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+      if ((e = cudaEventCreateWithFlags(&hp.out_done[i], cudaEventDisableTiming)) != cudaSuccess) return e;
+    }
+  }
+  *out = &hp;
+  return cudaSuccess;
+}
+
+struct HostChunk {  // device bytes of one chunk of cb batch elements
+  size_t q, kv, o, l, ws;
+};
+HostChunk host_chunk(int cb, int Hq, int Hkv, int N, int d, size_t fwd_ws) {
+  HostChunk c;
+  c.q = align_up((size_t)cb * Hq * N * d * 2, 256);
+  c.kv = align_up((size_t)cb * Hkv * N * d * 2, 256);
+  c.o = c.q;
+  c.l = align_up((size_t)cb * Hq * N * 4, 256);
+  c.ws = align_up(fwd_ws, 256);
+  return c;
+}
+}  // namespace
+
+attnfuse_status attnfuse_fwd_host_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                                 attnfuse_rope_mode rope_mode, int chunk_b,
+                                                 size_t* bytes) {
+  if (!bytes) return fail(ATTNFUSE_ERR_INVALID_ARG, "bytes is NULL");
+  attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
+  if (rc) return rc;
+  if (chunk_b < 1 || chunk_b > B) return fail(ATTNFUSE_ERR_INVALID_ARG, "chunk_b %d (B = %d)", chunk_b, B);
+  size_t fw = 0;
+  const attnfuse_rope_mode m = static_cast<attnfuse_rope_mode>(rope_mode & ~ATTNFUSE_ROPE_REUSE_TABLE);
+  if ((rc = attnfuse_fwd_workspace_size(chunk_b, Hq, Hkv, N, d, m, &fw))) return rc;
+  const HostChunk c = host_chunk(chunk_b, Hq, Hkv, N, d, fw);
+  *bytes = 2 * (c.q + 2 * c.kv + c.o + c.l) + c.ws;
+  return ok();
+}
+
+attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, void* out, float* lse,
+                                  int B, int Hq, int Hkv, int N, int d, float scale,
+                                  float rope_theta, attnfuse_rope_mode rope_mode,
+                                  const attnfuse_variant* variant, int chunk_b, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream) {
+  if (!q || !k || !v || !out) return fail(ATTNFUSE_ERR_INVALID_ARG, "q, k, v and out must be host pointers");
+  if (rope_mode & ATTNFUSE_ROPE_REUSE_TABLE)
+    return fail(ATTNFUSE_ERR_INVALID_ARG, "the host forward builds its own table: no REUSE_TABLE");
+  size_t need = 0;
+  attnfuse_status rc = attnfuse_fwd_host_workspace_size(B, Hq, Hkv, N, d, rope_mode, chunk_b, &need);
+  if (rc) return rc;
+  if (!workspace || workspace_bytes < need || !aligned16(workspace))
+    return fail(ATTNFUSE_ERR_WORKSPACE_TOO_SMALL, "workspace needs %zu bytes (got %zu)", need,
+                workspace_bytes);
+  rope_mode = resolve_rope(rope_mode, N, d, false);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(ATTNFUSE_ERR_UNSUPPORTED, "device index %d", dev);
+  std::lock_guard<std::mutex> lk(g_pipe_mu);
+  HostPipe* hp = nullptr;
+  if ((e = host_pipe(dev, &hp)) != cudaSuccess) return cuda_fail(e, "host pipeline setup");
+  size_t fw = 0;
+  if ((rc = attnfuse_fwd_workspace_size(chunk_b, Hq, Hkv, N, d, rope_mode, &fw))) return rc;
+  const HostChunk c = host_chunk(chunk_b, Hq, Hkv, N, d, fw);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  uint8_t* fwd_ws = base + 2 * (c.q + 2 * c.kv + c.o + c.l);
+  // the copies start after what the caller queued on `stream`
+  if ((e = cudaEventRecord(hp->start, stream)) != cudaSuccess) return cuda_fail(e, "event");
+  cudaStreamWaitEvent(hp->in, hp->start, 0);
+  cudaStreamWaitEvent(hp->out, hp->start, 0);
+  const size_t q_el = (size_t)Hq * N * d, kv_el = (size_t)Hkv * N * d, l_el = (size_t)Hq * N;
+  const int TQ = (N + 127) / 128;
+  bool table_built = false;
+  for (int b0 = 0, ci = 0; b0 < B; b0 += chunk_b, ++ci) {
+    const int cb = std::min(chunk_b, B - b0);
+    const int bi = ci & 1;
+    uint8_t* set = base + bi * (c.q + 2 * c.kv + c.o + c.l);
+    void* dq = set;
+    void* dk = set + c.q;
+    void* dv = set + c.q + c.kv;
+    void* dout = set + c.q + 2 * c.kv;
+    float* dlse = lse ? reinterpret_cast<float*>(set + c.q + 2 * c.kv + c.o) : nullptr;
+    // copy-in once the forward two chunks back has read this buffer set
+    if (ci >= 2) cudaStreamWaitEvent(hp->in, hp->fwd_done[bi], 0);
+    const size_t qb = (size_t)cb * q_el * 2, kvb = (size_t)cb * kv_el * 2;
+    e = cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + (size_t)b0 * q_el * 2, qb, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + (size_t)b0 * kv_el * 2, kvb, cudaMemcpyHostToDevice, hp->in);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + (size_t)b0 * kv_el * 2, kvb, cudaMemcpyHostToDevice, hp->in);
+    if (e != cudaSuccess) return cuda_fail(e, "copy-in");
+    cudaEventRecord(hp->in_done[bi], hp->in);
+    // the forward, once its inputs are in and this buffer set's output has been copied out
+    cudaStreamWaitEvent(stream, hp->in_done[bi], 0);
+    if (ci >= 2) cudaStreamWaitEvent(stream, hp->out_done[bi], 0);
+    attnfuse_variant vc;
+    if (variant) {
+      vc = *variant;
+      if (vc.bias == ATTNFUSE_BIAS_ADDITIVE && vc.add_bias)
+        vc.add_bias = static_cast<const uint8_t*>(vc.add_bias) +
+                      (size_t)b0 * vc.add_bias_strides[0] * (vc.add_bias_is_bf16 ? 2 : 4);
+      if (vc.tile_visits) vc.tile_visits += (size_t)b0 * Hq * TQ * TQ;
+    }
+    const int64_t qs[4] = {(int64_t)q_el, (int64_t)N * d, d, 1};
+    const int64_t ks[4] = {(int64_t)kv_el, (int64_t)N * d, d, 1};
+    const int mode = rope_mode | ((rope_mode != ATTNFUSE_ROPE_NONE && table_built) ? ATTNFUSE_ROPE_REUSE_TABLE : 0);
+    rc = attnfuse_fwd(dq, qs, dk, ks, dv, ks, dout, qs, dlse, cb, Hq, Hkv, N, d, scale, rope_theta,
+                      static_cast<attnfuse_rope_mode>(mode), variant ? &vc : nullptr, fwd_ws, c.ws,
+                      stream);
+    if (rc) return rc;
+    table_built = true;
+    cudaEventRecord(hp->fwd_done[bi], stream);
+    // copy-out
+    cudaStreamWaitEvent(hp->out, hp->fwd_done[bi], 0);
+    e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + (size_t)b0 * q_el * 2, dout, qb, cudaMemcpyDeviceToHost, hp->out);
+    if (e == cudaSuccess && lse)
+      e = cudaMemcpyAsync(lse + (size_t)b0 * l_el, dlse, (size_t)cb * l_el * 4, cudaMemcpyDeviceToHost, hp->out);
+    if (e != cudaSuccess) return cuda_fail(e, "copy-out");
+    cudaEventRecord(hp->out_done[bi], hp->out);
+  }
+  // completion on the caller's stream: every copy-out has landed
+  const int nchunks = (B + chunk_b - 1) / chunk_b;
+  for (int i = 0; i < std::min(nchunks, 2); ++i) cudaStreamWaitEvent(stream, hp->out_done[(nchunks - 1 - i) & 1], 0);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "host forward");
+  return ok();
+}
+
 attnfuse_status attnfuse_rope_table(void* table, size_t table_bytes, int N, int d,
                                     float rope_theta, cudaStream_t stream) {
   if (N <= 0 || (d != 64 && d != 128))
@@ -644,8 +789,8 @@ attnfuse_status attnfuse_bwd(const void* q, const int64_t q_strides[4], const vo
     // Q' and K' once, in the backward kernels' in-tile recurrence (bit-identical to FUSED)
     void* qr = ws;
     void* kr = ws + align_up((size_t)B * Hq * N * d * 2, 256);
-    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, p.rope_cs, false, 128, stream);
-    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, p.rope_cs, false, 128, stream);
+    cudaError_t e = launch_prerotate(q, q_strides, qr, B, Hq, N, d, p.rope_cs, false, 128, stream, nullptr);
+    if (e == cudaSuccess) e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, p.rope_cs, false, 128, stream, nullptr);
     if (e != cudaSuccess) return cuda_fail(e, "prerotate launch");
     qs_c[0] = (int64_t)Hq * N * d; qs_c[1] = (int64_t)N * d; qs_c[2] = d; qs_c[3] = 1;
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;

@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(kDqThreads, 1) dq_kernel(const __grid_constant
           if (*abort_flag) {
             ok = false;
           } else if (now - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-            atomicExch(status, kDevTimeout);
+            atomicOr(status, kDevTimeout);
             *abort_flag = 1;
             ok = false;
           }

@@ -60,6 +60,21 @@ __device__ __forceinline__ void rot_chunk_cs(uint4& lo, uint4& hi, const float (
   }
 }
 
+// fp16 range of the rotating modes: running per-half maximum of |x| as fp16 bits (the bit
+// patterns of non-negative halves order like their values, NaN above infinity), and the status
+// bit raised once a rotated value reached 65504 (cvt.rn.satfinite saturates there) or is not
+// finite.
+__device__ __forceinline__ uint32_t f16_absmax(uint32_t acc, uint32_t w) {
+  return __vmaxu2(acc, w & 0x7FFF7FFFu);
+}
+__device__ __forceinline__ uint32_t f16_absmax(uint32_t acc, const uint4& w) {
+  return f16_absmax(f16_absmax(f16_absmax(f16_absmax(acc, w.x), w.y), w.z), w.w);
+}
+__device__ __forceinline__ void report_f16_range(int* status, uint32_t acc) {
+  if (status && ((acc & 0xFFFFu) >= 0x7BFFu || (acc >> 16) >= 0x7BFFu))
+    atomicOr(status, kDevF16Range);
+}
+
 // Packed-pair version of rot_chunk_cs for 8 pairs with (cos, sin) held as 4 packed pairs each
 // (c2[w] = (c[2w], c[2w+1])) and ns2 = -s2. Per lane it performs exactly rot_pair's
 // operations, so the results are bit-identical to rot_chunk_cs.

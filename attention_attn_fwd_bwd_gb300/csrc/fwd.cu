@@ -388,6 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
       const int bh = b * p.Hkv + kvh;
       const __nv_bfloat16* src = p.k_raw + b * p.k_sb + kvh * p.k_sh;
       uint16_t* dst = p.k_rot + (int64_t)bh * kN * D;
+      uint32_t f16max = 0;  // |K'| as fp16 bits, per half
       int i = 0;
       for (int j = next_tile(ctl, p, jb, je); j < je; j = next_tile(ctl, p, j + 1, je), ++i) {
         if ((i & 3) != wr) continue;
@@ -424,6 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
 #pragma unroll
           for (int k = 0; k < CP; ++k) {
             rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
+            f16max = f16_absmax(f16_absmax(f16max, lo[k]), hi[k]);
             if (k + 1 < CP) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
           }
 #pragma unroll
@@ -441,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         __syncwarp();
         if (lane == 0) st_release_gpu(flag, 2u);
       }
+      report_f16_range(status, f16max);
     } else if (ROPE) {
       // each CTA rotates its own K stages in place after they land
       constexpr int CP = D / 16;    // chunk pairs per row
@@ -458,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           nws2[w] = f2_pack(-ws[2 * w], -ws[2 * w + 1]);
         }
       }
+      uint32_t f16max = 0;  // |K'| as fp16 bits, per half
       int i = 0;
       for (int j = next_tile(ctl, p, jb, je); j < je; j = next_tile(ctl, p, j + 1, je), ++i) {
         const int st = i % KST;
@@ -490,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             uint4 lo = *reinterpret_cast<uint4*>(tile + offl);
             uint4 hi = *reinterpret_cast<uint4*>(tile + offh);
             rot_chunk_cs2<true>(lo, hi, c2, s2, ns2);
+            f16max = f16_absmax(f16_absmax(f16max, lo), hi);
             *reinterpret_cast<uint4*>(tile + offl) = lo;
             *reinterpret_cast<uint4*>(tile + offh) = hi;
           }
@@ -498,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
         fence_proxy_async_smem();
         mbar_arrive(&ctl->k_ready[st]);
       }
+      report_f16_range(status, f16max);
     }
   } else {
     // ======================= softmax (one thread per query row) =======================
@@ -513,6 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
     const uint32_t tS = tmem + lane_off + s * 128;
     const uint32_t tO = tmem + lane_off + 256 + s * D;
     bool ok = true;
+    uint32_t qmax = 0;  // |Q'| as fp16 bits, per half (fused RoPE)
     if (valid) {
       // Rotate this sub-tile's Q in place, with coalesced table reads: a warp instruction
       // covers whole table rows (lane f holds entries 2f, 2f+1 of its row, i.e. dims 2f, 2f+1
@@ -546,8 +553,10 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
             float yl0, yh0, yl1, yh1;
             rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
             rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
-            *reinterpret_cast<uint32_t*>(tile + offl) = pack_f16x2_sat(yl0, yl1);
-            *reinterpret_cast<uint32_t*>(tile + offh) = pack_f16x2_sat(yh0, yh1);
+            const uint32_t wl = pack_f16x2_sat(yl0, yl1), wh = pack_f16x2_sat(yh0, yh1);
+            qmax = f16_absmax(f16_absmax(qmax, wl), wh);
+            *reinterpret_cast<uint32_t*>(tile + offl) = wl;
+            *reinterpret_cast<uint32_t*>(tile + offh) = wh;
           }
           if (k + 1 < RPT) {  // next row of this thread: 8 positions on (advance_cs8 order)
             float c0, s0, c1, s1;
@@ -557,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) fwd_kernel(const __grid_constant_
           }
         }
         fence_proxy_async_smem();
+        report_f16_range(status, qmax);
       }
       mbar_arrive(&ctl->q_ready[s]);
     }
@@ -776,9 +786,11 @@ __global__ void rope_table_kernel(float2* __restrict__ cs, int N, int half, Rope
 template <bool OUT_F16>
 __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb, int64_t sh,
                                  int64_t sn, __nv_bfloat16* __restrict__ out, int H, int N, int d,
-                                 const float2* __restrict__ cs, int RG, int BLK, int64_t chains) {
+                                 const float2* __restrict__ cs, int RG, int BLK, int64_t chains,
+                                 int* status) {
   const int cp = d / 16;
   const int nblk = (N + BLK - 1) / BLK;
+  uint32_t f16max = 0;  // fp16 output: |x'| as fp16 bits, per half
   for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < chains;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int c = static_cast<int>(idx % cp);
@@ -801,11 +813,13 @@ __global__ void prerotate_kernel(const __nv_bfloat16* __restrict__ x, int64_t sb
       uint4 lo = *reinterpret_cast<const uint4*>(src + n * sn);
       uint4 hi = *reinterpret_cast<const uint4*>(src + n * sn + d / 2);
       rot_chunk_cs<OUT_F16>(lo, hi, cc, ss);
+      if (OUT_F16) f16max = f16_absmax(f16_absmax(f16max, lo), hi);
       *reinterpret_cast<uint4*>(dst + (int64_t)n * d) = lo;
       *reinterpret_cast<uint4*>(dst + (int64_t)n * d + d / 2) = hi;
       if (n + RG < blk * BLK + BLK) advance_cs8(cc, ss, wc, ws);
     }
   }
+  if (OUT_F16) report_f16_range(status, f16max);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -836,7 +850,7 @@ cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
 
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
                              int N, int d, const float2* cs, bool out_f16, int block,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, int* status) {
   // the recurrence of the target kernel (see prerotate_kernel)
   const int cp = d / 16;
   int RG = 1, BLK = 1;                       // block == 0: each row's own table entry
@@ -851,10 +865,10 @@ cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, i
   const int threads = 256;
   const int blocks = static_cast<int>(std::min<int64_t>((chains + threads - 1) / threads, 152 * 16));
   void (*fn)(const __nv_bfloat16*, int64_t, int64_t, int64_t, __nv_bfloat16*, int, int, int,
-             const float2*, int, int, int64_t) = out_f16 ? prerotate_kernel<true> : prerotate_kernel<false>;
+             const float2*, int, int, int64_t, int*) = out_f16 ? prerotate_kernel<true> : prerotate_kernel<false>;
   fn<<<blocks, threads, 0, stream>>>(
       static_cast<const __nv_bfloat16*>(x), strides[0], strides[1], strides[2],
-      static_cast<__nv_bfloat16*>(out), H, N, d, cs, RG, BLK, chains);
+      static_cast<__nv_bfloat16*>(out), H, N, d, cs, RG, BLK, chains, status);
   return cudaGetLastError();
 }
 

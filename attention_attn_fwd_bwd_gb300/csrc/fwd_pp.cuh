@@ -472,7 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (idle == 1u) t0 = now;
             if (*abort_flag) break;
             if (now - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-              atomicExch(status, kDevTimeout);
+              atomicOr(status, kDevTimeout);
               *abort_flag = 1;
               break;
             }
@@ -640,6 +640,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t pol_tab = l2_policy_evict_last();  // the table stays in L2
       const uint64_t pol_in = l2_policy_evict_first();  // K is read once here
       const uint64_t pol_out = l2_policy_evict_last();  // K' is re-read by every unit
+      uint32_t f16max = 0;                               // |K'| as fp16 bits, per half
       int ik = 0;
       bool ok = true;
       for (int u = 0; ok; ++u) {
@@ -687,6 +688,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
+              f16max = f16_absmax(f16_absmax(f16max, lo[k]), hi[k]);
               if (k < 3) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
             }
 #pragma unroll
@@ -707,6 +709,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (ok && lane == 0) mbar_arrive(&ctl->meta_empty[e]);
       }
+      report_f16_range(status, f16max);
     }
     if (FP8) {
       // V (e4m3) is widened to bf16 once per block of 128 keys x 64 dims (this CTA's half of a
@@ -780,6 +783,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* const visits = var.visits;
     int sc = 0;  // S of this slot consumed (phase of s_full)
     bool ok = true;
+    uint32_t f16max = 0;  // |Q'| as fp16 bits, per half (fused RoPE)
     // Q' = R_m Q of unit un in place (fp16 with fused RoPE), then the slot's MMAs may read it.
     auto prep_q = [&](const UnitMeta& Mq, int un) {
       const int qq0 = Mq.q0[s][rank];
@@ -810,8 +814,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               float yl0, yh0, yl1, yh1;
               rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
               rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
-              *reinterpret_cast<uint32_t*>(tile + off) = pack_f16x2_sat(yl0, yl1);
-              *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = pack_f16x2_sat(yh0, yh1);
+              const uint32_t wl = pack_f16x2_sat(yl0, yl1), wh = pack_f16x2_sat(yh0, yh1);
+              f16max = f16_absmax(f16_absmax(f16max, wl), wh);
+              *reinterpret_cast<uint32_t*>(tile + off) = wl;
+              *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = wh;
             }
             float c0f, s0f, c1f, s1f;
             rot_pair(cs.x, cs.y, wstep.x, wstep.y, c0f, s0f);
@@ -1039,6 +1045,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&ctl->meta_empty[e]);
       if (!more) break;
     }
+    if (ROPE) report_f16_range(status, f16max);
   }
 
   __syncwarp();

@@ -111,7 +111,7 @@ cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
 // of 128).
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
                              int N, int d, const float2* cs, bool out_f16, int block,
-                             cudaStream_t stream);
+                             cudaStream_t stream, int* status);
 cudaError_t launch_wait_timeout(uint64_t limit_ns, int* status, cudaStream_t stream);
 // Record a message for attnfuse_last_error() and return code.
 int set_last_error(int code, const char* msg);

@@ -17,7 +17,7 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, int* status) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(smem_u32(&bar), 0)) {
       if (globaltimer_ns() - t0 > limit_ns) {
-        atomicExch(status, kDevTimeout);
+        atomicOr(status, kDevTimeout);
         break;
       }
     }

@@ -12,11 +12,12 @@
 namespace afx {
 
 // ---------------------------------------------------------------------------------------------
-// Device status word (one per process, in the library module). Non-zero = a kernel gave up.
+// Device status word (one per process, in the library module): a bit set per kind of event.
 // ---------------------------------------------------------------------------------------------
 enum : int {
   kDevOk = 0,
-  kDevTimeout = 1,
+  kDevTimeout = 1,    // a kernel gave up waiting
+  kDevF16Range = 2,   // a rotated Q' / K' value reached the fp16 limit (saturated) or is not finite
 };
 
 // Wall-clock limit for any single wait, in nanoseconds (globaltimer). Generous: a legitimate
@@ -120,7 +121,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if ((++spins & 255u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-        if (status) atomicExch(status, kDevTimeout);
+        if (status) atomicOr(status, kDevTimeout);
         if (abort_flag) *abort_flag = 1;
         return false;
       }
@@ -145,7 +146,7 @@ __device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t want, i
     if ((++spins & 63u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-        if (status) atomicExch(status, kDevTimeout);
+        if (status) atomicOr(status, kDevTimeout);
         if (abort_flag) *abort_flag = 1;
         return false;
       }
@@ -241,7 +242,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
     if ((++spins & 255u) == 0) {
       if (abort_flag && *abort_flag) return false;
       if (globaltimer_ns() - t0 > ATTNFUSE_WAIT_LIMIT_NS) {
-        if (status) atomicExch(status, kDevTimeout);
+        if (status) atomicOr(status, kDevTimeout);
         if (abort_flag) *abort_flag = 1;
         return false;
       }

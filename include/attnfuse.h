@@ -52,12 +52,15 @@ typedef int attnfuse_status;
 #define ATTNFUSE_ERR_WORKSPACE_TOO_SMALL 3
 #define ATTNFUSE_ERR_CUDA 4
 #define ATTNFUSE_ERR_TIMEOUT 5
+#define ATTNFUSE_ERR_FP16_RANGE 6 /* device status: a rotated Q' / K' value saturated fp16 */
 
 /* Where RoPE is applied (paper §4.1 "Fused RoPE" vs. the pre-rotation of Fig. 1a / §5.3).
  * In both rotating modes the rotation runs in fp32 and the rotated Q', K' are rounded to fp16
  * (not bf16) before the score MMA: fp16 keeps 3 more mantissa bits, which keeps the LSE within
  * 1e-3 of the exact value. fp16 saturates at +-65504, so these modes need |q|, |k| < 46000
- * (a rotation can grow one component by sqrt(2)). ROPE_NONE feeds bf16 inputs unchanged. */
+ * (a rotation can grow one component by sqrt(2)); a call that saturates (or meets a
+ * non-finite input) still completes, and sets ATTNFUSE_ERR_FP16_RANGE in the device status
+ * word (attnfuse_device_status). ROPE_NONE feeds bf16 inputs unchanged. */
 typedef enum {
   ATTNFUSE_ROPE_NONE = 0,      /* no rotation: plain scaled_dot_product */
   ATTNFUSE_ROPE_FUSED = 1,     /* rotate inside the attention kernel: each Q tile once in
@@ -146,7 +149,10 @@ const char* attnfuse_last_error(void);
 int attnfuse_version(void);
 
 /* Synchronise `stream`, then read (and if `clear`, reset) the device status word of the
- * current device: ATTNFUSE_OK, or ATTNFUSE_ERR_TIMEOUT if a kernel gave up waiting. */
+ * current device: ATTNFUSE_OK; ATTNFUSE_ERR_TIMEOUT if a kernel gave up waiting; else
+ * ATTNFUSE_ERR_FP16_RANGE if a forward in a rotating mode (FUSED or PREROTATE) produced a
+ * rotated Q' or K' element of magnitude >= 65504 or not finite: the fp16 operand saturated
+ * (or the input was not finite) and that call's scores are not to be trusted. */
 attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code);
 
 /* ------------------------------------------------------------------------------------------
@@ -167,6 +173,31 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
                              float rope_theta, attnfuse_rope_mode rope_mode,
                              const attnfuse_variant* variant, void* workspace,
                              size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------------------------
+ * Forward on host buffers. q, k, v, out and lse (lse may be NULL) are host pointers to
+ * contiguous [B, H, N, d] bf16 arrays (lse: [B, Hq, N] fp32); page-locked memory (cudaHostAlloc
+ * or cudaHostRegister) lets the copies run asynchronously. The batch is processed in chunks of
+ * chunk_b elements through two device buffer sets, so the copy-in of chunk c+1, the forward of
+ * chunk c and the copy-out of chunk c-1 overlap: the copies run on two streams the library
+ * creates once per device, the forwards on `stream`, ordered by events. The call returns after
+ * queueing; the results are in out / lse once `stream` has reached this point (the copy-ins
+ * start after the work queued on `stream` before the call). Other arguments as attnfuse_fwd
+ * (no ATTNFUSE_ROPE_REUSE_TABLE: the first chunk builds the table, the others reuse it). The
+ * variant's device arrays are indexed per chunk: an additive bias with a batch stride and
+ * tile_visits are offset by the chunk's first batch element. workspace: device memory of
+ * attnfuse_fwd_host_workspace_size bytes (two chunk buffer sets and one forward workspace).
+ * Calls on one device are serialised by a lock while they queue work.
+ * ------------------------------------------------------------------------------------------ */
+attnfuse_status attnfuse_fwd_host_workspace_size(int B, int Hq, int Hkv, int N, int d,
+                                                 attnfuse_rope_mode rope_mode, int chunk_b,
+                                                 size_t* bytes);
+
+attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, void* out,
+                                  float* lse, int B, int Hq, int Hkv, int N, int d, float scale,
+                                  float rope_theta, attnfuse_rope_mode rope_mode,
+                                  const attnfuse_variant* variant, int chunk_b, void* workspace,
+                                  size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------------------------
  * e4m3 (fp8) forward (paper §9.1 future work: low-precision attention), head dim 128.

@@ -255,3 +255,26 @@ def test_timeout_path_reports_status():
     assert af.device_status(clear=True) == 0
     # the context is still usable
     test_tiny_config()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("rope_mode", [af.ROPE_FUSED, af.ROPE_PREROTATE])
+@pytest.mark.parametrize("which", ["q", "k"])
+def test_fp16_range_is_reported(d, rope_mode, which):
+    """The rotating modes round Q' and K' to fp16: an element beyond 65504 saturates, and the
+    call reports it through the device status word (ATTNFUSE_ERR_FP16_RANGE = 6), which a read
+    clears. Position 0 rotates by angle 0, so a value of 70000 there reaches the rounding as it
+    is. Without RoPE the bf16 operands are used as they are and nothing is reported."""
+    dev = torch.device("cuda")
+    N = 300
+    x = inputs.prefill(1, 4, 2, N, d, seed=33)
+    t = x[which].clone()
+    t[0, 1, 0, 3] = 70000.0
+    x[which] = t
+    q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
+    assert af.device_status() == 0
+    af.fwd(q, k, v, rope_theta=1e4, rope_mode=rope_mode)
+    assert af.device_status() == 6
+    assert af.device_status() == 0
+    af.fwd(q, k, v, rope_theta=1e4, rope_mode=af.ROPE_NONE)
+    assert af.device_status() == 0
