@@ -267,15 +267,14 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
 // ATTNFUSE_ROPE_AUTO: the faster of on-chip rotation and pre-rotation, by the crossover
 // N* measured on GB300 (the paper's Rotation Calculus, §5.3; B*N = 16384 tokens, causal).
 // The pre-rotation pass streams at ~5 TB/s, so it costs ~70 us per 16k-token, 32-head call.
-// Head dim 64: fusion wins below N* ~ 3.2k (forward; t_prerotate / t_fused = 1.23 at N = 256,
-// 1.08 at 1024, 1.00 at 2048 and 4096, 0.99 at 8192) and ~ 260 (backward, which re-reads each
-// K tile once per query tile). Head
-// dim 128: the persistent forward rotates each K block once per call (shared through L2) and
-// each Q tile in shared memory, and wins below N* ~ 14k (1.13 at N = 256, 1.06 at 2048, 1.02
-// at 4096, 1.00 at 16384); the backward pre-rotates at every N.
-constexpr int kAutoFusedBelowN64Fwd = 3160;
+// Head dim 64: fusion wins below N* ~ 1.85k (forward; t_prerotate / t_fused over two sweeps:
+// 1.19-1.23 at N = 256, 1.04-1.08 at 1024, 0.98-1.00 at 2048) and ~ 260 (backward, which
+// re-reads each K tile once per query tile). Head dim 128: the persistent forward rotates Q in
+// shared memory and takes K' from a one-pass rotation of K; it wins below N* ~ 3.3k (1.05 at
+// N = 256, 1.02 at 2048, 0.99 at 4096, 0.97 at 16384). The backward pre-rotates at every N.
+constexpr int kAutoFusedBelowN64Fwd = 1850;
 constexpr int kAutoFusedBelowN64Bwd = 258;
-constexpr int kAutoFusedBelowN128Fwd = 14000;
+constexpr int kAutoFusedBelowN128Fwd = 3340;
 
 static attnfuse_rope_mode resolve_rope(attnfuse_rope_mode m, int N, int d, bool backward) {
   if (m != ATTNFUSE_ROPE_AUTO) return m;
@@ -399,7 +398,15 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
     qa = qr; ka = kr; qs = qs_c; ks = ks_c;
   }
-  if (rope_mode == ATTNFUSE_ROPE_FUSED && (d == 128 || share_rotated_k_d64(N, p.var))) {
+  if (rope_mode == ATTNFUSE_ROPE_FUSED && d == 128) {
+    // head dim 128: Q is rotated in the forward, per work unit in shared memory; K (1/g of Q
+    // with GQA) by one pass into the workspace copy K' before it, with the forward's chains
+    uint8_t* kr = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
+    cudaError_t e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, 1, stream, st);
+    if (e != cudaSuccess) return cuda_fail(e, "K rotation launch");
+    ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
+    ka = kr; ks = ks_c;
+  } else if (rope_mode == ATTNFUSE_ROPE_FUSED && (d == 128 || share_rotated_k_d64(N, p.var))) {
     // K is rotated once per call inside the forward, per 64-key block (head dim 128) or
     // 128-key tile (head dim 64), by whichever CTA needs it first, into a workspace copy that
     // every CTA then loads with TMA
@@ -444,9 +451,6 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
 // ---------------------------------------------------------------------------------------------
 namespace {
 size_t fp8_v_bytes(int B, int Hkv, int N, int d) { return align_up((size_t)B * Hkv * N * d * 2, 256); }
-size_t fp8_sync_bytes(int B, int Hkv, int N) {
-  return align_up((size_t)B * Hkv * 2 * ((N + 127) / 128) * sizeof(uint32_t), 256);
-}
 attnfuse_status check_tensor8(const void* p, const int64_t st[4], const char* name) {
   if (!p) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s is NULL", name);
   if (!aligned16(p)) return fail(ATTNFUSE_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
@@ -467,7 +471,7 @@ attnfuse_status attnfuse_fwd_fp8_workspace_size(int B, int Hq, int Hkv, int N, i
   attnfuse_status rc = check_shape(B, Hq, Hkv, N, d);
   if (rc) return rc;
   if (d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "e4m3 forward needs head dim 128 (got %d)", d);
-  *bytes = fp8_v_bytes(B, Hkv, N, d) + fp8_sync_bytes(B, Hkv, N);
+  *bytes = fp8_v_bytes(B, Hkv, N, d);
   return ok();
 }
 
@@ -503,16 +507,14 @@ attnfuse_status attnfuse_fwd_fp8(const void* q, const int64_t q_strides[4], cons
   int* st = nullptr;
   if ((rc = device_state(&st))) return rc;
   uint8_t* base = static_cast<uint8_t*>(workspace);
-  p.v_raw = static_cast<const uint8_t*>(v);
-  p.v_sb = v_strides[0]; p.v_sh = v_strides[1]; p.v_sn = v_strides[2];
-  p.v_wide = reinterpret_cast<uint16_t*>(base);
-  p.v_sync = reinterpret_cast<uint32_t*>(base + fp8_v_bytes(B, Hkv, N, d));
-  cudaError_t e = cudaMemsetAsync(p.v_sync, 0, fp8_sync_bytes(B, Hkv, N), stream);
-  if (e != cudaSuccess) return cuda_fail(e, "v_sync reset");
+  // V widened to bf16 (exact) by one pass; the P V MMAs read it like a bf16 V
+  void* v_wide = base;
+  cudaError_t e = launch_widen_e4m3(v, v_strides, v_wide, B, Hkv, N, d, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "V widening launch");
   int64_t vs_c[4] = {(int64_t)Hkv * N * d, (int64_t)N * d, d, 1};
   if ((rc = encode_bhnd8(&p.tmQ, q, q_strides, B, Hq, N, d, "q", 128))) return rc;
   if ((rc = encode_bhnd8(&p.tmK, k, k_strides, B, Hkv, N, d, "k", 64))) return rc;
-  if ((rc = encode_bhnd(&p.tmV, p.v_wide, vs_c, B, Hkv, N, d, "v (widened)"))) return rc;
+  if ((rc = encode_bhnd(&p.tmV, v_wide, vs_c, B, Hkv, N, d, "v (widened)"))) return rc;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.o_sb = o_strides[0]; p.o_sh = o_strides[1]; p.o_sn = o_strides[2];
   p.lse = lse;

@@ -8,25 +8,28 @@
 // two heads at two positions or four positions of one head.
 //
 // Each slot is an independent online softmax over its own rows, with its own score buffer S_s
-// and output accumulator O_s in tensor memory. Per kv tile i, slot s runs
-//     O_s += P_s V(i-1);  S_s = Q_s K(i)^T
+// and output accumulator O_s in tensor memory and its own P buffer in shared memory. Per kv
+// tile i, slot s runs
+//     S_s = Q_s K(i)    as soon as the slot's softmax has read S_s of tile i-1 into registers,
+//     O_s += P_s V(i-1) once that softmax has written P_s (bf16) to shared memory,
 // as M = 256 cta_group::2 MMAs (both CTAs' rows of a slot at once; each CTA supplies half of
-// every K and V tile), issued by the slot's own thread. P_s is written over S_s: the MMA that
-// overwrites S_s is issued by the same thread after the one that reads P_s, and one thread's
-// MMAs complete in order.
+// every K and V tile), issued by the slot's own thread: the next tile's scores are computed
+// while the softmax of the current one runs. The softmax rewrites P_s only after the PV that
+// read it has completed.
 //
 // TMEM (512 columns, same addresses in both CTAs): S_0 [0,128), S_1 [128,256), O_0 [256,384),
-// O_1 [384,512); P_s occupies the first 64 columns of S_s (bf16 pairs).
+// O_1 [384,512).
 // Warp roles (16 warps):
 //   warp 0      TMA producer (Q per unit and slot, this CTA's halves of K and V tiles); also
-//               forwards "K / V half landed" to the even CTA (K only without fused RoPE)
+//               forwards "K / V half landed" to the even CTA
 //   warps 1, 2  MMA issuers of slot 0 / slot 1 (even CTA only)
 //   warp 3      scheduler: per-unit metadata (tiles, ranges, block-sparse bitmaps) into a ring
 //   warps 4-7   softmax of slot 0, warps 8-11 softmax of slot 1: one query row per thread;
-//               also rotate their Q tile (fused RoPE) and write O and LSE at the end of a unit
-//   warps 12-15 K rotators (fused RoPE): rotate each 64-key block of K once per call into a
-//               workspace copy K' (fp16) that every CTA loads with TMA; with e4m3 inputs they
-//               widen V to bf16 the same way (the scores then run on kind::f8f6f4 MMAs)
+//               they write O and LSE at the end of a unit
+//   warps 12-15 fused RoPE: rotate each unit's Q tiles in place as they land (12-13 slot 0,
+//               14-15 slot 1); the keys come rotated (K') from a pass the host launches
+//               first. e4m3 inputs: V comes widened to bf16 from a pass the host launches
+//               first, and the scores run on kind::f8f6f4 MMAs
 // Every wait is bounded (see ptx.cuh).
 #pragma once
 #include <cuda.h>
@@ -45,14 +48,15 @@ constexpr int kD = 128;                // head dim
 constexpr int kBM = 128;               // query rows per slot and CTA
 constexpr int kBN = 128;               // keys per kv tile (64 per CTA for K)
 constexpr int kThreads = 512;
-constexpr int kKSt = 5;                // K stages (released when both slots' S are done)
-constexpr int kVSt = 4;                // V stages (released when both slots' PV are done)
+constexpr int kKSt = 3;                // K stages (released when both slots' S are done)
+constexpr int kVSt = 2;                // V stages (released when both slots' PV are done)
 constexpr int kRing = 4;               // unit metadata entries in flight
 constexpr uint32_t kQTile = kBM * kD * 2;        // 32 KB: 128 rows x 128 dims, 2 panels
 constexpr uint32_t kKHalf = 64u * kD * 2u;       // 16 KB: 64 keys x 128 dims, 2 panels of 8 KB
 constexpr uint32_t kVHalf = kBN * 64u * 2u;      // 16 KB: 128 keys x 64 dims, 1 panel
 constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = 2 * kQTile;
+constexpr uint32_t kOffP = 2 * kQTile;           // P of slot s: bf16, laid out like a Q tile
+constexpr uint32_t kOffK = kOffP + 2 * kQTile;
 constexpr uint32_t kOffV = kOffK + kKSt * kKHalf;
 constexpr uint32_t kOffCtl = kOffV + kVSt * kVHalf;
 constexpr uint32_t kTmS = 0, kTmO = 256;         // + 128 * slot
@@ -80,8 +84,8 @@ struct UnitMeta {
 struct Ctl {
   uint64_t q_full[2], k_full[kKSt], v_full[kVSt];   // local TMA completion
   uint64_t q_empty[2], k_empty[kKSt], v_empty[kVSt];  // MMA commits (multicast to both CTAs)
-  uint64_t s_full[2], o_full[2];                       // MMA commits (multicast)
-  uint64_t q_ready[2], k_ready[kKSt], v_ready[kVSt], p_full[2];  // even CTA: both CTAs arrive
+  uint64_t s_full[2], o_full[2], pv_done[2];           // MMA commits (multicast)
+  uint64_t q_ready[2], k_ready[kKSt], v_ready[kVSt], p_full[2], s_free[2];  // even CTA: both CTAs arrive
   uint64_t meta_full[kRing], meta_empty[kRing];
   uint64_t mma_final;
   uint32_t tmem_base;
@@ -257,7 +261,7 @@ __device__ void fill_meta(UnitMeta& M, const FwdParams& p, const Sched& S, int c
 }  // namespace
 
 // RK: how the score operands are produced (kRopeNone / kRopeFused / kRopePrerotated, or
-// kFp8: e4m3 Q and K used as they are, e4m3 V widened to bf16).
+// kFp8: e4m3 Q and K used as they are; V widened to bf16 by the host's pass).
 // BIAS: score bias compiled in (0 none, 1 ALiBi, 2 additive). NORM: 0 softmax, 1 ReLU
 // normaliser (P = relu(s) / N, no row sum).
 template <int RK, int BIAS, int NORM>
@@ -283,8 +287,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->q_empty[s], 1);
       mbar_init(&ctl->s_full[s], 1);
       mbar_init(&ctl->o_full[s], 1);
-      mbar_init(&ctl->q_ready[s], 8);   // the slot's 4 softmax warps, both CTAs
+      mbar_init(&ctl->q_ready[s], ROPE ? 4 : 8);   // the slot's 2 Q rotators (fused RoPE) or
+                                                   // 4 softmax warps, both CTAs
       mbar_init(&ctl->p_full[s], 8);
+      mbar_init(&ctl->s_free[s], 8);    // the slot's 4 softmax warps have read S, both CTAs
+      mbar_init(&ctl->pv_done[s], 1);
     }
     for (int s = 0; s < kKSt; ++s) {
       mbar_init(&ctl->k_full[s], 1);
@@ -296,9 +303,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->v_empty[s], 2);
       mbar_init(&ctl->v_ready[s], 2);
     }
-    // ring consumers: producer, (even CTA) two issuers, (fused RoPE, e4m3) four rotator warps,
+    // ring consumers: producer, (even CTA) two issuers, (fused RoPE) four rotator warps,
     // eight softmax warps
-    const int consumers = 1 + (rank == 0 ? 2 : 0) + ((ROPE || FP8) ? 4 : 0) + 8;
+    const int consumers = 1 + (rank == 0 ? 2 : 0) + (ROPE ? 4 : 0) + 8;
     for (int e = 0; e < kRing; ++e) {
       mbar_init(&ctl->meta_full[e], 32);
       mbar_init(&ctl->meta_empty[e], consumers);
@@ -353,24 +360,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       auto meta_ready = [&](int u) {
         return mbar_test(&ctl->meta_full[u % kRing], (u / kRing) & 1);
       };
-      // A block another CTA's warps write for this kernel (fused RoPE: K'; e4m3: widened V)
-      // is ready once its flag reads 2; TMA may then copy it.
-      auto flag_done = [&](const uint32_t* f) {
-        if (ld_acquire_gpu(f) != 2u) return false;
-        fence_proxy_async_global();
-        return true;
-      };
-      const int nkb = (p.N + 63) / 64, nvb = 2 * ((p.N + kBN - 1) / kBN);
-      // this CTA's 64-key block of kv tile j, rotated
-      auto k_block_rotated = [&](const UnitMeta& M, int j) {
-        const int kb = 2 * j + rank;
-        if (kb >= nkb) return true;  // past the end: the copy reads zeros
-        return flag_done(p.k_sync + (M.b * p.Hkv + M.kvh) * nkb + kb);
-      };
-      // this CTA's 64 dims of the 128 keys of kv tile j, widened
-      auto v_block_widened = [&](const UnitMeta& M, int j) {
-        return flag_done(p.v_sync + (M.b * p.Hkv + M.kvh) * nvb + 2 * j + rank);
-      };
       while (true) {
         bool moved = false;
         // ---- Q ----
@@ -403,8 +392,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               moved = true;
             } else {
               const int st = ik % kKSt;
-              if ((ik < kKSt || mbar_test(&ctl->k_empty[st], ((ik / kKSt) - 1) & 1)) &&
-                  (!ROPE || k_block_rotated(M, jk))) {
+              if (ik < kKSt || mbar_test(&ctl->k_empty[st], ((ik / kKSt) - 1) & 1)) {
                 mbar_arrive_expect_tx(&ctl->k_full[st], FP8 ? kKHalf / 2 : kKHalf);
                 for (int pn = 0; pn < (FP8 ? 1 : 2); ++pn)
                   tma_load_4d_hint(smem + kOffK + st * kKHalf + pn * (64 * 128), &p.tmK, &ctl->k_full[st],
@@ -429,8 +417,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               moved = true;
             } else if (iv < ik) {
               const int st = iv % kVSt;
-              if ((iv < kVSt || mbar_test(&ctl->v_empty[st], ((iv / kVSt) - 1) & 1)) &&
-                  (!FP8 || v_block_widened(M, jv))) {
+              if (iv < kVSt || mbar_test(&ctl->v_empty[st], ((iv / kVSt) - 1) & 1)) {
                 mbar_arrive_expect_tx(&ctl->v_full[st], kVHalf);
                 tma_load_4d_hint(smem + kOffV + st * kVHalf, &p.tmV, &ctl->v_full[st], rank * 64,
                                  jv * kBN, M.kvh, M.b, pol_keep);
@@ -489,12 +476,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_wait(&ctl->q_full[k & 1], (k >> 1) & 1, status, nullptr);
     } else if ((warp == 1 || warp == 2) && lane == 0 && rank == 0) {
       // ======================= pair-MMA issuer of slot s =======================
-      // Per kv tile i the issuer of slot s issues one burst: O_s += P_s V(i-1), then
-      // S_s = Q_s K(i) (that S overwrites the P the PV reads; one thread's MMAs complete in
-      // order). The two issuers run concurrently on different SM sub-partitions, so each
-      // one's barrier waits overlap the other's MMAs. Every wait of a burst comes before its
-      // MMAs: a shared-memory access while MMAs stream their operands from shared memory
-      // costs the issuing thread a couple of hundred cycles.
+      // Per kv tile i the issuer of slot s runs S_s = Q_s K(i) as soon as the slot's softmax
+      // has read S_s of the tile before into registers (s_free), and then O_s += P_s V(i-1)
+      // once that softmax has written P_s to shared memory (p_full). The scores of the next
+      // tile are thus computed while the softmax of the current one runs. The two issuers run
+      // concurrently on different SM sub-partitions, so each one's barrier waits overlap the
+      // other's MMAs.
       const int s = warp - 1;
       constexpr uint32_t idesc_s = FP8 ? idesc_e4m3_f32(256, kBN) : idesc_f32acc(256, kBN, 0, 0, RK != kRopeNone);
       constexpr uint32_t idesc_o = idesc_bf16_f32(256, kD, 0, 1);
@@ -504,30 +491,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       static_assert(kSmem < (1u << 18), "descriptor address field");
       constexpr uint32_t dhi = desc_sw128_hi(1024);
       const uint32_t dQ = desc_sw128_lo(smem_u32(smem + kOffQ + s * kQTile), 16);
+      const uint32_t dP = desc_sw128_lo(smem_u32(smem + kOffP + s * kQTile), 16);
       const uint32_t dK0 = desc_sw128_lo(smem_u32(smem + kOffK), 16);
       const uint32_t dV0 = desc_sw128_lo(smem_u32(smem + kOffV), kVHalf);
       const uint32_t tS = tmem + kTmS + 128 * s, tO = tmem + kTmO + 128 * s;
       int ik = 0;          // kv tiles walked (K and V copy index)
-      int pc = 0;          // S issued (phase of s_full / p_full)
+      int sc = 0;          // S issued (phases of s_full and s_free)
+      int pvc = 0;         // PV issued (phases of p_full and pv_done)
       bool pend = false;   // a PV waits for its P
       int pend_v = 0;      // its V copy index
       bool pend_acc = false, pend_last = false;
       bool ok = true;
-      // the PV of the pending tile (its P and V waited on by the caller)
-      auto issue_pv = [&]() {
+      // the pending PV, once its P is in shared memory and its V has landed
+      auto flush_pv = [&]() {
+        ok = mbar_wait_cluster(&ctl->p_full[s], pvc & 1, status, abort_flag) &&
+             mbar_wait_cluster(&ctl->v_ready[pend_v % kVSt], (pend_v / kVSt) & 1, status, abort_flag);
+        if (!ok) return;
+        tc_fence_after();
         const int vs = pend_v % kVSt;
         const uint32_t bv = dV0 + vs * (kVHalf >> 4);
-        mma_ts_pair_w(tO, tS, bv, dhi, idesc_o, pend_acc ? 1u : 0u);
+        if (pend_acc)
+          mma_ss_pair_w<1>(tO, dP, bv, dhi, idesc_o);
+        else
+          mma_ss_pair_w<0>(tO, dP, bv, dhi, idesc_o);
 #pragma unroll
         for (int kk = 1; kk < kBN / 16; ++kk)
-          mma_ts_pair_w(tO, tS + kk * 8, bv + kk * (2048 >> 4), dhi, idesc_o, 1u);
+          mma_ss_pair_w<1>(tO, dP + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4),
+                           bv + kk * (2048 >> 4), dhi, idesc_o);
         mma_commit_pair(&ctl->v_empty[vs], 3);
+        mma_commit_pair(&ctl->pv_done[s], 3);
         if (pend_last) mma_commit_pair(&ctl->o_full[s], 3);
+        ++pvc;
         pend = false;
-      };
-      auto wait_pv_inputs = [&]() {
-        ok = mbar_wait_cluster(&ctl->p_full[s], (pc - 1) & 1, status, abort_flag) &&
-             mbar_wait_cluster(&ctl->v_ready[pend_v % kVSt], (pend_v / kVSt) & 1, status, abort_flag);
       };
       for (int u = 0; ok; ++u) {
         const int e = u % kRing;
@@ -542,10 +537,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // for that O before this unit's epilogue), then this unit's rotated Q.
         auto open_slot = [&]() {
           if (pend) {
-            wait_pv_inputs();
+            flush_pv();
             if (!ok) return;
-            tc_fence_after();
-            issue_pv();
           }
           ok = mbar_wait_cluster(&ctl->q_ready[s], u & 1, status, abort_flag);
           if (ok && ns == 0) {
@@ -557,16 +550,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = jb; ok && j < je; j = next_tile(M, bs, j), ++ik) {
           const bool a = bs ? pbit(M.sbits[s], j) : (j >= slo && j < shi);
           const int st = ik % kKSt;
-          // ---- all waits of the burst ----
           if (!opened) open_slot();
-          if (ok && pend) wait_pv_inputs();
+          if (ok && !a) {
+            // no MMA of this slot reads K(ik) or V(ik): release both once they have landed.
+            // The pending PV goes first: a later V copy into its stage waits for it.
+            if (pend) flush_pv();
+            if (ok) ok = mbar_wait_cluster(&ctl->k_ready[st], (ik / kKSt) & 1, status, abort_flag);
+            if (ok) ok = mbar_wait_cluster(&ctl->v_ready[ik % kVSt], (ik / kVSt) & 1, status, abort_flag);
+            if (!ok) break;
+            mma_commit_pair(&ctl->v_empty[ik % kVSt], 3);
+            mma_commit_pair(&ctl->k_empty[st], 3);
+            continue;
+          }
+          // ---- waits for S(j): Q, K(j) landed, the slot's previous S read ----
           if (ok) ok = mbar_wait_cluster(&ctl->k_ready[st], (ik / kKSt) & 1, status, abort_flag);
-          if (ok && !a) ok = mbar_wait_cluster(&ctl->v_ready[ik % kVSt], (ik / kVSt) & 1, status, abort_flag);
+          if (ok && sc > 0) ok = mbar_wait_cluster(&ctl->s_free[s], (sc - 1) & 1, status, abort_flag);
           if (!ok) break;
           tc_fence_after();
-          // ---- MMAs ----
-          if (pend) issue_pv();
-          if (a) {
+          {
             const uint32_t bk = dK0 + st * (kKHalf >> 4);
             if constexpr (FP8) {
               // one 128-byte panel per row: four k-steps of 32 e4m3 values (32 bytes)
@@ -582,66 +583,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                  bk + (((kk >> 2) * (64 * 128) + (kk & 3) * 32) >> 4), dhi, idesc_s);
             }
             mma_commit_pair(&ctl->s_full[s], 3);
-            ++pc;
+            ++sc;
             ++cnt;
             if (cnt == ns) mma_commit_pair(&ctl->q_empty[s], 3);
-            pend = true;
-            pend_v = ik;
-            pend_acc = cnt > 1;
-            pend_last = cnt == ns;
-          } else {
-            // no PV of this slot reads V(ik)
-            mma_commit_pair(&ctl->v_empty[ik % kVSt], 3);
           }
           mma_commit_pair(&ctl->k_empty[st], 3);
+          // ---- the previous tile's PV, then this tile's becomes pending ----
+          if (pend) {
+            flush_pv();
+            if (!ok) break;
+          }
+          pend = true;
+          pend_v = ik;
+          pend_acc = cnt > 1;
+          pend_last = cnt == ns;
         }
         if (ok && !opened) open_slot();
         if (ok) mbar_arrive(&ctl->meta_empty[e]);
       }
-      if (ok && pend) {
-        wait_pv_inputs();
-        if (ok) {
-          tc_fence_after();
-          issue_pv();
-        }
-      }
+      if (ok && pend) flush_pv();
       // All MMAs must finish before TMEM is released.
       mma_commit_pair(&ctl->mma_final, 3);
       mbar_wait(&ctl->mma_final, 0, status, nullptr);
     }
   } else if (warp >= 12) {
-    // ======================= K rotators (fused RoPE) =======================
+    // ======================= Q rotators (fused RoPE) =======================
     setmaxnreg_dec<kRegsRot>();
     if (ROPE) {
-      // K' = R_n K is made once per 64-key block and call. The rotator warps walk the blocks
-      // their units load (this CTA's half of every kv tile), warp w taking every fourth; the
-      // first warp of any CTA to claim a block rotates it from global memory into the fp16 K'
-      // buffer and flags it, and the producers of every CTA copy K' with TMA (mostly from L2).
-      // Lane (c, rl) rotates 16-byte chunk c of both halves of rows rg + 16k (k < 4) of the
-      // four chains rg = rl + 4i; a chain starts from its table entry and steps the (cos, sin)
-      // of 16 positions per row (the pre-rotation pass uses the same chains, so K' is
-      // bit-identical to its output).
-      const int wr = warp - 12;
-      const int c = lane & 7, rl = lane >> 3;
-      const int kN = p.N, nkb = (kN + 63) / 64;
-      const float2* const cs_tab = p.rope_cs;
-      constexpr uint64_t kSign2 = 0x8000000080000000ull;
-      uint64_t wc2[4], ws2[4], nws2[4];  // (cos, sin) of 16 positions, pairs of dims
-      {
-        float wc[8], ws[8];
-        load_cs8(cs_tab + (size_t)16 * (kD / 2) + c * 8, wc, ws);
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          wc2[w] = f2_pack(wc[2 * w], wc[2 * w + 1]);
-          ws2[w] = f2_pack(ws[2 * w], ws[2 * w + 1]);
-          nws2[w] = ws2[w] ^ kSign2;
-        }
-      }
-      const uint64_t pol_tab = l2_policy_evict_last();  // the table stays in L2
-      const uint64_t pol_in = l2_policy_evict_first();  // K is read once here
-      const uint64_t pol_out = l2_policy_evict_last();  // K' is re-read by every unit
-      uint32_t f16max = 0;                               // |K'| as fp16 bits, per half
-      int ik = 0;
+      // ---- Q rotators: Q' = R_m Q of each unit's tiles, in place in shared memory (fp16), as
+      // soon as a tile lands; warps 12-13 take slot 0, warps 14-15 slot 1. Warp w2 of a slot
+      // rotates the rows of the query-tile recurrence chains (query_cs8) c0 = w2 + 2i, rows
+      // c0 + 8k, each chain starting from its table entry and stepping 8 positions; lane f
+      // takes dims 2f, 2f+1 and their partners 64+2f, 64+2f+1. K' comes from the rotation
+      // pass the host launches before this kernel. ----
+      const int s = (warp - 12) >> 1, w2 = (warp - 12) & 1;
+      const int N = p.N;
+      const uint64_t pol_tab = l2_policy_evict_last();
+      const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
+      const float4 wstep = ldg_f4_hint(tab + (size_t)8 * (kD / 4) + lane, pol_tab);
+      uint8_t* tile = smem + kOffQ + s * kQTile;
+      const uint32_t within = static_cast<uint32_t>(lane & 3) * 4u;
+      uint32_t f16max = 0;  // |Q'| as fp16 bits, per half
       bool ok = true;
       for (int u = 0; ok; ++u) {
         const int e = u % kRing;
@@ -649,122 +631,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
         const UnitMeta& M = ctl->ring[e];
         if (!M.live) break;
-        const int bh = M.b * p.Hkv + M.kvh;
-        const __nv_bfloat16* src = p.k_raw + M.b * p.k_sb + M.kvh * p.k_sh;
-        uint16_t* dst = p.k_rot + (int64_t)bh * kN * kD;
-        for (int j = M.jb; j < M.je; j = next_tile(M, bs, j), ++ik) {
-          const int kb = 2 * j + rank;
-          if ((ik & 3) != wr || kb >= nkb) continue;
-          uint32_t* flag = p.k_sync + bh * nkb + kb;
-          uint32_t mine = 0;
-          if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(flag) == 0u)
-            mine = atomicCAS(flag, 0u, 1u) == 0u ? 1u : 0u;
-          if (!__shfl_sync(0xffffffffu, mine, 0)) continue;
-          const int n0 = kb * 64;
-#pragma unroll 1
-          for (int i = 0; i < 4; ++i) {
-            const int rg = rl + 4 * i;
-            float4 pre[4];
-            {
-              const float4* t = reinterpret_cast<const float4*>(
-                  cs_tab + (size_t)min(n0 + rg, kN - 1) * (kD / 2) + c * 8);
+        const int qq0 = M.q0[s][rank];
+        const bool qvalid = M.qv[s][rank] != 0;
+        float4 cs[4];
 #pragma unroll
-              for (int w = 0; w < 4; ++w) pre[w] = ldg_f4_hint(t + w, pol_tab);
-            }
-            uint4 lo[4], hi[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const __nv_bfloat16* row = src + (int64_t)min(n0 + rg + 16 * k, kN - 1) * p.k_sn + c * 8;
-              lo[k] = ldg_u4_hint(row, pol_in);
-              hi[k] = ldg_u4_hint(row + 64, pol_in);
-            }
-            uint64_t c2[4], s2[4], ns2[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-              c2[w] = f2_pack(pre[w].x, pre[w].z);
-              s2[w] = f2_pack(pre[w].y, pre[w].w);
-              ns2[w] = s2[w] ^ kSign2;
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              rot_chunk_cs2<true>(lo[k], hi[k], c2, s2, ns2);
-              f16max = f16_absmax(f16_absmax(f16max, lo[k]), hi[k]);
-              if (k < 3) advance_cs2(c2, s2, ns2, wc2, ws2, nws2);
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int n = n0 + rg + 16 * k;
-              if (n < kN) {
-                uint16_t* out = dst + (int64_t)n * kD + c * 8;
-                stg_u4_hint(out, lo[k], pol_out);
-                stg_u4_hint(out + 64, hi[k], pol_out);
-              }
-            }
-          }
-          // K' visible to other CTAs' TMA copies before the flag says so
-          fence_proxy_async_global();
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(flag, 2u);
-        }
-        if (ok && lane == 0) mbar_arrive(&ctl->meta_empty[e]);
-      }
-      report_f16_range(status, f16max);
-    }
-    if (FP8) {
-      // V (e4m3) is widened to bf16 once per block of 128 keys x 64 dims (this CTA's half of a
-      // kv tile's PV operand) and call, claimed and flagged like K' above, into a workspace
-      // copy that the producers copy with TMA. Lane (row rr, quarter q4) widens 16 values of
-      // rows rr + 8i; four rows are loaded before any is converted.
-      const int wr = warp - 12;
-      const int rr = lane >> 2, q4 = lane & 3;
-      const int kN = p.N, nvb = 2 * ((kN + kBN - 1) / kBN);
-      const uint64_t pol_in = l2_policy_evict_first();  // V is read once here
-      const uint64_t pol_out = l2_policy_evict_last();  // and the widened copy by every unit
-      int ik = 0;
-      bool ok = true;
-      for (int u = 0; ok; ++u) {
-        const int e = u % kRing;
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->meta_full[e], (u / kRing) & 1, status, abort_flag));
+        for (int i = 0; i < 4; ++i)
+          cs[i] = qvalid ? ldg_f4_hint(tab + (size_t)min(qq0 + w2 + 2 * i, N - 1) * (kD / 4) + lane, pol_tab)
+                         : make_float4(0.f, 0.f, 0.f, 0.f);
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full[s], u & 1, status, abort_flag));
         if (!ok) break;
-        const UnitMeta& M = ctl->ring[e];
-        if (!M.live) break;
-        const int bh = M.b * p.Hkv + M.kvh;
-        const int c0 = rank * 64 + q4 * 16;  // first dim of this lane's 16
-        const uint8_t* src = p.v_raw + M.b * p.v_sb + M.kvh * p.v_sh + c0;
-        uint16_t* dst = p.v_wide + (int64_t)bh * kN * kD + c0;
-        for (int j = M.jb; j < M.je; j = next_tile(M, bs, j), ++ik) {
-          if ((ik & 3) != wr) continue;
-          uint32_t* flag = p.v_sync + bh * nvb + 2 * j + rank;
-          uint32_t mine = 0;
-          if (lane == 0 && *reinterpret_cast<volatile uint32_t*>(flag) == 0u)
-            mine = atomicCAS(flag, 0u, 1u) == 0u ? 1u : 0u;
-          if (!__shfl_sync(0xffffffffu, mine, 0)) continue;
-          const int n0 = j * kBN + rr;
-#pragma unroll 1
-          for (int i0 = 0; i0 < kBN / 8; i0 += 4) {
-            uint4 x[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-              x[i] = ldg_u4_hint(src + (int64_t)min(n0 + 8 * (i0 + i), kN - 1) * p.v_sn, pol_in);
+        if (qvalid) {
+#pragma unroll 2
+          for (int k = 0; k < kBM / 8; ++k) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              const int n = n0 + 8 * (i0 + i);
-              uint4 lo, hi;
-              e4m3x16_to_bf16(x[i], lo, hi);
-              if (n < kN) {
-                stg_u4_hint(dst + (int64_t)n * kD, lo, pol_out);
-                stg_u4_hint(dst + (int64_t)n * kD + 8, hi, pol_out);
+              const int rr = w2 + 2 * i + 8 * k;
+              if (qq0 + rr < N) {
+                const uint32_t off = sw128_offset(rr, lane >> 2) + within;
+                const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + off);
+                const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + kBM * 128 + off);
+                float yl0, yh0, yl1, yh1;
+                rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs[i].x, cs[i].y, yl0, yh0);
+                rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs[i].z, cs[i].w, yl1, yh1);
+                const uint32_t wl = pack_f16x2_sat(yl0, yl1), wh = pack_f16x2_sat(yh0, yh1);
+                f16max = f16_absmax(f16_absmax(f16max, wl), wh);
+                *reinterpret_cast<uint32_t*>(tile + off) = wl;
+                *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = wh;
               }
+              float c0f, s0f, c1f, s1f;
+              rot_pair(cs[i].x, cs[i].y, wstep.x, wstep.y, c0f, s0f);
+              rot_pair(cs[i].z, cs[i].w, wstep.z, wstep.w, c1f, s1f);
+              cs[i] = make_float4(c0f, s0f, c1f, s1f);
             }
           }
-          fence_proxy_async_global();
-          __threadfence();
-          __syncwarp();
-          if (lane == 0) st_release_gpu(flag, 2u);
+          fence_proxy_async_smem();
         }
-        if (ok && lane == 0) mbar_arrive(&ctl->meta_empty[e]);
+        __syncwarp();
+        if (lane == 0) {
+          arrive_leader(&ctl->q_ready[s], rank);
+          mbar_arrive(&ctl->meta_empty[e]);
+        }
       }
+      report_f16_range(status, f16max);
     }
   } else {
     // ======================= softmax of slot s (one query row per thread) =======================
@@ -782,51 +690,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int TK = (N + kBN - 1) / kBN;
     uint8_t* const visits = var.visits;
     int sc = 0;  // S of this slot consumed (phase of s_full)
+    int pc = 0;  // P of this slot written (phase of p_full; PV pc-1 completes phase pc-1 of pv_done)
     bool ok = true;
-    uint32_t f16max = 0;  // |Q'| as fp16 bits, per half (fused RoPE)
     // Q' = R_m Q of unit un in place (fp16 with fused RoPE), then the slot's MMAs may read it.
     auto prep_q = [&](const UnitMeta& Mq, int un) {
-      const int qq0 = Mq.q0[s][rank];
-      const bool qvalid = Mq.qv[s][rank] != 0;
+      (void)Mq;
+      if (ROPE) return;  // the Q rotators wait for the tile, rotate it and signal q_ready
       ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full[s], un & 1, status, abort_flag));
       if (!ok) return;
-      if (ROPE && qvalid) {
-        // Warp wq rotates the rows of two query-tile recurrence chains (query_cs8): rows
-        // wq + 8k and wq + 4 + 8k, each starting from its table entry and stepping 8 positions.
-        // Lane f takes dims 2f, 2f+1 and their partners 64+2f, 64+2f+1 (one 16-byte table read
-        // per row start).
-        const uint64_t pol_tab = l2_policy_evict_last();
-        const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
-        const float4 wstep = ldg_f4_hint(tab + (size_t)8 * (kD / 4) + lane, pol_tab);
-        uint8_t* tile = smem + kOffQ + s * kQTile;
-        const uint32_t within = static_cast<uint32_t>(lane & 3) * 4u;
-#pragma unroll
-        for (int ch = 0; ch < 2; ++ch) {
-          const int c0 = wq + 4 * ch;
-          float4 cs = ldg_f4_hint(tab + (size_t)min(qq0 + c0, N - 1) * (kD / 4) + lane, pol_tab);
-#pragma unroll 4
-          for (int k = 0; k < kBM / 8; ++k) {
-            const int rr = c0 + 8 * k;
-            if (qq0 + rr < N) {
-              const uint32_t off = sw128_offset(rr, lane >> 2) + within;
-              const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + off);
-              const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + kBM * 128 + off);
-              float yl0, yh0, yl1, yh1;
-              rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs.x, cs.y, yl0, yh0);
-              rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs.z, cs.w, yl1, yh1);
-              const uint32_t wl = pack_f16x2_sat(yl0, yl1), wh = pack_f16x2_sat(yh0, yh1);
-              f16max = f16_absmax(f16_absmax(f16max, wl), wh);
-              *reinterpret_cast<uint32_t*>(tile + off) = wl;
-              *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = wh;
-            }
-            float c0f, s0f, c1f, s1f;
-            rot_pair(cs.x, cs.y, wstep.x, wstep.y, c0f, s0f);
-            rot_pair(cs.z, cs.w, wstep.z, wstep.w, c1f, s1f);
-            cs = make_float4(c0f, s0f, c1f, s1f);
-          }
-        }
-        fence_proxy_async_smem();
-      }
       __syncwarp();
       if (lane == 0) arrive_leader(&ctl->q_ready[s], rank);
     };
@@ -885,6 +756,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tmem_ld32<64>(tS + 64, xr);
         tmem_ld32<96>(tS + 96, xr);
         tmem_wait_ld();
+        // S is in registers: the issuer may compute the next tile's S over it
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) arrive_leader(&ctl->s_free[s], rank);
+        bool pv_seen = false;
+        // the slot's previous PV has completed: O holds every earlier tile and the P buffer
+        // may be rewritten
+        auto wait_prev_pv = [&]() -> bool {
+          if (pv_seen || pc == 0) return true;
+          pv_seen = true;
+          return __all_sync(0xffffffffu, mbar_wait(&ctl->pv_done[s], (pc - 1) & 1, status, abort_flag));
+        };
         float x[128];
 #pragma unroll
         for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(xr[c]);
@@ -954,7 +837,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const float m_new = (mx > m_run + 8.0f) ? mx : m_run;
           const bool grow = m_new > m_run && m_run != kNegInf;
           if (!first && __any_sync(0xffffffffu, grow)) {
-            // O holds the slot's previous tiles (their PV completed before this S did)
+            // O must hold the slot's previous tiles before it is rescaled
+            if (!wait_prev_pv()) {
+              ok = false;
+              break;
+            }
             const float alpha = grow ? ex2_approx(m_run - m_new) : 1.f;
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
@@ -982,9 +869,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           l_run += f2_lo(acc) + f2_hi(acc);
         }
         first = false;
-        tmem_st32<0>(tS, pk);
-        tmem_st32<32>(tS + 32, pk);
-        tmem_wait_st();
+        // P (bf16) into the slot's shared-memory buffer, row r, laid out like a Q tile (two
+        // 128-byte-swizzled panels of 64 keys), once the PV that read the buffer has completed
+        if (!wait_prev_pv()) {
+          ok = false;
+          break;
+        }
+        {
+          uint8_t* prow = smem + kOffP + s * kQTile;
+#pragma unroll
+          for (int q = 0; q < 16; ++q)
+            *reinterpret_cast<uint4*>(prow + (q >> 3) * (kBM * 128) + sw128_offset(r, q & 7)) =
+                make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+        ++pc;
+        fence_proxy_async_smem();
+        tmem_wait_st();    // a rescaled O is in TMEM before the PV accumulates into it
         tc_fence_before();
         __syncwarp();
         if (lane == 0) arrive_leader(&ctl->p_full[s], rank);
@@ -1045,7 +945,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&ctl->meta_empty[e]);
       if (!more) break;
     }
-    if (ROPE) report_f16_range(status, f16max);
   }
 
   __syncwarp();

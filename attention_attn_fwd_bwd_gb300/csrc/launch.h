@@ -30,14 +30,7 @@ struct FwdParams {
   int64_t k_sb, k_sh, k_sn;
   uint16_t* k_rot;
   uint32_t* k_sync;
-  // e4m3 forward: V (e4m3, byte strides) is widened once per 128-key x 64-dim block into
-  // v_wide (bf16 [B, Hkv, N, d], contiguous; tmV maps it), v_sync[block] as k_sync; O is
-  // multiplied by o_scale (V's dequantisation scale)
-  const uint8_t* v_raw;
-  int64_t v_sb, v_sh, v_sn;
-  uint16_t* v_wide;
-  uint32_t* v_sync;
-  float o_scale;
+  float o_scale;  // e4m3 forward: O is multiplied by V's dequantisation scale
   VariantDev var;
   int* status;
 };
@@ -109,6 +102,9 @@ cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
 // recurrence (fp16 output); otherwise the in-block key recurrence of the kernels (forward keys:
 // fp16 output, blocks of 64 / 128 for head dim 128 / 64; backward Q and K: bf16 output, blocks
 // of 128).
+// e4m3 [B, H, N, d] (element = byte strides) -> contiguous bf16, exactly (fwd_pp_fp8.cu)
+cudaError_t launch_widen_e4m3(const void* v, const int64_t* strides, void* out, int B, int H, int N,
+                              int d, cudaStream_t stream);
 cudaError_t launch_prerotate(const void* x, const int64_t* strides, void* out, int B, int H,
                              int N, int d, const float2* cs, bool out_f16, int block,
                              cudaStream_t stream, int* status);

@@ -344,6 +344,15 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* ptr) {
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ptr) : "memory");
   return v;
 }
+// A counter one warp of a CTA publishes to another through shared memory.
+__device__ __forceinline__ void st_release_cta_smem(uint32_t* ptr, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(ptr)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta_smem(const uint32_t* ptr) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(ptr)) : "memory");
+  return v;
+}
 // Order this thread's generic-proxy global accesses with its later async-proxy ones (TMA).
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");

@@ -63,11 +63,13 @@ typedef int attnfuse_status;
  * word (attnfuse_device_status). ROPE_NONE feeds bf16 inputs unchanged. */
 typedef enum {
   ATTNFUSE_ROPE_NONE = 0,      /* no rotation: plain scaled_dot_product */
-  ATTNFUSE_ROPE_FUSED = 1,     /* rotate inside the attention kernel: each Q tile once in
-                                  shared memory; each block of K (64 keys at head dim 128, 128
-                                  at 64) once per call by the first CTA that needs it, into a
-                                  workspace copy K' that every CTA reads from L2 (no separate
-                                  pass, no Q' round trip) */
+  ATTNFUSE_ROPE_FUSED = 1,     /* rotate in the attention kernel: each Q tile once, in
+                                  shared memory, as it lands (no Q' round trip). K: head dim
+                                  128, one pass writes K' to the workspace just before the
+                                  forward (K is 1/g of Q's size); head dim 64, the forward
+                                  rotates each K tile once per call into a workspace copy
+                                  shared through L2 (long sequences) or per CTA in shared
+                                  memory (short ones) */
   ATTNFUSE_ROPE_PREROTATE = 2, /* separate rotate kernel writes Q', K' to the workspace, then
                                   attention runs without rotation (the paper's baseline) */
   ATTNFUSE_ROPE_AUTO = 3       /* the faster of FUSED and PREROTATE for this call's N, head dim
@@ -208,11 +210,11 @@ attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, v
  * positive and finite); out (bf16) and lse (fp32, or NULL) are as in attnfuse_fwd.
  * The scores S = Q K^T run on tcgen05 kind::f8f6f4 MMAs (exact products, fp32 accumulation);
  * q_scale * k_scale * scale is applied with the softmax scale. V is widened to bf16 (exact)
- * once per call into the workspace and P V runs as in the bf16 forward; v_scale multiplies O.
- * No RoPE: q and k are used as given (a caller with rotary positions quantises the rotated
- * tensors). variant: as attnfuse_fwd (all masks, ALiBi, additive bias, both normalisers).
- * Workspace: attnfuse_fwd_fp8_workspace_size bytes (the widened V, B*Hkv*N*256 bytes, and one
- * 32-bit flag per 128-key x 64-dim block, zeroed by every call with cudaMemsetAsync).
+ * by one pass into the workspace before the forward, and P V runs as in the bf16 forward;
+ * v_scale multiplies O. No RoPE: q and k are used as given (a caller with rotary positions
+ * quantises the rotated tensors). variant: as attnfuse_fwd (all masks, ALiBi, additive bias,
+ * both normalisers). Workspace: attnfuse_fwd_fp8_workspace_size bytes (the widened V,
+ * B*Hkv*N*256 bytes).
  * Errors: ATTNFUSE_ERR_UNSUPPORTED for d != 128; ATTNFUSE_ERR_INVALID_ARG for bad pointers,
  * strides or scales; ATTNFUSE_ERR_WORKSPACE_TOO_SMALL.
  * ------------------------------------------------------------------------------------------ */
@@ -317,8 +319,8 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
 
 /* The mode ATTNFUSE_ROPE_AUTO resolves to for sequence length N and head dim d, for the
  * forward (backward = 0) or the backward (backward = 1). Measured on GB300 with B*N = 16384
- * tokens, causal: fusion wins for head dim 64 below N ~ 3.2k (forward) and N ~ 260
- * (backward), and for the head-dim-128 forward below N ~ 14k; above those, and for the
+ * tokens, causal: fusion wins for head dim 64 below N ~ 1.85k (forward) and N ~ 260
+ * (backward), and for the head-dim-128 forward below N ~ 3.3k; above those, and for the
  * head-dim-128 backward at every N, the pre-rotation pass is cheaper than rotating K tiles on
  * chip. The workspace size functions accept ATTNFUSE_ROPE_AUTO and size for the resolved mode. */
 attnfuse_status attnfuse_rope_auto_mode(int N, int d, int backward, attnfuse_rope_mode* mode);
