@@ -77,15 +77,17 @@ attnfuse_status device_state(int** status) {
 }
 
 // bf16 [B, H, N, d] view with element strides; box (64, box_rows, 1, 1), 128-byte swizzle.
+// box_x = 32 (64-byte rows) takes the 64-byte swizzle.
 attnfuse_status encode_bhnd(CUtensorMap* m, const void* ptr, const int64_t st[4], int B, int H,
-                            int N, int d, const char* name, int box_rows = 128) {
+                            int N, int d, const char* name, int box_rows = 128, int box_x = 64) {
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)H, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)st[2] * 2, (cuuint64_t)st[1] * 2, (cuuint64_t)st[0] * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t box[4] = {(cuuint32_t)box_x, (cuuint32_t)box_rows, 1, 1};
   cuuint32_t es[4] = {1, 1, 1, 1};
   CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims,
                         strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        box_x == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS)
     return fail(ATTNFUSE_ERR_INVALID_ARG, "%s: tensor map encode failed (CUresult %d)", name,
@@ -148,6 +150,17 @@ int rope_table_rows(int N) { return N < 128 ? 128 : N; }
 size_t fused_k_bytes(int B, int Hkv, int N, int d) {
   return align_up((size_t)B * Hkv * N * d * 2, 256);
 }
+// Head dim 64 runs on the persistent CTA-pair forward (fwd_pp.cuh) when its work units share K
+// tiles across heads (an even GQA group) or are long, else on the one-CTA forward (fwd.cu).
+// A pair-kernel unit is four 128-row query tiles of one KV head; with one query head per KV
+// head they are four consecutive positions, whose kv ranges differ, and few units balance
+// poorly over the clusters. Measured on GB300 (ms, no RoPE / fused RoPE, causal):
+//   B=4 Hq=32 Hkv=8 N=4096   pairs 0.512 / 0.544   one-CTA 0.557 / 0.617
+//   B=8 Hq=32 Hkv=8 N=2048   pairs 0.297 / 0.328   one-CTA 0.328 / 0.374
+//   B=1 H=16 N=16384         pairs 0.935 / 0.974   one-CTA 0.984 / 1.072
+//   B=2 H=16 N=4096          pairs 0.164 / 0.191   one-CTA 0.150 / 0.186
+//   B=16 H=16 N=1024         pairs 0.158 / 0.203   one-CTA 0.117 / 0.151
+bool d64_on_pairs(int g, int N) { return g % 2 == 0 || N >= 8192; }
 // Head dim 64 (one CTA per 256 query rows, not persistent): rotating each K tile once and
 // sharing it through L2 pays when many query tiles re-read it; with few readers the copy's
 // latency on the first reader's path costs more than rotating K stages in place per CTA.
@@ -398,15 +411,16 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
     qa = qr; ka = kr; qs = qs_c; ks = ks_c;
   }
-  if (rope_mode == ATTNFUSE_ROPE_FUSED && d == 128) {
-    // head dim 128: Q is rotated in the forward, per work unit in shared memory; K (1/g of Q
-    // with GQA) by one pass into the workspace copy K' before it, with the forward's chains
+  const bool pairs = d == 128 || d64_on_pairs(Hq / Hkv, N);  // the persistent CTA-pair forward
+  if (rope_mode == ATTNFUSE_ROPE_FUSED && pairs) {
+    // Q is rotated in the forward, per work unit in shared memory; K (1/g of Q with GQA) by
+    // one pass into the workspace copy K' before it, with the forward's chains
     uint8_t* kr = static_cast<uint8_t*>(workspace) + rope_table_bytes(N, d);
     cudaError_t e = launch_prerotate(k, k_strides, kr, B, Hkv, N, d, cs, true, 1, stream, st);
     if (e != cudaSuccess) return cuda_fail(e, "K rotation launch");
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
     ka = kr; ks = ks_c;
-  } else if (rope_mode == ATTNFUSE_ROPE_FUSED && (d == 128 || share_rotated_k_d64(N, p.var))) {
+  } else if (rope_mode == ATTNFUSE_ROPE_FUSED && share_rotated_k_d64(N, p.var)) {
     // K is rotated once per call inside the forward, per 64-key block (head dim 128) or
     // 128-key tile (head dim 64), by whichever CTA needs it first, into a workspace copy that
     // every CTA then loads with TMA
@@ -421,9 +435,9 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     ka = p.k_rot; ks = ks_c;
   }
   if ((rc = encode_bhnd(&p.tmQ, qa, qs, B, Hq, N, d, "q"))) return rc;
-  // head dim 128 runs on CTA pairs, each loading 64-key halves of K
-  if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k", d == 128 ? 64 : 128))) return rc;
-  if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v"))) return rc;
+  // the CTA-pair forward loads 64-key halves of K and d/2-dim halves of V
+  if ((rc = encode_bhnd(&p.tmK, ka, ks, B, Hkv, N, d, "k", pairs ? 64 : 128))) return rc;
+  if ((rc = encode_bhnd(&p.tmV, v, v_strides, B, Hkv, N, d, "v", 128, pairs && d == 64 ? 32 : 64))) return rc;
   p.rope_cs = cs;
   p.out = static_cast<__nv_bfloat16*>(out);
   p.o_sb = o_strides[0]; p.o_sh = o_strides[1]; p.o_sn = o_strides[2];
@@ -440,8 +454,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   if (grid > 0x7fffffff) return fail(ATTNFUSE_ERR_UNSUPPORTED, "problem too large (grid %lld)", (long long)grid);
   const int rk = rope_mode == ATTNFUSE_ROPE_FUSED ? kRopeFused
                  : rope_mode == ATTNFUSE_ROPE_PREROTATE ? kRopePrerotated : kRopeNone;
-  cudaError_t e = d == 128 ? launch_fwd_pp(p, rk, p.var.norm, stream)
-                           : launch_fwd(p, d, rk, (int)grid, stream);
+  cudaError_t e = pairs ? launch_fwd_pp(p, d, rk, p.var.norm, stream)
+                        : launch_fwd(p, d, rk, (int)grid, stream);
   if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return ok();
 }
@@ -526,7 +540,7 @@ attnfuse_status attnfuse_fwd_fp8(const void* q, const int64_t q_strides[4], cons
   p.scale = s_qk;
   p.o_scale = v_scale;
   p.status = st;
-  e = launch_fwd_pp(p, kFp8, p.var.norm, stream);
+  e = launch_fwd_pp(p, 128, kFp8, p.var.norm, stream);
   if (e != cudaSuccess) return cuda_fail(e, "e4m3 forward launch");
   return ok();
 }

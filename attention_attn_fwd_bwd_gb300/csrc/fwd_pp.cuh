@@ -44,22 +44,31 @@ namespace afx {
 
 namespace {
 
-constexpr int kD = 128;                // head dim
 constexpr int kBM = 128;               // query rows per slot and CTA
 constexpr int kBN = 128;               // keys per kv tile (64 per CTA for K)
 constexpr int kThreads = 512;
-constexpr int kKSt = 3;                // K stages (released when both slots' S are done)
-constexpr int kVSt = 2;                // V stages (released when both slots' PV are done)
+constexpr int kStMax = 4;              // largest K / V stage count
 constexpr int kRing = 4;               // unit metadata entries in flight
-constexpr uint32_t kQTile = kBM * kD * 2;        // 32 KB: 128 rows x 128 dims, 2 panels
-constexpr uint32_t kKHalf = 64u * kD * 2u;       // 16 KB: 64 keys x 128 dims, 2 panels of 8 KB
-constexpr uint32_t kVHalf = kBN * 64u * 2u;      // 16 KB: 128 keys x 64 dims, 1 panel
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffP = 2 * kQTile;           // P of slot s: bf16, laid out like a Q tile
-constexpr uint32_t kOffK = kOffP + 2 * kQTile;
-constexpr uint32_t kOffV = kOffK + kKSt * kKHalf;
-constexpr uint32_t kOffCtl = kOffV + kVSt * kVHalf;
+constexpr uint32_t kPTile = kBM * kBN * 2;       // 32 KB: P of one slot, two 64-key panels
 constexpr uint32_t kTmS = 0, kTmO = 256;         // + 128 * slot
+
+// Shared-memory plan for head dim D (128 or 64). Q, K and P rows are 128-byte swizzled (one
+// 64-dim panel per 128 bytes); each CTA's half of a V tile holds D/2 dims of 128 keys: 128-byte
+// rows for D = 128, 64-byte rows (64-byte swizzle) for D = 64.
+template <int D>
+struct PPCfg {
+  static constexpr int KSt = D == 128 ? 3 : 4;   // K stages (released when both slots' S are done)
+  static constexpr int VSt = D == 128 ? 2 : 4;   // V stages (released when both slots' PV are done)
+  static constexpr uint32_t QTile = kBM * D * 2;
+  static constexpr uint32_t KHalf = 64u * D * 2u;
+  static constexpr uint32_t VHalf = kBN * (D / 2) * 2u;
+  static constexpr uint32_t OffQ = 0;
+  static constexpr uint32_t OffP = 2 * QTile;
+  static constexpr uint32_t OffK = OffP + 2 * kPTile;
+  static constexpr uint32_t OffV = OffK + KSt * KHalf;
+  static constexpr uint32_t OffCtl = OffV + VSt * VHalf;
+  static_assert(KSt <= kStMax && VSt <= kStMax, "stage arrays");
+};
 
 constexpr uint32_t kRegsLow = 56;    // warpgroup 0: producer, issuers, scheduler
 constexpr uint32_t kRegsRot = 104;    // warpgroup 3: K rotators
@@ -82,10 +91,10 @@ struct UnitMeta {
 };
 
 struct Ctl {
-  uint64_t q_full[2], k_full[kKSt], v_full[kVSt];   // local TMA completion
-  uint64_t q_empty[2], k_empty[kKSt], v_empty[kVSt];  // MMA commits (multicast to both CTAs)
+  uint64_t q_full[2], k_full[kStMax], v_full[kStMax];   // local TMA completion
+  uint64_t q_empty[2], k_empty[kStMax], v_empty[kStMax];  // MMA commits (multicast to both CTAs)
   uint64_t s_full[2], o_full[2], pv_done[2];           // MMA commits (multicast)
-  uint64_t q_ready[2], k_ready[kKSt], v_ready[kVSt], p_full[2], s_free[2];  // even CTA: both CTAs arrive
+  uint64_t q_ready[2], k_ready[kStMax], v_ready[kStMax], p_full[2], s_free[2];  // even CTA: both CTAs arrive
   uint64_t meta_full[kRing], meta_empty[kRing];
   uint64_t mma_final;
   uint32_t tmem_base;
@@ -93,8 +102,9 @@ struct Ctl {
   UnitMeta ring[kRing];
 };
 
-constexpr size_t kSmem = 1024 + kOffCtl + sizeof(Ctl);
-static_assert(kSmem <= 232448, "shared memory budget");
+template <int D>
+__host__ __device__ constexpr size_t pp_smem() { return 1024 + PPCfg<D>::OffCtl + sizeof(Ctl); }
+static_assert(pp_smem<128>() <= 232448 && pp_smem<64>() <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool pbit(const uint32_t* w, int i) { return (w[i >> 5] >> (i & 31)) & 1u; }
 
@@ -264,9 +274,16 @@ __device__ void fill_meta(UnitMeta& M, const FwdParams& p, const Sched& S, int c
 // kFp8: e4m3 Q and K used as they are; V widened to bf16 by the host's pass).
 // BIAS: score bias compiled in (0 none, 1 ALiBi, 2 additive). NORM: 0 softmax, 1 ReLU
 // normaliser (P = relu(s) / N, no row sum).
-template <int RK, int BIAS, int NORM>
+template <int RK, int BIAS, int NORM, int D>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     fwd_pp_kernel(const __grid_constant__ FwdParams p) {
+  using C = PPCfg<D>;
+  constexpr int kD = D;
+  constexpr int kKSt = C::KSt, kVSt = C::VSt;
+  constexpr uint32_t kQTile = C::QTile, kKHalf = C::KHalf, kVHalf = C::VHalf;
+  constexpr uint32_t kOffQ = C::OffQ, kOffP = C::OffP, kOffK = C::OffK, kOffV = C::OffV,
+                     kOffCtl = C::OffCtl;
+  constexpr size_t kSmem = pp_smem<D>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -369,7 +386,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             dq = true;
           } else if (uq == 0 || mbar_test(&ctl->q_empty[sq], (uq - 1) & 1)) {
             mbar_arrive_expect_tx(&ctl->q_full[sq], FP8 ? kQTile / 2 : kQTile);
-            for (int pn = 0; pn < (FP8 ? 1 : 2); ++pn)
+            for (int pn = 0; pn < (FP8 ? 1 : kD / 64); ++pn)
               tma_load_4d_hint(smem + kOffQ + sq * kQTile + pn * (kBM * 128), &p.tmQ, &ctl->q_full[sq],
                                pn * 64, M.q0[sq][rank], M.head[sq][rank], M.b, pol_stream);
             if (++sq == 2) {
@@ -394,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int st = ik % kKSt;
               if (ik < kKSt || mbar_test(&ctl->k_empty[st], ((ik / kKSt) - 1) & 1)) {
                 mbar_arrive_expect_tx(&ctl->k_full[st], FP8 ? kKHalf / 2 : kKHalf);
-                for (int pn = 0; pn < (FP8 ? 1 : 2); ++pn)
+                for (int pn = 0; pn < (FP8 ? 1 : kD / 64); ++pn)
                   tma_load_4d_hint(smem + kOffK + st * kKHalf + pn * (64 * 128), &p.tmK, &ctl->k_full[st],
                                    pn * 64, jk * kBN + rank * 64, M.kvh, M.b, pol_keep);
                 ++ik;
@@ -419,7 +436,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               const int st = iv % kVSt;
               if (iv < kVSt || mbar_test(&ctl->v_empty[st], ((iv / kVSt) - 1) & 1)) {
                 mbar_arrive_expect_tx(&ctl->v_full[st], kVHalf);
-                tma_load_4d_hint(smem + kOffV + st * kVHalf, &p.tmV, &ctl->v_full[st], rank * 64,
+                tma_load_4d_hint(smem + kOffV + st * kVHalf, &p.tmV, &ctl->v_full[st], rank * (kD / 2),
                                  jv * kBN, M.kvh, M.b, pol_keep);
                 ++iv;
                 jv = next_tile(M, bs, jv);
@@ -491,9 +508,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       static_assert(kSmem < (1u << 18), "descriptor address field");
       constexpr uint32_t dhi = desc_sw128_hi(1024);
       const uint32_t dQ = desc_sw128_lo(smem_u32(smem + kOffQ + s * kQTile), 16);
-      const uint32_t dP = desc_sw128_lo(smem_u32(smem + kOffP + s * kQTile), 16);
+      const uint32_t dP = desc_sw128_lo(smem_u32(smem + kOffP + s * kPTile), 16);
       const uint32_t dK0 = desc_sw128_lo(smem_u32(smem + kOffK), 16);
       const uint32_t dV0 = desc_sw128_lo(smem_u32(smem + kOffV), kVHalf);
+      // V halves: D/2 dims of 128 keys, MN-major; 128-byte rows (8-key atoms of 1024 bytes) for
+      // D = 128, 64-byte rows (64-byte swizzle, atoms of 512 bytes) for D = 64
+      constexpr uint32_t dhi_v = kD == 128 ? desc_sw128_hi(1024) : desc_sw64_hi(512);
+      constexpr uint32_t kVStep = (kD / 2) * 2 * 16;  // bytes of 16 keys
       const uint32_t tS = tmem + kTmS + 128 * s, tO = tmem + kTmO + 128 * s;
       int ik = 0;          // kv tiles walked (K and V copy index)
       int sc = 0;          // S issued (phases of s_full and s_free)
@@ -511,13 +532,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int vs = pend_v % kVSt;
         const uint32_t bv = dV0 + vs * (kVHalf >> 4);
         if (pend_acc)
-          mma_ss_pair_w<1>(tO, dP, bv, dhi, idesc_o);
+          mma_ss_pair_w2<1>(tO, dP, dhi, bv, dhi_v, idesc_o);
         else
-          mma_ss_pair_w<0>(tO, dP, bv, dhi, idesc_o);
+          mma_ss_pair_w2<0>(tO, dP, dhi, bv, dhi_v, idesc_o);
 #pragma unroll
         for (int kk = 1; kk < kBN / 16; ++kk)
-          mma_ss_pair_w<1>(tO, dP + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4),
-                           bv + kk * (2048 >> 4), dhi, idesc_o);
+          mma_ss_pair_w2<1>(tO, dP + (((kk >> 2) * (kBM * 128) + (kk & 3) * 32) >> 4), dhi,
+                            bv + kk * (kVStep >> 4), dhi_v, idesc_o);
         mma_commit_pair(&ctl->v_empty[vs], 3);
         mma_commit_pair(&ctl->pv_done[s], 3);
         if (pend_last) mma_commit_pair(&ctl->o_full[s], 3);
@@ -541,10 +562,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) return;
           }
           ok = mbar_wait_cluster(&ctl->q_ready[s], u & 1, status, abort_flag);
-          if (ok && ns == 0) {
-            mma_commit_pair(&ctl->q_empty[s], 3);
-            mma_commit_pair(&ctl->o_full[s], 3);
-          }
+          // a slot with no tiles in this unit releases its Q buffer at once; it has no O, and
+          // its softmax writes zeros without waiting for one (o_full completes one phase per
+          // unit with tiles, so an empty slot can never run a phase ahead of its softmax)
+          if (ok && ns == 0) mma_commit_pair(&ctl->q_empty[s], 3);
           opened = true;
         };
         for (int j = jb; ok && j < je; j = next_tile(M, bs, j), ++ik) {
@@ -612,17 +633,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (ROPE) {
       // ---- Q rotators: Q' = R_m Q of each unit's tiles, in place in shared memory (fp16), as
       // soon as a tile lands; warps 12-13 take slot 0, warps 14-15 slot 1. Warp w2 of a slot
-      // rotates the rows of the query-tile recurrence chains (query_cs8) c0 = w2 + 2i, rows
-      // c0 + 8k, each chain starting from its table entry and stepping 8 positions; lane f
-      // takes dims 2f, 2f+1 and their partners 64+2f, 64+2f+1. K' comes from the rotation
-      // pass the host launches before this kernel. ----
+      // rotates the rows of the query-tile recurrence chains (query_cs8) c0 = w2 + 2i (i < 4),
+      // rows c0 + 8k, each chain starting from its table entry and stepping 8 positions. Lane f
+      // of a row takes dims 2f, 2f+1 and their partners D/2+2f, D/2+2f+1 (F4 = D/4 lanes per
+      // row, so a warp instruction covers RPI = 32/F4 chains). K' comes from the rotation pass
+      // the host launches before this kernel. ----
+      constexpr int F4 = kD / 4, RPI = 32 / F4;
       const int s = (warp - 12) >> 1, w2 = (warp - 12) & 1;
+      const int f = lane % F4, rsub = lane / F4;
       const int N = p.N;
       const uint64_t pol_tab = l2_policy_evict_last();
       const float4* tab = reinterpret_cast<const float4*>(p.rope_cs);
-      const float4 wstep = ldg_f4_hint(tab + (size_t)8 * (kD / 4) + lane, pol_tab);
+      const float4 wstep = ldg_f4_hint(tab + (size_t)8 * F4 + f, pol_tab);
       uint8_t* tile = smem + kOffQ + s * kQTile;
-      const uint32_t within = static_cast<uint32_t>(lane & 3) * 4u;
+      const uint32_t within = static_cast<uint32_t>(f & 3) * 4u;
       uint32_t f16max = 0;  // |Q'| as fp16 bits, per half
       bool ok = true;
       for (int u = 0; ok; ++u) {
@@ -633,10 +657,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!M.live) break;
         const int qq0 = M.q0[s][rank];
         const bool qvalid = M.qv[s][rank] != 0;
-        float4 cs[4];
+        float4 cs[4 / RPI];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-          cs[i] = qvalid ? ldg_f4_hint(tab + (size_t)min(qq0 + w2 + 2 * i, N - 1) * (kD / 4) + lane, pol_tab)
+        for (int i = 0; i < 4 / RPI; ++i)
+          cs[i] = qvalid ? ldg_f4_hint(tab + (size_t)min(qq0 + w2 + 2 * (RPI * i + rsub), N - 1) * F4 + f, pol_tab)
                          : make_float4(0.f, 0.f, 0.f, 0.f);
         ok = __all_sync(0xffffffffu, mbar_wait(&ctl->q_full[s], u & 1, status, abort_flag));
         if (!ok) break;
@@ -644,19 +668,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll 2
           for (int k = 0; k < kBM / 8; ++k) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int rr = w2 + 2 * i + 8 * k;
+            for (int i = 0; i < 4 / RPI; ++i) {
+              const int rr = w2 + 2 * (RPI * i + rsub) + 8 * k;
               if (qq0 + rr < N) {
-                const uint32_t off = sw128_offset(rr, lane >> 2) + within;
-                const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + off);
-                const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + kBM * 128 + off);
+                const uint32_t offl = sw128_offset(rr, f >> 2) + within;
+                const uint32_t offh = kD == 128 ? offl + kBM * 128 : sw128_offset(rr, (f >> 2) + 4) + within;
+                const uint32_t l2w = *reinterpret_cast<const uint32_t*>(tile + offl);
+                const uint32_t h2w = *reinterpret_cast<const uint32_t*>(tile + offh);
                 float yl0, yh0, yl1, yh1;
                 rot_pair(bf16lo_to_f32(l2w), bf16lo_to_f32(h2w), cs[i].x, cs[i].y, yl0, yh0);
                 rot_pair(bf16hi_to_f32(l2w), bf16hi_to_f32(h2w), cs[i].z, cs[i].w, yl1, yh1);
                 const uint32_t wl = pack_f16x2_sat(yl0, yl1), wh = pack_f16x2_sat(yh0, yh1);
                 f16max = f16_absmax(f16_absmax(f16max, wl), wh);
-                *reinterpret_cast<uint32_t*>(tile + off) = wl;
-                *reinterpret_cast<uint32_t*>(tile + kBM * 128 + off) = wh;
+                *reinterpret_cast<uint32_t*>(tile + offl) = wl;
+                *reinterpret_cast<uint32_t*>(tile + offh) = wh;
               }
               float c0f, s0f, c1f, s1f;
               rot_pair(cs[i].x, cs[i].y, wstep.x, wstep.y, c0f, s0f);
@@ -691,6 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* const visits = var.visits;
     int sc = 0;  // S of this slot consumed (phase of s_full)
     int pc = 0;  // P of this slot written (phase of p_full; PV pc-1 completes phase pc-1 of pv_done)
+    int oc = 0;  // units with tiles finished (phase of o_full)
     bool ok = true;
     // Q' = R_m Q of unit un in place (fp16 with fused RoPE), then the slot's MMAs may read it.
     auto prep_q = [&](const UnitMeta& Mq, int un) {
@@ -844,7 +870,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
             const float alpha = grow ? ex2_approx(m_run - m_new) : 1.f;
 #pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
+            for (int ch = 0; ch < kD / 32; ++ch) {
               uint32_t o[32];
               tmem_ld32(tO + ch * 32, o);
               tmem_wait_ld();
@@ -876,7 +902,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         {
-          uint8_t* prow = smem + kOffP + s * kQTile;
+          uint8_t* prow = smem + kOffP + s * kPTile;
 #pragma unroll
           for (int q = 0; q < 16; ++q)
             *reinterpret_cast<uint4*>(prow + (q >> 3) * (kBM * 128) + sw128_offset(r, q & 7)) =
@@ -905,16 +931,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (!ok) break;
       }
       // ---- epilogue: O / l and LSE once the slot's last PV has completed ----
-      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[s], u & 1, status, abort_flag));
-      if (!ok) break;
-      tc_fence_after();
       const bool have = M.ns[s] > 0;
+      if (have) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[s], oc & 1, status, abort_flag));
+        if (!ok) break;
+        ++oc;
+      }
+      tc_fence_after();
       if (valid) {
         float inv = NORM == 1 ? 1.f : ((l_run > 0.f) ? 1.f / l_run : 0.f);
         if constexpr (FP8) inv *= p.o_scale;
         __nv_bfloat16* orow = p.out + b * p.o_sb + head * p.o_sh + (int64_t)m * p.o_sn;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
+        for (int ch = 0; ch < kD / 32; ++ch) {
           uint32_t o[32];
           if (have) {
             tmem_ld32(tO + ch * 32, o);
@@ -957,11 +986,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 using FwdFn = void (*)(FwdParams);
 
 // The kernel instance for one RoPE kind, bias kind and normaliser.
-template <int RK>
+template <int RK, int D>
 FwdFn fwd_pp_pick(int bias, int norm) {
   if (norm == 1)
-    return bias == 1 ? fwd_pp_kernel<RK, 1, 1> : bias == 2 ? fwd_pp_kernel<RK, 2, 1> : fwd_pp_kernel<RK, 0, 1>;
-  return bias == 1 ? fwd_pp_kernel<RK, 1, 0> : bias == 2 ? fwd_pp_kernel<RK, 2, 0> : fwd_pp_kernel<RK, 0, 0>;
+    return bias == 1 ? fwd_pp_kernel<RK, 1, 1, D> : bias == 2 ? fwd_pp_kernel<RK, 2, 1, D> : fwd_pp_kernel<RK, 0, 1, D>;
+  return bias == 1 ? fwd_pp_kernel<RK, 1, 0, D> : bias == 2 ? fwd_pp_kernel<RK, 2, 0, D> : fwd_pp_kernel<RK, 0, 0, D>;
 }
 
 }  // namespace afx

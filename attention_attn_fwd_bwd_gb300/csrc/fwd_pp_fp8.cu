@@ -6,7 +6,7 @@
 
 namespace afx {
 
-FwdFn fwd_pp_pick_fp8(int bias, int norm) { return fwd_pp_pick<kFp8>(bias, norm); }
+FwdFn fwd_pp_pick_fp8(int bias, int norm) { return fwd_pp_pick<kFp8, 128>(bias, norm); }
 
 namespace {
 

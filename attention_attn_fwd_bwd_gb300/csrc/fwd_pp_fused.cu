@@ -3,6 +3,6 @@
 
 namespace afx {
 
-FwdFn fwd_pp_pick_fused(int bias, int norm) { return fwd_pp_pick<kRopeFused>(bias, norm); }
+FwdFn fwd_pp_pick_fused(int bias, int norm) { return fwd_pp_pick<kRopeFused, 128>(bias, norm); }
 
 }  // namespace afx

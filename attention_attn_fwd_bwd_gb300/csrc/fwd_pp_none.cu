@@ -3,6 +3,6 @@
 
 namespace afx {
 
-FwdFn fwd_pp_pick_none(int bias, int norm) { return fwd_pp_pick<kRopeNone>(bias, norm); }
+FwdFn fwd_pp_pick_none(int bias, int norm) { return fwd_pp_pick<kRopeNone, 128>(bias, norm); }
 
 }  // namespace afx

@@ -3,6 +3,6 @@
 
 namespace afx {
 
-FwdFn fwd_pp_pick_pre(int bias, int norm) { return fwd_pp_pick<kRopePrerotated>(bias, norm); }
+FwdFn fwd_pp_pick_pre(int bias, int norm) { return fwd_pp_pick<kRopePrerotated, 128>(bias, norm); }
 
 }  // namespace afx

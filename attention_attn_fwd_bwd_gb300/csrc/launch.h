@@ -94,8 +94,8 @@ constexpr int kFp8 = 3;             // head-dim-128 forward: e4m3 Q and K (score
 cudaError_t launch_fwd(const FwdParams& p, int d, int rope_kind, int grid, cudaStream_t stream);
 // Head dim 128, persistent: clusters of two CTAs walk units of four 128-row query tiles of
 // one KV head (two independent softmax slots per CTA). norm: 0 softmax, 1 ReLU (P = relu(s)/N).
-size_t fwd_pp_smem_size();
-cudaError_t launch_fwd_pp(FwdParams p, int rope_kind, int norm, cudaStream_t stream);
+size_t fwd_pp_smem_size(int d);
+cudaError_t launch_fwd_pp(FwdParams p, int d, int rope_kind, int norm, cudaStream_t stream);
 cudaError_t launch_rope_table(float2* cs, int N, int half, const RopeFreqs& f,
                               cudaStream_t stream);
 // block: 0 = rotate with the table entry of each row; -1 = the forward kernels' query-tile

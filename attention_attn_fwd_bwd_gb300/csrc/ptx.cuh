@@ -467,6 +467,11 @@ __device__ __forceinline__ uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_b
   return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
 
+// The high word of a 64-byte-swizzle descriptor (rows of 64 bytes, 8-row atoms of 512 bytes).
+__host__ __device__ constexpr uint32_t desc_sw64_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (4u << 29);
+}
+
 // Pair MMAs taking split descriptors (see above); ACC: accumulate into D (1) or overwrite (0).
 template <int ACC>
 __device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo,
@@ -478,6 +483,19 @@ __device__ __forceinline__ void mma_ss_pair_w(uint32_t d_tmem, uint32_t a_lo, ui
       "mov.b64 b, {%2, %3};\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %4, p;\n\t}" ::"r"(d_tmem),
       "r"(a_lo), "r"(b_lo), "r"(hi), "r"(idesc), "n"(ACC)
+      : "memory");
+}
+// The same with separate high words for A and B (operands of different swizzle modes).
+template <int ACC>
+__device__ __forceinline__ void mma_ss_pair_w2(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
+                                               uint32_t b_lo, uint32_t b_hi, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b64 a, b;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "mov.b64 a, {%1, %2};\n\t"
+      "mov.b64 b, {%3, %4};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_lo), "r"(a_hi), "r"(b_lo), "r"(b_hi), "r"(idesc), "n"(ACC)
       : "memory");
 }
 // The same with 8-bit operands (kind::f8f6f4; A and B of the same format, set in idesc).

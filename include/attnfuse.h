@@ -64,12 +64,12 @@ typedef int attnfuse_status;
 typedef enum {
   ATTNFUSE_ROPE_NONE = 0,      /* no rotation: plain scaled_dot_product */
   ATTNFUSE_ROPE_FUSED = 1,     /* rotate in the attention kernel: each Q tile once, in
-                                  shared memory, as it lands (no Q' round trip). K: head dim
-                                  128, one pass writes K' to the workspace just before the
-                                  forward (K is 1/g of Q's size); head dim 64, the forward
-                                  rotates each K tile once per call into a workspace copy
-                                  shared through L2 (long sequences) or per CTA in shared
-                                  memory (short ones) */
+                                  shared memory, as it lands (no Q' round trip). K: one pass
+                                  writes K' to the workspace just before the forward (K is 1/g
+                                  of Q's size); on the head-dim-64 one-CTA forward (one query
+                                  head per KV head, N < 8192) the forward rotates each K tile
+                                  once per call into a workspace copy shared through L2 (long
+                                  sequences) or per CTA in shared memory (short ones) */
   ATTNFUSE_ROPE_PREROTATE = 2, /* separate rotate kernel writes Q', K' to the workspace, then
                                   attention runs without rotation (the paper's baseline) */
   ATTNFUSE_ROPE_AUTO = 3       /* the faster of FUSED and PREROTATE for this call's N, head dim

@@ -278,3 +278,13 @@ def test_fp16_range_is_reported(d, rope_mode, which):
     assert af.device_status() == 0
     af.fwd(q, k, v, rope_theta=1e4, rope_mode=af.ROPE_NONE)
     assert af.device_status() == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("rope_mode", [af.ROPE_NONE, af.ROPE_FUSED])
+@pytest.mark.parametrize("N", [129, 256])
+def test_many_units_with_an_empty_slot(d, rope_mode, N):
+    """With one head per work unit (Hq == Hkv) and two query tiles, a unit's second slot has no
+    rows; many such units per cluster (B * H >> the number of clusters) must not let that
+    slot's bookkeeping run a unit ahead of its softmax."""
+    _run(40, 4, 4, N, d, rope_mode, "causal", seed=N + d)
