@@ -376,7 +376,6 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
   if ((rc = to_dev_variant(variant, N, Hq, &p.var))) return rc;
   if (p.var.norm == ATTNFUSE_NORM_RELU) {
     if (lse) return fail(ATTNFUSE_ERR_INVALID_ARG, "relu_attention has no LSE: pass lse = NULL");
-    if (d != 128) return fail(ATTNFUSE_ERR_UNSUPPORTED, "relu_attention needs head dim 128");
   }
   size_t need = 0;
   if ((rc = attnfuse_fwd_workspace_size(B, Hq, Hkv, N, d, rope_mode, &need))) return rc;
@@ -411,7 +410,8 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
     ks_c[0] = (int64_t)Hkv * N * d; ks_c[1] = (int64_t)N * d; ks_c[2] = d; ks_c[3] = 1;
     qa = qr; ka = kr; qs = qs_c; ks = ks_c;
   }
-  const bool pairs = d == 128 || d64_on_pairs(Hq / Hkv, N);  // the persistent CTA-pair forward
+  // the persistent CTA-pair forward (the only one with the ReLU normaliser)
+  const bool pairs = d == 128 || p.var.norm == ATTNFUSE_NORM_RELU || d64_on_pairs(Hq / Hkv, N);
   if (rope_mode == ATTNFUSE_ROPE_FUSED && pairs) {
     // Q is rotated in the forward, per work unit in shared memory; K (1/g of Q with GQA) by
     // one pass into the workspace copy K' before it, with the forward's chains

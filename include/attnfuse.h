@@ -103,8 +103,8 @@ typedef enum {
  * without defining it; this library reads it as ReLU attention divided by the sequence length:
  *   O_m = (1/N) sum_{allowed n} max(s_mn, 0) v_n.
  * It has no log-sum-exp (lse must be NULL) and no backward (attnfuse_bwd returns
- * ATTNFUSE_ERR_UNSUPPORTED); the forward supports it for head dim 128 with every mask, bias
- * and rope mode. */
+ * ATTNFUSE_ERR_UNSUPPORTED); the forward supports it for head dims 64 and 128 with every mask,
+ * bias and rope mode. */
 typedef enum {
   ATTNFUSE_NORM_SOFTMAX = 0,
   ATTNFUSE_NORM_RELU = 1

@@ -1,6 +1,6 @@
 """relu_attention (the paper's §3.1 normaliser, read as O_m = (1/N) sum_n max(s_mn, 0) v_n over
 the visible keys) on the GPU against the fp64 oracle: every mask and bias kind, each rope mode,
-GQA ratios that map to each unit shape of the head-dim-128 forward, ragged N."""
+GQA ratios that map to each unit shape of the persistent forward, head dims 64 and 128, ragged N."""
 import math
 
 import numpy as np
@@ -23,15 +23,15 @@ def _lib():
     af.load()
 
 
-def _relu_run(B, Hq, Hkv, N, rope_mode, vname, seed, theta=1e4):
+def _relu_run(B, Hq, Hkv, N, rope_mode, vname, seed, theta=1e4, d=128):
     import oracle
 
     dev = torch.device("cuda")
-    x = inputs.prefill(B, Hq, Hkv, N, 128, seed)
+    x = inputs.prefill(B, Hq, Hkv, N, d, seed)
     q, k, v = (x[n].to(dev) for n in ("q", "k", "v"))
     gvar, ovar = variant_pair(vname, N, Hq, dev, seed, B=B)
     gvar.norm, ovar.norm = af.NORM_RELU, oracle.NORM_RELU
-    scale = 1.0 / math.sqrt(128)
+    scale = 1.0 / math.sqrt(d)
     out, lse = af.fwd(q, k, v, scale=scale, rope_theta=theta, rope_mode=rope_mode, variant=gvar)
     torch.cuda.synchronize()
     assert lse is None
@@ -66,3 +66,10 @@ def test_relu_rejects_lse_and_backward():
     out, _ = af.fwd(q, k, v, variant=var)
     with pytest.raises(af.AttnfuseError, match="softmax normaliser only"):
         af.bwd(q, k, v, out, torch.zeros(1, 2, 64, device=dev), out, variant=var)
+
+
+@pytest.mark.parametrize("gqa", [(4, 1), (2, 2)])
+@pytest.mark.parametrize("rope_mode", [af.ROPE_NONE, af.ROPE_FUSED])
+def test_relu_head_dim_64(gqa, rope_mode):
+    """Head dim 64 runs relu_attention on the persistent pair kernel for every group size."""
+    _relu_run(2, gqa[0], gqa[1], 300, rope_mode, "causal", seed=64 + gqa[0], d=64)
