@@ -95,6 +95,7 @@ struct Ctl {
   uint64_t q_empty[2], k_empty[kStMax], v_empty[kStMax];  // MMA commits (multicast to both CTAs)
   uint64_t s_full[2], o_full[2], pv_done[2];           // MMA commits (multicast)
   uint64_t q_ready[2], k_ready[kStMax], v_ready[kStMax], p_full[2], s_free[2];  // even CTA: both CTAs arrive
+  uint64_t o_read[2];  // even CTA: the slot's softmax warps of both CTAs took an O phase before an empty unit
   uint64_t meta_full[kRing], meta_empty[kRing];
   uint64_t mma_final;
   uint32_t tmem_base;
@@ -292,6 +293,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const VariantDev& var = p.var;
   constexpr bool ROPE = (RK == kRopeFused);
   constexpr bool FP8 = (RK == kFp8);
+  // How a slot with no tiles in a unit completes that unit's O phase (both keep one o_full
+  // phase per unit, in order with the softmax's waits). With fused RoPE the issuer commits it
+  // once the slot's softmax warps of both CTAs have taken the previous phase (o_read); otherwise
+  // the slot's softmax warps complete it themselves. Both are correct; each instance uses the
+  // one that measured faster for it.
+  constexpr bool kORead = ROPE;
   const int rank = static_cast<int>(cluster_ctarank());
   const int cid = static_cast<int>(blockIdx.x) >> 1;
   const Sched S = make_sched(p);
@@ -309,6 +316,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ctl->p_full[s], 8);
       mbar_init(&ctl->s_free[s], 8);    // the slot's 4 softmax warps have read S, both CTAs
       mbar_init(&ctl->pv_done[s], 1);
+      if constexpr (kORead) mbar_init(&ctl->o_read[s], 8);
     }
     for (int s = 0; s < kKSt; ++s) {
       mbar_init(&ctl->k_full[s], 1);
@@ -562,10 +570,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) return;
           }
           ok = mbar_wait_cluster(&ctl->q_ready[s], u & 1, status, abort_flag);
-          // a slot with no tiles in this unit releases its Q buffer at once; it has no O, and
-          // its softmax writes zeros without waiting for one (o_full completes one phase per
-          // unit with tiles, so an empty slot can never run a phase ahead of its softmax)
-          if (ok && ns == 0) mma_commit_pair(&ctl->q_empty[s], 3);
+          // A slot with no tiles in this unit releases its Q buffer at once; it has no O (its
+          // softmax writes zeros). With kORead the issuer completes the unit's O phase without
+          // an MMA; that commit completes as soon as the previous PVs have, so it first waits
+          // until the slot's softmax warps of both CTAs have taken the previous phase (o_full
+          // never runs two phases ahead of a waiter).
+          if (ok && ns == 0) {
+            mma_commit_pair(&ctl->q_empty[s], 3);
+            if constexpr (kORead) {
+              if (u > 0) ok = mbar_wait_cluster(&ctl->o_read[s], (u - 1) & 1, status, abort_flag);
+              if (ok) mma_commit_pair(&ctl->o_full[s], 3);
+            }
+          }
           opened = true;
         };
         for (int j = jb; ok && j < je; j = next_tile(M, bs, j), ++ik) {
@@ -716,7 +732,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint8_t* const visits = var.visits;
     int sc = 0;  // S of this slot consumed (phase of s_full)
     int pc = 0;  // P of this slot written (phase of p_full; PV pc-1 completes phase pc-1 of pv_done)
-    int oc = 0;  // units with tiles finished (phase of o_full)
     bool ok = true;
     // Q' = R_m Q of unit un in place (fp16 with fused RoPE), then the slot's MMAs may read it.
     auto prep_q = [&](const UnitMeta& Mq, int un) {
@@ -932,10 +947,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // ---- epilogue: O / l and LSE once the slot's last PV has completed ----
       const bool have = M.ns[s] > 0;
-      if (have) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[s], oc & 1, status, abort_flag));
-        if (!ok) break;
-        ++oc;
+      if constexpr (!kORead) {
+        if (!have) {
+          // no MMA completes this unit's O phase: the slot's four warps, all past the previous
+          // phase, complete it themselves
+          named_bar_sync(1 + s, 128);
+          if (wq == 0 && lane == 0) mbar_arrive(&ctl->o_full[s]);
+        }
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(&ctl->o_full[s], u & 1, status, abort_flag));
+      if (!ok) break;
+      // o_read phase u: the issuer may complete an empty next unit's O phase
+      if constexpr (kORead) {
+        if (more && lane == 0) arrive_leader(&ctl->o_read[s], rank);
       }
       tc_fence_after();
       if (valid) {
