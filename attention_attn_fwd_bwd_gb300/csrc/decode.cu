@@ -97,6 +97,9 @@ __global__ void __launch_bounds__(kDecThreads) decode_kernel(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  // Launched as a programmatic dependent: the set-up above overlaps the end of the previous
+  // kernel on the stream; global memory is read and written only once that kernel has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 3) {
     // ---- query tile: row h = R_{q_pos} q[b, kvh*g + h], bf16, 128B-swizzled ----
@@ -422,21 +425,23 @@ cudaError_t launch_decode(const DecParams& p, int d, bool rope_q, cudaStream_t s
   }
   cudaError_t e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.splits_used, p.Hkv, p.B);
-  k1<<<grid, kDecThreads, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  // Programmatic dependent launch: the combine grid may start launching while phase 1 drains.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.B * p.Hq);
-  cfg.blockDim = dim3(d);
-  cfg.dynamicSmemBytes = 0;
-  cfg.stream = stream;
+  // Programmatic dependent launches: phase 1's set-up may overlap the previous kernel on the
+  // stream, and the combine grid may start launching while phase 1 drains.
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits_used, p.Hkv, p.B);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k1, p);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(p.B * p.Hq);
+  cfg.blockDim = dim3(d);
+  cfg.dynamicSmemBytes = 0;
   return cudaLaunchKernelEx(&cfg, k2, p);
 }
 

@@ -70,9 +70,9 @@ struct PPCfg {
   static_assert(KSt <= kStMax && VSt <= kStMax, "stage arrays");
 };
 
-constexpr uint32_t kRegsLow = 56;    // warpgroup 0: producer, issuers, scheduler
-constexpr uint32_t kRegsRot = 104;    // warpgroup 3: K rotators
-constexpr uint32_t kRegsSm = 176;    // warpgroups 1, 2: softmax
+constexpr uint32_t kRegsLow = 72;    // warpgroup 0: producer, issuers, scheduler
+constexpr uint32_t kRegsRot = 56;     // warpgroup 3: Q rotators
+constexpr uint32_t kRegsSm = 192;    // warpgroups 1, 2: softmax
 static_assert(kRegsLow + kRegsRot + 2 * kRegsSm <= 4 * (65536 / kThreads),
               "register split exceeds the registers the CTA is launched with");
 
