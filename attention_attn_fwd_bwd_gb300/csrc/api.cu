@@ -283,11 +283,11 @@ attnfuse_status attnfuse_device_status(cudaStream_t stream, int clear, int* code
 // Head dim 64: fusion wins below N* ~ 1.85k (forward; t_prerotate / t_fused over two sweeps:
 // 1.19-1.23 at N = 256, 1.04-1.08 at 1024, 0.98-1.00 at 2048) and ~ 260 (backward, which
 // re-reads each K tile once per query tile). Head dim 128: the persistent forward rotates Q in
-// shared memory and takes K' from a one-pass rotation of K; it wins below N* ~ 3.6k (1.05 at
-// N = 256, 1.02 at 2048, 1.00 at 4096, 0.97 at 16384). The backward pre-rotates at every N.
+// shared memory and takes K' from a one-pass rotation of K; it wins below N* ~ 15k (1.08 at
+// N = 256, 1.04 at 2048, 1.02 at 4096, 1.01 at 8192, 1.00 at 16384). The backward pre-rotates at every N.
 constexpr int kAutoFusedBelowN64Fwd = 1850;
 constexpr int kAutoFusedBelowN64Bwd = 258;
-constexpr int kAutoFusedBelowN128Fwd = 3600;
+constexpr int kAutoFusedBelowN128Fwd = 14900;
 
 static attnfuse_rope_mode resolve_rope(attnfuse_rope_mode m, int N, int d, bool backward) {
   if (m != ATTNFUSE_ROPE_AUTO) return m;

@@ -320,7 +320,7 @@ attnfuse_status attnfuse_rope_prerotate(const void* x, const int64_t x_strides[4
 /* The mode ATTNFUSE_ROPE_AUTO resolves to for sequence length N and head dim d, for the
  * forward (backward = 0) or the backward (backward = 1). Measured on GB300 with B*N = 16384
  * tokens, causal: fusion wins for head dim 64 below N ~ 1.85k (forward) and N ~ 260
- * (backward), and for the head-dim-128 forward below N ~ 3.6k; above those, and for the
+ * (backward), and for the head-dim-128 forward below N ~ 15k; above those, and for the
  * head-dim-128 backward at every N, the pre-rotation pass is cheaper than rotating K tiles on
  * chip. The workspace size functions accept ATTNFUSE_ROPE_AUTO and size for the resolved mode. */
 attnfuse_status attnfuse_rope_auto_mode(int N, int d, int backward, attnfuse_rope_mode* mode);

@@ -157,10 +157,10 @@ def test_rope_auto_mode_rule(lib):
     m = ctypes.c_int()
     auto = lambda N, d, bwd: (lib.attnfuse_rope_auto_mode(N, d, bwd, ctypes.byref(m)), m.value)
     FUSED, PRE = af.ROPE_FUSED, af.ROPE_PREROTATE
-    # head dim 128: fusion wins for the forward below the measured crossover (3600); the
+    # head dim 128: fusion wins for the forward below the measured crossover (14900); the
     # backward pre-rotates at every N
-    assert auto(256, 128, 0) == (OK, FUSED) and auto(3599, 128, 0) == (OK, FUSED)
-    assert auto(3600, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
+    assert auto(256, 128, 0) == (OK, FUSED) and auto(14899, 128, 0) == (OK, FUSED)
+    assert auto(14900, 128, 0) == (OK, PRE) and auto(256, 128, 1) == (OK, PRE)
     # head dim 64: fusion wins below the measured crossovers (forward 1850, backward 258)
     assert auto(1849, 64, 0) == (OK, FUSED) and auto(1850, 64, 0) == (OK, PRE)
     assert auto(257, 64, 1) == (OK, FUSED) and auto(258, 64, 1) == (OK, PRE)

@@ -66,7 +66,7 @@ def test_relu_attention_maps_to_the_relu_normaliser():
 
 def test_rope_auto_rule():
     """The measured crossover (GB300, B*N = 16384): fusion wins for head dim 64 below
-    N ~ 1.85k (forward) and ~ 260 (backward), for the head-dim-128 forward below N ~ 3.6k;
+    N ~ 1.85k (forward) and ~ 260 (backward), for the head-dim-128 forward below N ~ 15k;
     pre-rotation everywhere else."""
     from attention_attn_fwd_bwd_gb300 import _build
 
@@ -80,9 +80,9 @@ def test_rope_auto_rule():
         assert af.rope_auto_mode(N, 64, backward=True) == af.ROPE_FUSED
     for N in (258, 1024, 4096):
         assert af.rope_auto_mode(N, 64, backward=True) == af.ROPE_PREROTATE
-    for N in (1, 256, 2048, 3599):
+    for N in (1, 256, 4096, 14899):
         assert af.rope_auto_mode(N, 128) == af.ROPE_FUSED
-    for N in (3600, 4096, 65536):
+    for N in (14900, 16384, 65536):
         assert af.rope_auto_mode(N, 128) == af.ROPE_PREROTATE
     for N in (1, 256, 4096):
         assert af.rope_auto_mode(N, 128, backward=True) == af.ROPE_PREROTATE
