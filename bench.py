@@ -891,6 +891,10 @@ def run_decode_bench(args, emit=True):
     peaks, src = measured_peaks()
     Hq, Hkv, d, L = 64, 8, 128, 32768
     flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device=dev)  # 4x the L2
+    # A write flush leaves up to a full L2 of dirty lines, written back to HBM while the timed
+    # call reads: 126 MiB of write-back next to the 134 MB a B=1 decode reads. Reading another
+    # buffer of 3x the L2 after the write leaves L2 clean (and still without the cache's lines).
+    evict = torch.zeros(384 * 1024 * 1024, dtype=torch.uint8, device=dev)
     rows = []
     for B in (1, 8):
         x = inputs.decode(B, Hq, Hkv, L, d, seed=5000 + B)
@@ -906,16 +910,19 @@ def run_decode_bench(args, emit=True):
                           workspace=ws)
             call = lambda: af.decode(q, kc, vc, L - 1, rope_theta=5e5, num_splits=splits,
                                      out=out, lse=lse, workspace=ws)
-            res = {"cold": [], "warm": []}
-            # cold L2: the flush (a write of 4x the L2) runs before each timed call
-            for _ in range(30):
-                flush.zero_()
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record()
-                call()
-                e1.record()
-                torch.cuda.synchronize()
-                res["cold"].append(e0.elapsed_time(e1) * 1e3)
+            res = {"cold": [], "cold_dirty": [], "warm": []}
+            # cold L2 before each timed call: a write of 4x the L2, then (clean) a read of 3x
+            for key in ("cold", "cold_dirty"):
+                for _ in range(30):
+                    flush.zero_()
+                    if key == "cold":
+                        evict.max()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record()
+                    call()
+                    e1.record()
+                    torch.cuda.synchronize()
+                    res[key].append(e0.elapsed_time(e1) * 1e3)
             # warm L2, device time: 20 back-to-back calls captured in one CUDA graph (the host's
             # per-call cost is measured separately below)
             g = _graph_of(lambda: [call() for _ in range(20)])
@@ -944,6 +951,9 @@ def run_decode_bench(args, emit=True):
                               "splits_used": used, "us_median_cold_l2": med,
                               "us_min_cold_l2": res["cold"][0],
                               "us_p90_cold_l2": res["cold"][int(0.9 * len(res["cold"]))],
+                              "cold_method": "512 MiB write, then 384 MiB read of another buffer",
+                              "us_median_cold_l2_dirty": res["cold_dirty"][len(res["cold_dirty"]) // 2],
+                              "frac_of_hbm_dirty": nbytes / (res["cold_dirty"][len(res["cold_dirty"]) // 2] * 1e-6) / 1e9 / float(peaks["hbm_gbs"]),
                               "us_median_warm_l2": res["warm"][len(res["warm"]) // 2],
                               "warm_method": "CUDA graph of 20 back-to-back calls, per call",
                               "us_host_per_eager_call": host_us,
