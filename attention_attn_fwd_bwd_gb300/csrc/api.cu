@@ -635,8 +635,17 @@ attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, v
   cudaStreamWaitEvent(hp->out, hp->start, 0);
   const size_t q_el = (size_t)Hq * N * d, kv_el = (size_t)Hkv * N * d, l_el = (size_t)Hq * N;
   const int TQ = (N + 127) / 128;
+  const int g = Hq / Hkv;
+  // With one batch element per chunk, each element is also split into hs groups of KV heads
+  // (contiguous in every array) until there are at least 8 chunks: the first chunk's copy-in
+  // and the last chunk's forward and copy-out, which nothing overlaps, shrink with the chunk.
+  int hs = 1;
+  if (chunk_b == 1)
+    while (B * hs < 8 && Hkv % (2 * hs) == 0) hs *= 2;
+  const int nh = Hkv / hs, qh = nh * g;  // KV and query heads of a chunk
   bool table_built = false;
-  for (int b0 = 0, ci = 0; b0 < B; b0 += chunk_b, ++ci) {
+  for (int ci = 0; ci * chunk_b < B * hs; ++ci) {
+    const int b0 = (ci / hs) * chunk_b, hg = ci % hs;
     const int cb = std::min(chunk_b, B - b0);
     const int bi = ci & 1;
     uint8_t* set = base + bi * (c.q + 2 * c.kv + c.o + c.l);
@@ -647,12 +656,16 @@ attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, v
     float* dlse = lse ? reinterpret_cast<float*>(set + c.q + 2 * c.kv + c.o) : nullptr;
     // copy-in once the forward two chunks back has read this buffer set
     if (ci >= 2) cudaStreamWaitEvent(hp->in, hp->fwd_done[bi], 0);
-    const size_t qb = (size_t)cb * q_el * 2, kvb = (size_t)cb * kv_el * 2;
-    e = cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + (size_t)b0 * q_el * 2, qb, cudaMemcpyHostToDevice, hp->in);
+    // elements before the chunk and in it (a chunk of several batch elements has hs = 1)
+    const size_t q0 = (size_t)b0 * q_el + (size_t)hg * qh * N * d;
+    const size_t k0 = (size_t)b0 * kv_el + (size_t)hg * nh * N * d;
+    const size_t l0 = (size_t)b0 * l_el + (size_t)hg * qh * N;
+    const size_t qb = (size_t)cb * qh * N * d * 2, kvb = (size_t)cb * nh * N * d * 2;
+    e = cudaMemcpyAsync(dq, static_cast<const uint8_t*>(q) + q0 * 2, qb, cudaMemcpyHostToDevice, hp->in);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + (size_t)b0 * kv_el * 2, kvb, cudaMemcpyHostToDevice, hp->in);
+      e = cudaMemcpyAsync(dk, static_cast<const uint8_t*>(k) + k0 * 2, kvb, cudaMemcpyHostToDevice, hp->in);
     if (e == cudaSuccess)
-      e = cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + (size_t)b0 * kv_el * 2, kvb, cudaMemcpyHostToDevice, hp->in);
+      e = cudaMemcpyAsync(dv, static_cast<const uint8_t*>(v) + k0 * 2, kvb, cudaMemcpyHostToDevice, hp->in);
     if (e != cudaSuccess) return cuda_fail(e, "copy-in");
     cudaEventRecord(hp->in_done[bi], hp->in);
     // the forward, once its inputs are in and this buffer set's output has been copied out
@@ -663,13 +676,15 @@ attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, v
       vc = *variant;
       if (vc.bias == ATTNFUSE_BIAS_ADDITIVE && vc.add_bias)
         vc.add_bias = static_cast<const uint8_t*>(vc.add_bias) +
-                      (size_t)b0 * vc.add_bias_strides[0] * (vc.add_bias_is_bf16 ? 2 : 4);
-      if (vc.tile_visits) vc.tile_visits += (size_t)b0 * Hq * TQ * TQ;
+                      ((size_t)b0 * vc.add_bias_strides[0] + (size_t)hg * qh * vc.add_bias_strides[1]) *
+                          (vc.add_bias_is_bf16 ? 2 : 4);
+      if (vc.bias == ATTNFUSE_BIAS_ALIBI && vc.alibi_slopes) vc.alibi_slopes += hg * qh;
+      if (vc.tile_visits) vc.tile_visits += ((size_t)b0 * Hq + (size_t)hg * qh) * TQ * TQ;
     }
-    const int64_t qs[4] = {(int64_t)q_el, (int64_t)N * d, d, 1};
-    const int64_t ks[4] = {(int64_t)kv_el, (int64_t)N * d, d, 1};
+    const int64_t qs[4] = {(int64_t)qh * N * d, (int64_t)N * d, d, 1};
+    const int64_t ks[4] = {(int64_t)nh * N * d, (int64_t)N * d, d, 1};
     const int mode = rope_mode | ((rope_mode != ATTNFUSE_ROPE_NONE && table_built) ? ATTNFUSE_ROPE_REUSE_TABLE : 0);
-    rc = attnfuse_fwd(dq, qs, dk, ks, dv, ks, dout, qs, dlse, cb, Hq, Hkv, N, d, scale, rope_theta,
+    rc = attnfuse_fwd(dq, qs, dk, ks, dv, ks, dout, qs, dlse, cb, qh, nh, N, d, scale, rope_theta,
                       static_cast<attnfuse_rope_mode>(mode), variant ? &vc : nullptr, fwd_ws, c.ws,
                       stream);
     if (rc) return rc;
@@ -677,14 +692,14 @@ attnfuse_status attnfuse_fwd_host(const void* q, const void* k, const void* v, v
     cudaEventRecord(hp->fwd_done[bi], stream);
     // copy-out
     cudaStreamWaitEvent(hp->out, hp->fwd_done[bi], 0);
-    e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + (size_t)b0 * q_el * 2, dout, qb, cudaMemcpyDeviceToHost, hp->out);
+    e = cudaMemcpyAsync(static_cast<uint8_t*>(out) + q0 * 2, dout, qb, cudaMemcpyDeviceToHost, hp->out);
     if (e == cudaSuccess && lse)
-      e = cudaMemcpyAsync(lse + (size_t)b0 * l_el, dlse, (size_t)cb * l_el * 4, cudaMemcpyDeviceToHost, hp->out);
+      e = cudaMemcpyAsync(lse + l0, dlse, (size_t)cb * qh * N * 4, cudaMemcpyDeviceToHost, hp->out);
     if (e != cudaSuccess) return cuda_fail(e, "copy-out");
     cudaEventRecord(hp->out_done[bi], hp->out);
   }
   // completion on the caller's stream: every copy-out has landed
-  const int nchunks = (B + chunk_b - 1) / chunk_b;
+  const int nchunks = (B + chunk_b - 1) / chunk_b * hs;
   for (int i = 0; i < std::min(nchunks, 2); ++i) cudaStreamWaitEvent(stream, hp->out_done[(nchunks - 1 - i) & 1], 0);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "host forward");
   return ok();

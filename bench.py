@@ -415,8 +415,9 @@ def run_ours(args, rank, world):
         e2e_ms = max_over_ranks(ev0.elapsed_time(ev1) / e2e_steps, dev)
         e2e = {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "api": f"attnfuse_fwd_host (pinned host buffers, batch chunks of {chunk_b}: "
-                      f"copy-in, forward and copy-out overlap)"}
+               "api": f"attnfuse_fwd_host (pinned host buffers, chunk_b={chunk_b}: chunks of one "
+                      f"batch element split into KV-head groups until there are 8; copy-in, "
+                      f"forward and copy-out overlap)"}
 
     if rank != 0:
         return

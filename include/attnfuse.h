@@ -185,9 +185,13 @@ attnfuse_status attnfuse_fwd(const void* q, const int64_t q_strides[4], const vo
  * creates once per device, the forwards on `stream`, ordered by events. The call returns after
  * queueing; the results are in out / lse once `stream` has reached this point (the copy-ins
  * start after the work queued on `stream` before the call). Other arguments as attnfuse_fwd
- * (no ATTNFUSE_ROPE_REUSE_TABLE: the first chunk builds the table, the others reuse it). The
- * variant's device arrays are indexed per chunk: an additive bias with a batch stride and
- * tile_visits are offset by the chunk's first batch element. workspace: device memory of
+ * (no ATTNFUSE_ROPE_REUSE_TABLE: the first chunk builds the table, the others reuse it). With
+ * chunk_b = 1 and fewer than 8 batch elements, each element is further split into groups of
+ * KV heads (with their query heads), halving while Hkv allows, until there are 8 chunks: the
+ * work that cannot overlap (the first copy-in, the last forward and copy-out) shrinks with
+ * the chunk. The variant's device arrays are indexed per chunk: an additive bias, the ALiBi
+ * slopes and tile_visits are offset by the chunk's first batch element and head. workspace:
+ * device memory of
  * attnfuse_fwd_host_workspace_size bytes (two chunk buffer sets and one forward workspace).
  * Calls on one device are serialised by a lock while they queue work.
  * ------------------------------------------------------------------------------------------ */

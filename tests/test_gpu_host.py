@@ -28,7 +28,7 @@ def _pinned(x):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("vname", ["causal", "window_100_c", "addbias_f32", "bs_64"])
+@pytest.mark.parametrize("vname", ["causal", "window_100_c", "addbias_f32", "addbias_bcast", "alibi", "bs_64"])
 @pytest.mark.parametrize("chunk_b", [1, 2])
 def test_host_forward_equals_device_forward(d, vname, chunk_b):
     dev = torch.device("cuda")
