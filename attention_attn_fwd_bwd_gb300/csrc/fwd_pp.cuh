@@ -1,4 +1,4 @@
-// Persistent forward attention for head dim 128 on CTA pairs with two query slots per CTA
+// Persistent forward attention for head dims 128 and 64 on CTA pairs with two query slots per CTA
 // (AttnFuse paper §4.1 fused RoPE, §2 online softmax, §3.1 combinators, §4.3 block skipping).
 //
 // A cluster of two CTAs (one per SM) walks a static list of work units. A unit is four
@@ -30,6 +30,8 @@
 //               14-15 slot 1); the keys come rotated (K') from a pass the host launches
 //               first. e4m3 inputs: V comes widened to bf16 from a pass the host launches
 //               first, and the scores run on kind::f8f6f4 MMAs
+// Registers: launched at 128 per thread, re-dealt with setmaxnreg to 72 (warps 0-3), 192
+// (softmax) and 56 (warps 12-15); at 176 for the softmax, ptxas spilled in its loop.
 // Every wait is bounded (see ptx.cuh).
 #pragma once
 #include <cuda.h>
